@@ -1,0 +1,271 @@
+"""fp64 CPU oracle for the AttnRes depth-wise aggregation.
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` may import this package. The CUDA
+library and its Python binding never import it, and it imports nothing from
+them: the two share no code. The one thing both sides use is the seeded input
+generator module, which holds none of the method's arithmetic.
+
+The arithmetic of one read lives in ``attnres_oracle.c`` (plain fp64 loops).
+This module adds the sequencing the pages describe on top of it:
+
+* ``full_read`` / ``full_pass``: Full AttnRes. Read r of a pass aggregates the
+  embedding and the r sublayer outputs before it (DepthBench reading notes,
+  section 2.3 "Full AttnRes", Appendix A; LLMRes blog, "Kimi AttnRes":
+  h_l = sum_{i=0}^{l-1} alpha_{i->l} v_i).
+* ``block_pass``: Block AttnRes by its plain definition (DepthBench reading
+  notes section 2.5; LLMRes blog "Block Attention Residuals"; datacamp
+  explainer "block attention residuals"): sublayer k in block n (0-based) with
+  in-block index j reads {embedding, b_1 .. b_n, P_k if j >= 1}, where b_m is
+  the plain sum of block m's member outputs and P_k the sum of the outputs of
+  the earlier sublayers of the current block. An empty running sum (j = 0) is
+  not a source. Sums are exact fp64 additions of the stored outputs.
+* ``block_stage1`` / ``block_merge`` / ``block_accumulate``: the per-operation
+  references for the two-stage computation (datacamp explainer, "two-stage
+  computation"), each written as the plain read over the source set the
+  operation stands for, not as the two-stage algorithm.
+
+parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
+(closed forms, invariants, hand-worked golden cases and an independent
+pure-Python brute force, ``oracle/bruteforce.py``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attnres_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+F32, BF16, F64 = 0, 1, 2
+
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile ``attnres_oracle.c`` into ``oracle/_build/liboracle.so``."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-shared", "-fPIC", "-Wall",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def load_library(path: str):
+    """Open an oracle shared library and declare its C signatures."""
+    lib = ctypes.CDLL(path)
+    lib.attnres_oracle_read.restype = ctypes.c_int
+    lib.attnres_oracle_read.argtypes = [
+        ctypes.c_int, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_int),
+        ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_double, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+        ctypes.c_void_p]
+    lib.attnres_oracle_threads.restype = ctypes.c_int
+    lib.attnres_oracle_threads.argtypes = []
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = load_library(build())
+    return _lib
+
+
+def threads() -> int:
+    """OpenMP threads one oracle call uses."""
+    return int(_load().attnres_oracle_threads())
+
+
+# ---------------------------------------------------------------- storage ----
+
+def as_stored(x):
+    """Return (contiguous numpy array, dtype tag) for a stored tensor.
+
+    Accepts numpy float32/float64 arrays, numpy uint16 arrays holding bf16 bit
+    patterns (tag must then be given by wrapping in ``Bf16Bits``), and CPU torch
+    tensors of dtype float32, float64 or bfloat16.
+    """
+    if isinstance(x, Bf16Bits):
+        return np.ascontiguousarray(x.bits, dtype=np.uint16), BF16
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach()
+            if x.device.type != "cpu":
+                raise ValueError("the oracle takes host tensors only")
+            if x.dtype == torch.bfloat16:
+                return np.ascontiguousarray(x.contiguous().view(torch.int16).numpy().view(np.uint16)), BF16
+            if x.dtype == torch.float32:
+                return np.ascontiguousarray(x.numpy()), F32
+            if x.dtype == torch.float64:
+                return np.ascontiguousarray(x.numpy()), F64
+            raise TypeError(f"unsupported tensor dtype {x.dtype}")
+    except ImportError:  # pragma: no cover - torch is always present here
+        pass
+    x = np.asarray(x)
+    if x.dtype == np.float32:
+        return np.ascontiguousarray(x), F32
+    if x.dtype == np.float64:
+        return np.ascontiguousarray(x), F64
+    raise TypeError(f"unsupported array dtype {x.dtype}")
+
+
+class Bf16Bits:
+    """A numpy uint16 array marked as holding bf16 bit patterns."""
+
+    def __init__(self, bits):
+        self.bits = np.asarray(bits, dtype=np.uint16)
+        self.shape = self.bits.shape
+
+
+def widen(x) -> np.ndarray:
+    """Exact fp64 copy of a stored tensor (bf16 widened bit-exactly)."""
+    arr, tag = as_stored(x)
+    if tag == BF16:
+        return (arr.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return arr.astype(np.float64)
+
+
+# ------------------------------------------------------------------ reads ----
+
+def read(sources, w, gamma, eps, rows=None):
+    """One AttnRes read over ``sources`` (each a stored [T, d] tensor).
+
+    Returns ``(out, lse)``: fp64 [n_rows, d] and fp64 [n_rows]. ``rows`` picks
+    token rows (default: all T).
+    """
+    if len(sources) < 1:
+        raise ValueError("a read needs at least one source")
+    arrs = [as_stored(s) for s in sources]
+    T, d = arrs[0][0].shape
+    for a, _ in arrs:
+        if a.shape != (T, d):
+            raise ValueError("all sources of a read must be [T, d]")
+    w64 = np.ascontiguousarray(np.asarray(w, dtype=np.float64).reshape(d))
+    g64 = np.ascontiguousarray(np.asarray(gamma, dtype=np.float64).reshape(d))
+    rows64 = np.arange(T, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    n_rows = rows64.shape[0]
+    out = np.empty((n_rows, d), dtype=np.float64)
+    lse = np.empty((n_rows,), dtype=np.float64)
+    n = len(arrs)
+    bases = (ctypes.c_void_p * n)(*[a.ctypes.data for a, _ in arrs])
+    tags = (ctypes.c_int * n)(*[t for _, t in arrs])
+    rc = _load().attnres_oracle_read(
+        n, bases, tags, T, d, w64.ctypes.data, g64.ctypes.data, float(eps),
+        rows64.ctypes.data if n_rows else None, n_rows,
+        out.ctypes.data if n_rows else None, lse.ctypes.data if n_rows else None)
+    if rc != 0:
+        raise ValueError(f"attnres_oracle_read failed with code {rc}")
+    return out, lse
+
+
+def _slices(V, n):
+    if isinstance(V, Bf16Bits):
+        return [Bf16Bits(V.bits[i]) for i in range(n)]
+    return [V[i] for i in range(n)]
+
+
+def full_read(V, n_src, w, gamma, eps, rows=None):
+    """Full AttnRes read over the first ``n_src`` entries of history V[n, T, d]."""
+    return read(_slices(V, n_src), w, gamma, eps, rows)
+
+
+def full_pass(V, R, W, Gamma, eps, rows=None):
+    """Full AttnRes pass: read r (0 <= r < R) aggregates V[0 .. r].
+
+    Returns fp64 [R, n_rows, d]. Sublayer r's own output is V[r + 1], so read r
+    sees the embedding and every earlier sublayer output, as in the pages'
+    h_l = sum_{i<l} alpha_{i->l} v_i.
+    """
+    outs = []
+    for r in range(R):
+        o, _ = full_read(V, r + 1, W[r], Gamma[r], eps, rows)
+        outs.append(o)
+    return np.stack(outs)
+
+
+def block_sources(k, S, emb64, F64):
+    """Source list of sublayer k of a Block AttnRes pass (all fp64, [rows, d]).
+
+    k is the 0-based global sublayer index, S the sublayers per block;
+    F64[q] is sublayer q's output. Returns [embedding, b_1 .. b_n] plus the
+    running sum of the current block when it is non-empty.
+    """
+    n, j = divmod(k, S)
+    srcs = [emb64]
+    for m in range(1, n + 1):
+        srcs.append(np.sum(F64[(m - 1) * S: m * S], axis=0))
+    if j >= 1:
+        srcs.append(np.sum(F64[n * S: k], axis=0))
+    return srcs
+
+
+def block_pass(emb, F, N, S, W, Gamma, eps, rows=None):
+    """Block AttnRes pass over N blocks of S sublayers, by definition.
+
+    emb: stored [T, d]; F: stored [N*S, T, d] sublayer outputs (F[q] is the
+    output of sublayer q and only feeds reads of later sublayers).
+    Returns fp64 [N*S, n_rows, d].
+    """
+    e64 = widen(emb)
+    f64 = widen(F)
+    T = e64.shape[0]
+    sel = np.arange(T, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    e64 = np.ascontiguousarray(e64[sel])
+    f64 = np.ascontiguousarray(f64[:, sel])
+    outs = []
+    for k in range(N * S):
+        srcs = [np.ascontiguousarray(s) for s in block_sources(k, S, e64, f64)]
+        o, _ = read(srcs, W[k], Gamma[k], eps)
+        outs.append(o)
+    return np.stack(outs)
+
+
+def block_stage1(Src, n_src, W, Gamma, eps, rows=None):
+    """Stage-1 reference: for each of the S queries, the read over Src[0 .. n_src).
+
+    Returns (O fp64 [S, n_rows, d], lse fp64 [S, n_rows]), O normalised.
+    """
+    outs, lses = [], []
+    for j in range(len(W)):
+        o, l = full_read(Src, n_src, W[j], Gamma[j], eps, rows)
+        outs.append(o)
+        lses.append(l)
+    return np.stack(outs), np.stack(lses)
+
+
+def block_accumulate(P, f, first):
+    """Running sum update P + f (or f alone when the running sum is empty)."""
+    f64 = widen(f)
+    return f64 if first else widen(P) + f64
+
+
+def block_merge(Src, n_src, P, f_prev, p_is_empty, w, gamma, eps, rows=None):
+    """Stage-2 reference: the read over {Src[0 .. n_src), P_new}.
+
+    P_new = P + f_prev (f_prev may be None: P_new = P; p_is_empty: P_new =
+    f_prev). Returns (out fp64 [n_rows, d], P_new fp64 [T, d]).
+    """
+    if f_prev is None:
+        if p_is_empty:
+            raise ValueError("an empty running sum with no f_prev has no source")
+        p_new = widen(P)
+    else:
+        p_new = block_accumulate(P, f_prev, p_is_empty)
+    srcs = _slices(Src, n_src) + [np.ascontiguousarray(p_new)]
+    out, _ = read(srcs, w, gamma, eps, rows)
+    return out, p_new

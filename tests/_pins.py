@@ -1,0 +1,271 @@
+"""Pins of the fp64 oracle: checks fixed by the pages and by mathematics.
+
+Each check takes the oracle module and raises AssertionError when the oracle
+disagrees with something that does not come from the oracle itself: a
+hand-worked golden case, a closed form, an invariant of the definition, or the
+independent pure-Python brute force. ``test_oracle_pins.py`` runs them against
+the oracle; ``test_oracle_mutants.py`` runs them against oracles with planted
+mistakes and requires each mistake to be caught.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+
+import numpy as np
+
+from oracle import bruteforce
+from tests._golden import load_cases
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _close(a, b, tol, what):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} != {b.shape}"
+    err = float(np.max(np.abs(a - b))) if a.size else 0.0
+    assert err <= tol, f"{what}: max abs error {err:.3e} > {tol:.1e}"
+
+
+# ------------------------------------------------------------------ golden ----
+
+def pin_golden(orc):
+    """Hand-worked reads (tests/golden/worked_examples.txt)."""
+    for c in load_cases():
+        d = c["d"]
+        if c["kind"] == "full":
+            srcs = [np.asarray(s, dtype=np.float64).reshape(1, d) for s in c["src"]]
+            out, _ = orc.read(srcs, c["w"][0], c["gamma"], c["eps"])
+            _close(out[0], c["expect"][0], c["tol"], c["name"])
+        else:
+            N, S = c["N"], c["S"]
+            emb = np.asarray(c["src"][0], dtype=np.float64).reshape(1, d)
+            F = np.asarray(c["src"][1:], dtype=np.float64).reshape(N * S, 1, d)
+            W = (np.tile(np.asarray(c["w_all"]), (N * S, 1)) if c["w_all"] is not None
+                 else c["w"])
+            G = np.tile(c["gamma"], (N * S, 1))
+            out = orc.block_pass(emb, F, N, S, W, G, c["eps"])
+            _close(out[:, 0, :], c["expect"], c["tol"], c["name"])
+
+
+def pin_bf16_widening(orc):
+    """bf16 storage is widened exactly: a single-source read returns it."""
+    bits = np.array([0x3F80, 0xC000, 0x4049, 0x0001, 0x7F7F, 0x8000, 0x3EAB, 0xBF00],
+                    dtype=np.uint16)
+    expect = np.array([1.0, -2.0, 3.140625, 2.0 ** -133, 3.3895313892515355e38,
+                       -0.0, 0.333984375, -0.5])
+    src = orc.Bf16Bits(bits.reshape(1, 8))
+    out, _ = orc.read([src], np.zeros(8), np.ones(8), 1e-6)
+    assert np.array_equal(out[0], expect), f"bf16 widening: {out[0]} != {expect}"
+    assert np.array_equal(orc.widen(src)[0], expect)
+
+
+# ------------------------------------------------------------ closed forms ----
+
+def pin_zero_query_is_mean(orc):
+    """w = 0 gives the uniform mean of the sources (all pages: zero-init query)."""
+    r = _rng(1)
+    for n, T, d in [(1, 3, 5), (4, 6, 7), (9, 2, 16)]:
+        V = r.standard_normal((n, T, d)) * np.sqrt(np.arange(1, n + 1))[:, None, None]
+        out, lse = orc.full_read(V, n, np.zeros(d), r.standard_normal(d), 1e-6)
+        _close(out, V.mean(axis=0), 1e-13, f"zero query mean n={n}")
+        _close(lse, np.full(T, math.log(n)), 1e-13, "zero query lse = log n")
+
+
+def pin_single_source_identity(orc):
+    """One source (the first sublayer reads the embedding) returns it unchanged."""
+    r = _rng(2)
+    V = r.standard_normal((1, 5, 11)) * 3.0
+    w = r.standard_normal(11)
+    out, _ = orc.full_read(V, 1, w, np.ones(11), 1e-6)
+    assert np.array_equal(out, V[0]), "single-source read must be the identity"
+
+
+def pin_two_sources_logistic(orc):
+    """d = 1, eps = 0: scores are +-w*gamma, so a_1 = 1/(1+exp(2 w gamma))."""
+    r = _rng(3)
+    for _ in range(8):
+        x, y = abs(r.standard_normal()) + 0.1, -abs(r.standard_normal()) - 0.1
+        w, g = r.standard_normal(), abs(r.standard_normal()) + 0.5
+        a1 = 1.0 / (1.0 + math.exp(2.0 * w * g))
+        srcs = [np.array([[x]]), np.array([[y]])]
+        out, lse = orc.read(srcs, [w], [g], 0.0)
+        _close(out[0, 0], (1 - a1) * x + a1 * y, 1e-14, "two-source logistic")
+        _close(lse[0], math.log(math.exp(w * g) + math.exp(-w * g)), 1e-14, "two-source lse")
+
+
+def pin_equal_sources(orc):
+    """All sources equal: the read returns that source for any w."""
+    r = _rng(4)
+    v = r.standard_normal((3, 9))
+    out, _ = orc.read([v] * 5, r.standard_normal(9) * 4, r.standard_normal(9), 1e-6)
+    _close(out, v, 1e-14, "equal sources")
+
+
+def pin_hardmax_limit(orc):
+    """Large w: the read tends to the source with the largest score.
+
+    d = 2, w = lambda * (1, 0), gamma = 1, eps = 0: the score of
+    v = rho * (cos t, sin t) is lambda * sqrt(2) * cos t, whatever rho is; the
+    source with the smallest |t| wins. Sources are built so that index 3 wins.
+    """
+    angles = [1.2, -0.9, 0.7, 0.05, -0.4, 2.5]
+    radii = [5.0, 0.3, 2.0, 0.7, 9.0, 1.0]
+    srcs = [np.array([[rho * math.cos(t), rho * math.sin(t)]]) for t, rho in zip(angles, radii)]
+    out, _ = orc.read(srcs, [300.0, 0.0], [1.0, 1.0], 0.0)
+    _close(out[0], srcs[3][0], 1e-12, "hardmax limit picks the largest score")
+
+
+# --------------------------------------------------------------- invariants ----
+
+def pin_permutation_invariance(orc):
+    """The read is a sum over the source set: order does not matter."""
+    r = _rng(5)
+    n, T, d = 6, 4, 10
+    V = r.standard_normal((n, T, d)) * np.arange(1, n + 1)[:, None, None]
+    w, g = r.standard_normal(d) * 0.5, r.standard_normal(d)
+    base, lb = orc.full_read(V, n, w, g, 1e-6)
+    for p in [r.permutation(n) for _ in range(4)]:
+        out, lse = orc.full_read(V[p], n, w, g, 1e-6)
+        _close(out, base, 1e-13, "permutation invariance")
+        _close(lse, lb, 1e-13, "permutation invariance (lse)")
+
+
+def pin_key_scale_invariance(orc):
+    """eps = 0: scaling a source changes its value but not its score.
+
+    The read is then affine in the scale c of one source:
+    z(c) = A + a_i * c * v_i with a_i independent of c.
+    """
+    r = _rng(6)
+    n, T, d = 4, 3, 8
+    V = r.standard_normal((n, T, d))
+    w, g = r.standard_normal(d), r.standard_normal(d)
+    outs = {}
+    for c in (0.5, 2.0, 7.0):
+        Vc = V.copy()
+        Vc[2] *= c
+        outs[c], _ = orc.full_read(Vc, n, w, g, 0.0)
+    lhs = outs[7.0] - outs[0.5]
+    rhs = (7.0 - 0.5) / (2.0 - 0.5) * (outs[2.0] - outs[0.5])
+    _close(lhs, rhs, 1e-12, "score independent of the source scale")
+    full_scaled, _ = orc.full_read(3.5 * V, n, w, g, 0.0)
+    base, _ = orc.full_read(V, n, w, g, 0.0)
+    _close(full_scaled, 3.5 * base, 1e-12, "scaling every source scales the read")
+
+
+def pin_split_merge(orc):
+    """Two parts merged by log-sum-exp equal the read over their union.
+
+    This is the identity the two-stage Block AttnRes computation relies on
+    (datacamp explainer, "two-stage computation": online-softmax merge).
+    """
+    r = _rng(7)
+    n, T, d = 7, 5, 12
+    V = r.standard_normal((n, T, d)) * 2
+    w, g = r.standard_normal(d), r.standard_normal(d) + 1
+    oa, la = orc.read([V[i] for i in range(3)], w, g, 1e-6)
+    ob, lb = orc.read([V[i] for i in range(3, n)], w, g, 1e-6)
+    ou, lu = orc.read([V[i] for i in range(n)], w, g, 1e-6)
+    m = np.maximum(la, lb)
+    ea, eb = np.exp(la - m), np.exp(lb - m)
+    merged = (oa * ea[:, None] + ob * eb[:, None]) / (ea + eb)[:, None]
+    _close(merged, ou, 1e-13, "split/merge = union")
+    _close(np.logaddexp(la, lb), lu, 1e-13, "lse of the union")
+
+
+def pin_block_s1_equals_full(orc):
+    """Block AttnRes with one sublayer per block is Full AttnRes."""
+    r = _rng(8)
+    L, T, d = 6, 3, 5
+    emb = r.standard_normal((T, d))
+    F = r.standard_normal((L, T, d)) * 1.5
+    W, G = r.standard_normal((L, d)), r.standard_normal((L, d))
+    blk = orc.block_pass(emb, F, L, 1, W, G, 1e-6)
+    hist = np.concatenate([emb[None], F[:-1]], axis=0)
+    full = orc.full_pass(hist, L, W, G, 1e-6)
+    _close(blk, full, 1e-13, "Block S=1 == Full")
+
+
+def pin_block_zero_query_means(orc):
+    """w = 0: each block read is the mean of its source set (written out here)."""
+    r = _rng(9)
+    N, S, T, d = 3, 4, 2, 3
+    emb = r.standard_normal((T, d))
+    F = r.standard_normal((N * S, T, d))
+    out = orc.block_pass(emb, F, N, S, np.zeros((N * S, d)), np.ones((N * S, d)), 1e-6)
+    for k in range(N * S):
+        n, j = divmod(k, S)
+        total = emb.copy()
+        count = 1
+        for m in range(n):                       # completed blocks 1..n
+            total = total + sum(F[m * S + q] for q in range(S))
+            count += 1
+        if j > 0:                                # non-empty running sum
+            total = total + sum(F[n * S + q] for q in range(j))
+            count += 1
+        _close(out[k], total / count, 1e-13, f"block mean at sublayer {k}")
+
+
+def pin_stage1_and_merge_reference(orc):
+    """Per-operation references agree with the block definition."""
+    r = _rng(10)
+    N, S, T, d = 3, 3, 4, 6
+    emb = r.standard_normal((T, d))
+    F = r.standard_normal((N * S, T, d))
+    W, G = r.standard_normal((N * S, d)), r.standard_normal((N * S, d))
+    full = orc.block_pass(emb, F, N, S, W, G, 1e-6)
+    n = 2                                          # block index (0-based)
+    Src = np.stack([emb, F[0:S].sum(0), F[S:2 * S].sum(0)])
+    O, lse = orc.block_stage1(Src, n + 1, W[n * S:(n + 1) * S], G[n * S:(n + 1) * S], 1e-6)
+    _close(O[0], full[n * S], 1e-13, "stage 1, first sublayer of a block")
+    P = None
+    for j in range(1, S):
+        out, P = orc.block_merge(Src, n + 1, P, F[n * S + j - 1], P is None,
+                                 W[n * S + j], G[n * S + j], 1e-6)
+        _close(out, full[n * S + j], 1e-13, f"merge at in-block index {j}")
+
+
+# --------------------------------------------------------------- brute force ----
+
+def pin_bruteforce(orc):
+    """Independent pure-Python fsum brute force on tiny shapes, all orders."""
+    r = _rng(11)
+    for n, T, d in [(1, 2, 1), (2, 3, 2), (3, 2, 3), (4, 1, 4), (5, 2, 3)]:
+        V = r.standard_normal((n, T, d)) * np.arange(1, n + 1)[:, None, None]
+        w, g = r.standard_normal(d), r.standard_normal(d)
+        for perm in itertools.permutations(range(n)):
+            out, lse = orc.full_read(V[list(perm)], n, w, g, 1e-3)
+            for t in range(T):
+                z, l = bruteforce.read([list(V[i, t]) for i in perm], list(w), list(g), 1e-3)
+                _close(out[t], z, 1e-12, f"brute force read n={n}")
+                _close(lse[t], l, 1e-12, f"brute force lse n={n}")
+    # Full pass and every block size dividing the sublayer count.
+    L, T, d = 6, 2, 3
+    emb = r.standard_normal((T, d))
+    F = r.standard_normal((L, T, d))
+    W, G = r.standard_normal((L, d)) * 2, r.standard_normal((L, d))
+    hist = np.concatenate([emb[None], F[:-1]])
+    fp = orc.full_pass(hist, L, W, G, 1e-6)
+    for S in [s for s in range(1, L + 1) if L % s == 0]:
+        bp = orc.block_pass(emb, F, L // S, S, W, G, 1e-6)
+        for t in range(T):
+            ref = bruteforce.block_pass(list(emb[t]), [list(F[q, t]) for q in range(L)], S,
+                                        [list(x) for x in W], [list(x) for x in G], 1e-6)
+            _close(bp[:, t, :], ref, 1e-12, f"brute force block S={S}")
+    for t in range(T):
+        ref = bruteforce.full_pass([list(hist[i, t]) for i in range(L)],
+                                   [list(x) for x in W], [list(x) for x in G], 1e-6)
+        _close(fp[:, t, :], ref, 1e-12, "brute force full pass")
+
+
+ALL_PINS = [
+    pin_golden, pin_bf16_widening, pin_zero_query_is_mean, pin_single_source_identity,
+    pin_two_sources_logistic, pin_equal_sources, pin_hardmax_limit,
+    pin_permutation_invariance, pin_key_scale_invariance, pin_split_merge,
+    pin_block_s1_equals_full, pin_block_zero_query_means, pin_stage1_and_merge_reference,
+    pin_bruteforce,
+]

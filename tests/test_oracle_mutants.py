@@ -1,0 +1,86 @@
+"""Planted mistakes in the oracle must each be caught by a pin (CPU only).
+
+Every mutant is a copy of the oracle with one plausible error: a dropped or
+misplaced term, a wrong sign or index, a wrong source set for Block AttnRes.
+The pins in tests/_pins.py are run against the mutant; at least one must fail.
+"""
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import _pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "attnres_oracle.c")
+
+C_MUTANTS = {
+    "eps_outside_root": ("1.0 / sqrt(sq / (double)d + eps)", "1.0 / (sqrt(sq / (double)d) + eps)"),
+    "sum_not_mean": ("sqrt(sq / (double)d + eps)", "sqrt(sq + eps)"),
+    "no_key_rmsnorm": ("double inv_rms = 1.0 / sqrt(sq / (double)d + eps);", "double inv_rms = 1.0; (void)sq;"),
+    "no_gain": ("w[k] * (gamma[k] * v[i][k] * inv_rms)", "w[k] * (v[i][k] * inv_rms)"),
+    "negated_score": ("e[i] = dot;", "e[i] = -dot;"),
+    "sqrt_d_scale": ("e[i] = dot;", "e[i] = dot / sqrt((double)d);"),
+    "gain_on_values": ("out[k] += a * v[i][k];", "out[k] += a * gamma[k] * v[i][k];"),
+    "reversed_query": ("w[k] * (gamma[k]", "w[d - 1 - k] * (gamma[k]"),
+    "unnormalised_weights": ("double a = exp(e[i] - m) / z;", "double a = exp(e[i] - m);"),
+    "lse_without_max": ("*lse = m + log(z);", "*lse = log(z);"),
+    "bf16_shift": ("<< 16;", "<< 15;"),
+    "first_source_dropped": ("for (int i = 0; i < n; ++i) {\n    double a", "for (int i = 1; i < n; ++i) {\n    double a"),
+}
+
+
+def _run_pins(orc):
+    failures = []
+    for pin in _pins.ALL_PINS:
+        try:
+            pin(orc)
+        except Exception as exc:  # any failure counts as caught
+            failures.append((pin.__name__, repr(exc)[:120]))
+    return failures
+
+
+@pytest.mark.parametrize("name", sorted(C_MUTANTS))
+def test_c_mutant_is_caught(name, tmp_path, monkeypatch):
+    old, new = C_MUTANTS[name]
+    text = open(SRC).read()
+    assert old in text, f"mutation site for {name} not found"
+    src = tmp_path / "mutant.c"
+    src.write_text(text.replace(old, new))
+    lib_path = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-shared", "-fPIC", "-o",
+                    str(lib_path), str(src), "-lm"], check=True)
+    monkeypatch.setattr(oracle, "_lib", oracle.load_library(str(lib_path)))
+    assert _run_pins(oracle), f"mutant {name} passed every pin"
+
+
+def _block_mutant(kind):
+    def sources(k, S, emb64, F64):
+        n, j = divmod(k, S)
+        zero = np.zeros_like(emb64)
+        srcs = [emb64]
+        for m in range(1, n + 1):
+            b = np.sum(F64[(m - 1) * S: m * S], axis=0)
+            if kind == "summary_is_mean":
+                b = b / S
+            if kind == "embedding_in_first_block" and m == 1:
+                b = b + emb64
+            srcs.append(b)
+        if kind == "one_block_short" and n >= 1:
+            srcs.pop()
+        if kind == "running_sum_as_zero_when_empty" and j == 0:
+            srcs.append(zero)
+        if j >= 1 and kind != "no_running_sum":
+            hi = k + 1 if kind == "running_sum_includes_self" else k
+            srcs.append(np.sum(F64[n * S: hi], axis=0))
+        return srcs
+    return sources
+
+
+@pytest.mark.parametrize("kind", ["summary_is_mean", "embedding_in_first_block",
+                                  "one_block_short", "running_sum_as_zero_when_empty",
+                                  "no_running_sum", "running_sum_includes_self"])
+def test_block_mutant_is_caught(kind, monkeypatch, oracle_mod):
+    monkeypatch.setattr(oracle, "block_sources", _block_mutant(kind))
+    assert _run_pins(oracle), f"block mutant {kind} passed every pin"
