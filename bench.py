@@ -1,0 +1,494 @@
+"""Benchmark of the AttnRes depth-wise aggregation on GB300.
+
+One step = one pass of the aggregation hot path over one batch of synthetic
+inputs already resident in HBM. The default workload is the Full AttnRes pass
+of the 400M model at its 32-layer shape: 64 sublayer reads, read r aggregating
+the embedding and the r earlier outputs, d = 896, T = 4 x 2048 tokens, bf16
+storage with fp32 arithmetic. The Block AttnRes pass (8 blocks of 8, d = 1024,
+T = 16384) is measured in the same run and reported under "block".
+
+Prints one JSON line (rank 0). Metric: tokens/s (higher is better), with the
+HBM roofline of the dominant kernel. ``--impl reference`` times the fp64 CPU
+oracle on the same workload instead (a bounded sample of token rows per step).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload NAME]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from depth_wise_attention_attnres_gb300 import inputs  # noqa: E402
+
+METRIC = "AttnRes aggregation tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+DEFAULT_WORKLOAD = "full_pass_64x8192x896_bf16"
+BLOCK_WORKLOAD = "block_pass_8x8x16384x1024_bf16"
+
+
+# ----------------------------------------------------------------- bytes ----
+
+def full_pass_bytes(R: int, T: int, d: int, es: int) -> int:
+    """Algorithmic bytes of a Full pass: read r moves r+1 source rows and
+    writes one output row per token: sum_r (r + 2) * T * d * es."""
+    return sum(r + 2 for r in range(R)) * T * d * es
+
+
+def block_pass_bytes(N: int, S: int, T: int, d: int, es: int, freeze_last: bool = False) -> dict:
+    """Algorithmic bytes per kernel of the two-stage Block pass.
+
+    stage 1 of block n (n+1 sources): reads (n+1) rows, writes S output rows
+    and S lse values per token. Merge j=1: reads O_j and f (P empty), writes P
+    and out. Merge j>=2: also reads P. Freeze: reads P and f, writes b.
+    """
+    E = T * d
+    st1 = merge = freeze = 0
+    for n in range(N):
+        st1 += (n + 1) * E * es + S * E * es + S * T * 4
+        for j in range(1, S):
+            merge += 2 * E * es + T * 4 + 4 * E + E * es + (4 * E if j >= 2 else 0)
+        if n + 1 < N or freeze_last:
+            freeze += (4 * E if S > 1 else 0) + E * es + E * es
+    return {"stage1": st1, "merge": merge, "freeze": freeze, "total": st1 + merge + freeze}
+
+
+# ---------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self) -> dict:
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- peaks ----
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# DRAM traffic per launch unit from an ncu capture, keyed by the sha256 of the
+# kernel source it was taken with (reported as null once the source changes).
+NCU_TRAFFIC = {}
+
+
+def kernel_digest(name: str) -> str:
+    path = os.path.join(ROOT, "depth_wise_attention_attnres_gb300", "csrc", name)
+    with open(path, "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+# ------------------------------------------------------------ distributed ----
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], device="cuda", dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- our arm ----
+
+class FullPassStep:
+    def __init__(self, wl, dev):
+        from depth_wise_attention_attnres_gb300 import binding
+        self.ar = binding
+        self.wl = wl
+        self.V, self.W, self.G = inputs.full_inputs(wl, dev)
+        self.out = torch.empty(wl.R, wl.T, wl.d, device=dev, dtype=inputs.DTYPES[wl.dtype])
+        self.launches = wl.R
+        es = 2 if wl.dtype == "bf16" else 4
+        self.bytes = full_pass_bytes(wl.R, wl.T, wl.d, es)
+
+    def __call__(self):
+        self.ar.attnres_full_pass(self.V, self.W, self.G, self.wl.eps, self.out)
+
+
+class BlockPassStep:
+    def __init__(self, wl, dev):
+        from depth_wise_attention_attnres_gb300 import binding
+        self.ar = binding
+        self.wl = wl
+        dt = inputs.DTYPES[wl.dtype]
+        emb, self.F, self.W, self.G = inputs.block_inputs(wl, dev)
+        self.Src = torch.empty(wl.N, wl.T, wl.d, device=dev, dtype=dt)
+        self.Src[0].copy_(emb)
+        del emb
+        self.O = torch.empty(max(wl.S - 1, 1), wl.T, wl.d, device=dev, dtype=dt)
+        self.lse = torch.empty(wl.S, wl.T, device=dev)
+        self.P = torch.empty(wl.T, wl.d, device=dev)
+        self.out = torch.empty(wl.N * wl.S, wl.T, wl.d, device=dev, dtype=dt)
+        self.launches = wl.N + wl.N * (wl.S - 1) + (wl.N - 1)
+        es = 2 if wl.dtype == "bf16" else 4
+        self.byte_parts = block_pass_bytes(wl.N, wl.S, wl.T, wl.d, es)
+        self.bytes = self.byte_parts["total"]
+
+    def __call__(self):
+        self.ar.attnres_block_pass(self.F, self.wl.N, self.wl.S, self.W, self.G, self.wl.eps,
+                                   self.Src, self.O, self.lse, self.P, self.out)
+
+
+def make_step(name, dev):
+    wl = inputs.WORKLOADS[name]
+    if wl.kind == "full_pass":
+        return FullPassStep(wl, dev)
+    if wl.kind == "block_pass":
+        return BlockPassStep(wl, dev)
+    raise ValueError(f"{name} is a parity case, not a benchmark workload")
+
+
+def time_graph(step, steps, warmup, world, stream):
+    """Capture one step in a CUDA graph; time `steps` replays with events."""
+    with torch.cuda.stream(stream):
+        step()  # first call outside capture (one-time attribute setup)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = start.elapsed_time(end) / steps
+    return ms, graph
+
+
+def time_block_kernels(step, reps, stream):
+    """Per-kernel device time of the Block pass (events around each launch)."""
+    ar, wl = step.ar, step.wl
+    T, d = wl.T, wl.d
+    acc = {"stage1": 0.0, "merge": 0.0, "freeze": 0.0}
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    marks = []
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            for n in range(wl.N):
+                k0 = n * wl.S
+                O = [step.out[k0]] + [step.O[j - 1] for j in range(1, wl.S)]
+                a, b = ev(), ev()
+                a.record(stream)
+                ar.attnres_block_stage1(step.Src, n + 1, step.W[k0:k0 + wl.S], step.G[k0:k0 + wl.S],
+                                        wl.eps, O, step.lse, stream=stream)
+                b.record(stream)
+                marks.append(("stage1", a, b))
+                for j in range(1, wl.S):
+                    a, b = ev(), ev()
+                    a.record(stream)
+                    ar.attnres_block_merge(step.O[j - 1], step.lse[j], step.P, step.F[k0 + j - 1], j == 1,
+                                           step.W[k0 + j], step.G[k0 + j], wl.eps, step.out[k0 + j],
+                                           stream=stream)
+                    b.record(stream)
+                    marks.append(("merge", a, b))
+                if n + 1 < wl.N:
+                    a, b = ev(), ev()
+                    a.record(stream)
+                    ar.attnres_block_summary_accumulate(step.P, step.F[k0 + wl.S - 1], wl.S == 1,
+                                                        step.Src[n + 1], stream=stream)
+                    b.record(stream)
+                    marks.append(("freeze", a, b))
+    torch.cuda.synchronize()
+    for kind, a, b in marks:
+        acc[kind] += a.elapsed_time(b)
+    return {k: v / reps for k, v in acc.items()}
+
+
+def run_e2e(step, steps, warmup, stream):
+    """Same metric through the public API with host buffers: H2D of the step's
+    inputs from pinned memory, the pass, D2H of the outputs, all timed."""
+    if isinstance(step, BlockPassStep):
+        dev_inputs = [step.F, step.W, step.G, step.Src[0]]
+    else:
+        dev_inputs = [step.V, step.W, step.G]
+    host_inputs = [t.cpu().pin_memory() for t in dev_inputs]
+    host_out = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_inputs)
+    d2h = host_out.numel() * host_out.element_size()
+
+    def once():
+        for h, dptr in zip(host_inputs, dev_inputs):
+            dptr.copy_(h, non_blocking=True)
+        step()
+        host_out.copy_(step.out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            once()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            once()
+        end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps, h2d, d2h
+
+
+def cpu_baseline(name, target_s=12.0):
+    """The fp64 oracle, as it stands, on a bounded sample of token rows."""
+    import oracle
+    oracle.build()
+    wl = inputs.WORKLOADS[name]
+    if wl.kind == "full_pass":
+        V, W, G = inputs.full_inputs(wl, "cpu")
+        W64, G64 = W.double(), G.double()
+
+        def run(rows):
+            oracle.full_pass(V, wl.R, W64, G64, wl.eps, rows)
+    else:
+        emb, F, W, G = inputs.block_inputs(wl, "cpu")
+        W64, G64 = W.double(), G.double()
+
+        def run(rows):
+            oracle.block_pass(emb[rows], F[:, rows, :], wl.N, wl.S, W64, G64, wl.eps)
+    probe = inputs.sample_rows(wl.T, 16)
+    t0 = time.perf_counter()
+    run(probe)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    nrows = int(min(wl.T, max(16, 16 * target_s / dt)))
+    rows = inputs.sample_rows(wl.T, nrows)
+    t0 = time.perf_counter()
+    run(rows)
+    dt = time.perf_counter() - t0
+    return {"value": len(rows) / dt, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{len(rows)} of {wl.T} token rows (stride-sampled) of {name}, fp64, "
+                      f"{dt:.1f} s; tokens are independent so tokens/s scales"}, (run, rows)
+
+
+def ours(args):
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    barrier(world)
+    __graft_entry__.build()
+    peaks = measured_peaks()
+    stream = torch.cuda.Stream(device=dev)
+    wl = inputs.WORKLOADS[args.workload]
+    step = make_step(args.workload, dev)
+
+    with ClockSampler(local) as clocks:
+        ms, graph = time_graph(step, args.steps, args.warmup, world, stream)
+    ms = max_over_ranks(ms, world)
+    tokens = wl.T * world
+    value = tokens / (ms / 1e3)
+    gbs = step.bytes / (ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "kind": wl.kind, "T": wl.T, "d": wl.d,
+                   "reads" if wl.kind == "full_pass" else "blocks": wl.R if wl.kind == "full_pass" else wl.N,
+                   **({"S": wl.S} if wl.kind == "block_pass" else {}),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (129 MB); no flush",
+                   "timing": "CUDA graph of one step, CUDA events on the launching stream"},
+        "algorithmic_gbs": gbs,
+        "gpu_launches": step.launches * args.steps,
+    }
+    del graph
+    torch.cuda.synchronize()
+
+    if wl.kind == "full_pass":
+        digest = kernel_digest("full_fwd.cu")
+        traffic = NCU_TRAFFIC.get(("full_fwd_bulk_kernel", digest))
+        line["roofline"] = {
+            "kernel": "full_fwd_bulk_kernel", "bound": "hbm", "achieved": gbs,
+            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+            "peak_source": peaks["source"],
+            "traffic": None if traffic is None else traffic * step.bytes / step.launches,
+            "per_launch_bytes": step.bytes / step.launches,
+            "note": "the step is R launches of this one kernel back to back in a CUDA graph; "
+                    "average launch duration = step time / R (gaps included)"}
+    else:
+        times = time_block_kernels(step, 3, stream)
+        parts = step.byte_parts
+        kernels = {k: {"ms": times[k], "gbs": parts[k] / (times[k] / 1e3) / 1e9 if times[k] else None}
+                   for k in ("stage1", "merge", "freeze")}
+        top = max(kernels, key=lambda k: kernels[k]["ms"])
+        g = kernels[top]["gbs"]
+        line["roofline"] = {
+            "kernel": {"stage1": "stage1_kernel", "merge": "merge_fast_kernel",
+                       "freeze": "accum_fast_kernel"}[top],
+            "bound": "hbm", "achieved": g, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": g / peaks["hbm_gbs"], "peak_source": peaks["source"], "traffic": None,
+            "per_kernel": kernels}
+
+    if not args.no_block and wl.kind == "full_pass" and world >= 1:
+        bstep = make_step(BLOCK_WORKLOAD, dev)
+        bms, bgraph = time_graph(bstep, args.steps, args.warmup, world, stream)
+        del bgraph
+        times = time_block_kernels(bstep, 3, stream)
+        parts = bstep.byte_parts
+        line["block"] = {
+            "workload": BLOCK_WORKLOAD, "ms_per_step": bms, "tokens_per_s": bstep.wl.T * world / (bms / 1e3),
+            "algorithmic_gbs": bstep.bytes / (bms / 1e3) / 1e9,
+            "frac": bstep.bytes / (bms / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "per_kernel_ms": times,
+            "per_kernel_gbs": {k: parts[k] / (times[k] / 1e3) / 1e9 for k in times if times[k]}}
+        del bstep
+        torch.cuda.empty_cache()
+
+    if not args.no_e2e:
+        ems, h2d, d2h = run_e2e(step, max(2, min(args.steps, 5)), 1, stream)
+        ems = max_over_ranks(ems, world)
+        line["e2e"] = {"value": tokens / (ems / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h, "ms_per_step": ems}
+    line["clocks"] = clocks.summary()
+    if rank == 0 and world >= 1 and not args.no_cpu_baseline:
+        base, _ = cpu_baseline(args.workload)
+        line["cpu_baseline"] = base
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = inputs.WORKLOADS[args.workload]
+    base, (run, rows) = cpu_baseline(args.workload, target_s=4.0)
+    for _ in range(args.warmup):
+        run(rows[:8])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run(rows)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = len(rows) / dt
+    base["value"] = value
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "kind": wl.kind, "T": wl.T, "d": wl.d,
+                   "sample_rows_per_step": len(rows)},
+        "cpu_baseline": base,
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(
+        n for n, w in inputs.WORKLOADS.items() if w.kind != "full_read"))
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-block", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args()
+    args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        reference(args)
+    else:
+        ours(args)
+
+
+if __name__ == "__main__":
+    main()

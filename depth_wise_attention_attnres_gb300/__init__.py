@@ -1,1 +1,20 @@
-"""GB300-native AttnRes depth-wise aggregation (Full and Block AttnRes)."""
+"""GB300-native AttnRes depth-wise aggregation (Full and Block AttnRes).
+
+The compute lives in ``libattnres.so`` (hand-written CUDA for sm_103a, C ABI
+declared in ``include/attnres.h``); ``binding`` exposes its entry points to
+Python under the same names.
+"""
+from .binding import (  # noqa: F401
+    AttnResError,
+    attnres_abi_version,
+    attnres_block_merge,
+    attnres_block_pass,
+    attnres_block_stage1,
+    attnres_block_summary_accumulate,
+    attnres_device_status,
+    attnres_full_fwd,
+    attnres_full_pass,
+    attnres_kernel_path,
+    attnres_status_string,
+    lib,
+)

@@ -1,0 +1,220 @@
+"""Thin Python binding over libattnres.so (argument marshalling only).
+
+Every function has the name of the C entry point it calls and does nothing
+but turn torch CUDA tensors into pointers, sizes and dtype codes, pass the
+current stream, and raise ``AttnResError`` on a non-zero status. All
+arithmetic happens in the library's CUDA kernels; there is no other path. If
+the library has not been built the first call raises ``RuntimeError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+from . import build as _build
+
+F32, BF16 = 0, 1
+_STATUS = {0: "ATTNRES_OK", 1: "ATTNRES_ERR_INVALID_ARG", 2: "ATTNRES_ERR_UNSUPPORTED",
+           3: "ATTNRES_ERR_CUDA", 4: "ATTNRES_ERR_TIMEOUT"}
+
+_lib = None
+_lock = threading.Lock()
+
+_VP, _I32, _I64, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+_SIGNATURES = {
+    "attnres_full_fwd": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _I32, _VP],
+    "attnres_full_pass": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _I64, _I32, _VP],
+    "attnres_block_stage1": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _I32, _F,
+                             ctypes.POINTER(_VP), _VP, _VP],
+    "attnres_block_merge": [_VP, _VP, _VP, _VP, _I32, _VP, _VP, _F, _I64, _I32, _I32, _VP, _VP],
+    "attnres_block_summary_accumulate": [_VP, _VP, _I32, _VP, _I64, _I32, _I32, _VP],
+    "attnres_block_pass": [_VP, _I64, _I32, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _I64,
+                           _I32, _VP, _VP, _VP, _VP, _I64, _VP],
+    "attnres_device_status": [_VP],
+    "attnres_status_string": [_I32],
+    "attnres_kernel_path": [_I32, _VP, _VP, _I32, _I32, _I64, _I32, _I32],
+    "attnres_abi_version": [],
+}
+
+
+class AttnResError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} returned {_STATUS.get(status, status)}: "
+                         f"{status_string(status)}")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"libattnres.so not found at {path}: build it first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            handle = ctypes.CDLL(path)
+            for name, args in _SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_char_p if name == "attnres_status_string" else ctypes.c_int
+            _lib = handle
+    return _lib
+
+
+def header_functions(path: str | None = None) -> list[str]:
+    """Names of the functions declared in include/attnres.h."""
+    path = path or os.path.join(_build.INCLUDE, "attnres.h")
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attnres_[a-z0-9_]+)\s*\(", text)))
+
+
+# ------------------------------------------------------------ marshalling ----
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"storage dtype must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("tensors passed to libattnres must be on a CUDA device")
+    return t.data_ptr()
+
+
+def _rows(t: torch.Tensor) -> tuple[int, int]:
+    """(T, d) of a [T, d] tensor with contiguous rows."""
+    if t.dim() != 2 or t.stride(1) != 1 or t.stride(0) != t.shape[1]:
+        raise ValueError("expected a contiguous [T, d] tensor")
+    return t.shape[0], t.shape[1]
+
+
+def _slices(t: torch.Tensor) -> tuple[int, int, int, int]:
+    """(n, T, d, stride) of [n, T, d] consecutive [T, d] slices."""
+    if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+        raise ValueError("expected [n, T, d] with contiguous [T, d] slices")
+    return t.shape[0], t.shape[1], t.shape[2], t.stride(0)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(name: str, status: int) -> None:
+    if status != 0:
+        raise AttnResError(name, status)
+
+
+# ---------------------------------------------------------------- entries ----
+
+def attnres_full_fwd(V: torch.Tensor, n_src: int, w: torch.Tensor, gamma: torch.Tensor,
+                     eps: float, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """One Full AttnRes read over V[0 .. n_src) (V is [n, T, d]) into out [T, d]."""
+    _, T, d, stride = _slices(V)
+    if _rows(out) != (T, d):
+        raise ValueError("out must be [T, d]")
+    _check("attnres_full_fwd", lib().attnres_full_fwd(
+        _ptr(V), stride, n_src, T, d, _dtype(V), _ptr(w), _ptr(gamma), eps, _ptr(out),
+        _dtype(out), _stream(stream)))
+    return out
+
+
+def attnres_full_pass(V: torch.Tensor, W: torch.Tensor, Gamma: torch.Tensor, eps: float,
+                      out: torch.Tensor, R: int | None = None, stream=None) -> torch.Tensor:
+    """R reads over history V [R, T, d]; read r uses V[0 .. r] and writes out[r]."""
+    n, T, d, stride = _slices(V)
+    R = n if R is None else R
+    on, oT, od, ostride = _slices(out)
+    if (oT, od) != (T, d) or on < R:
+        raise ValueError("out must be [R, T, d]")
+    _check("attnres_full_pass", lib().attnres_full_pass(
+        _ptr(V), stride, R, T, d, _dtype(V), _ptr(W), _ptr(Gamma), eps, _ptr(out), ostride,
+        _dtype(out), _stream(stream)))
+    return out
+
+
+def attnres_block_stage1(Src: torch.Tensor, n_src: int, W: torch.Tensor, Gamma: torch.Tensor,
+                         eps: float, O: list, lse: torch.Tensor | None, stream=None) -> None:
+    """Stage 1: the S = len(O) queries of W [S, d] over Src[0 .. n_src)."""
+    _, T, d, stride = _slices(Src)
+    S = len(O)
+    ptrs = (ctypes.c_void_p * max(S, 1))(*[_ptr(o) for o in O])
+    _check("attnres_block_stage1", lib().attnres_block_stage1(
+        _ptr(Src), stride, n_src, T, d, _dtype(Src), _ptr(W), _ptr(Gamma), S, eps, ptrs,
+        _ptr(lse), _stream(stream)))
+
+
+def attnres_block_merge(O_j: torch.Tensor, lse_j: torch.Tensor, P: torch.Tensor, f_prev,
+                        p_is_empty: bool, w: torch.Tensor, gamma: torch.Tensor, eps: float,
+                        out: torch.Tensor, stream=None) -> torch.Tensor:
+    """Stage 2 for one sublayer (running sum P updated in place when f_prev is given)."""
+    T, d = _rows(O_j)
+    _check("attnres_block_merge", lib().attnres_block_merge(
+        _ptr(O_j), _ptr(lse_j), _ptr(P), _ptr(f_prev), int(bool(p_is_empty)), _ptr(w),
+        _ptr(gamma), eps, T, d, _dtype(O_j), _ptr(out), _stream(stream)))
+    return out
+
+
+def attnres_block_summary_accumulate(P, f: torch.Tensor, p_is_empty: bool, summary_out=None,
+                                     stream=None) -> None:
+    """P += f, or (freeze) summary_out = round(P + f)."""
+    T, d = _rows(f)
+    _check("attnres_block_summary_accumulate", lib().attnres_block_summary_accumulate(
+        _ptr(P), _ptr(f), int(bool(p_is_empty)), _ptr(summary_out), T, d, _dtype(f),
+        _stream(stream)))
+
+
+def attnres_block_pass(F: torch.Tensor, N: int, S: int, W: torch.Tensor, Gamma: torch.Tensor,
+                       eps: float, Src: torch.Tensor, O_scratch, lse_scratch: torch.Tensor,
+                       P_scratch, out: torch.Tensor, freeze_last: bool = False,
+                       stream=None) -> torch.Tensor:
+    """N blocks of S sublayers by the two-stage computation (Src[0] = embedding)."""
+    _, T, d, fstride = _slices(F)
+    _, _, _, sstride = _slices(Src)
+    _, _, _, ostride = _slices(out)
+    _check("attnres_block_pass", lib().attnres_block_pass(
+        _ptr(F), fstride, N, S, T, d, _dtype(F), _ptr(W), _ptr(Gamma), eps, _ptr(Src), sstride,
+        int(bool(freeze_last)), _ptr(O_scratch), _ptr(lse_scratch), _ptr(P_scratch), _ptr(out),
+        ostride, _stream(stream)))
+    return out
+
+
+def attnres_device_status(stream=None) -> int:
+    return int(lib().attnres_device_status(_stream(stream)))
+
+
+def status_string(status: int) -> str:
+    return lib().attnres_status_string(int(status)).decode()
+
+
+attnres_status_string = status_string
+
+
+def attnres_kernel_path(op: int, src_ptr: int, out_ptr: int, n_or_s: int, s: int, T: int, d: int,
+                        dtype: int) -> int:
+    return int(lib().attnres_kernel_path(op, src_ptr, out_ptr, n_or_s, s, T, d, dtype))
+
+
+def attnres_abi_version() -> int:
+    return int(lib().attnres_abi_version())

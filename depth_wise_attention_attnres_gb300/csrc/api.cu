@@ -1,0 +1,405 @@
+// C ABI of the AttnRes aggregation library: argument checks, kernel choice,
+// pass sequencing and device status. Every computation runs in the kernels of
+// full_fwd.cu, stage1.cu, merge.cu and generic.cu.
+#include <cuda_runtime.h>
+
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "attnres.h"
+#include "internal.h"
+
+namespace attnres {
+
+namespace {
+std::mutex g_mu;
+std::map<std::pair<const void*, int>, int> g_smem_set;            // (kernel, device) -> bytes
+std::map<std::tuple<const void*, int, int, int>, int> g_occ;      // (kernel, dev, thr, smem)
+std::map<int, int> g_sms;
+
+int current_device() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return dev;
+}
+}  // namespace
+
+int sm_count() {
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_sms.find(dev);
+  if (it != g_sms.end()) return it->second;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+  g_sms[dev] = n;
+  return n;
+}
+
+cudaError_t allow_dynamic_smem(const void* kernel, int bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto key = std::make_pair(kernel, dev);
+  auto it = g_smem_set.find(key);
+  if (it != g_smem_set.end() && it->second >= bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) g_smem_set[key] = bytes;
+  return e;
+}
+
+int blocks_per_sm(const void* kernel, int threads, int smem_bytes) {
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto key = std::make_tuple(kernel, dev, threads, smem_bytes);
+  auto it = g_occ.find(key);
+  if (it != g_occ.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    n = 1;
+  }
+  if (n < 1) n = 1;
+  g_occ[key] = n;
+  return n;
+}
+
+}  // namespace attnres
+
+using namespace attnres;
+
+namespace {
+
+constexpr int kGenericScoreLimit = 200 * 1024;  // bytes of scores per warp
+
+bool valid_dtype(int32_t t) { return t == ATTNRES_F32 || t == ATTNRES_BF16; }
+int elem_size(int32_t t) { return t == ATTNRES_BF16 ? 2 : 4; }
+bool valid_eps(float eps) { return eps >= 0.0f && eps < 3.0e38f; }
+
+struct Range {
+  uintptr_t lo = 0, hi = 0;  // [lo, hi)
+};
+Range range_of(const void* p, int64_t bytes) {
+  Range r;
+  r.lo = reinterpret_cast<uintptr_t>(p);
+  r.hi = r.lo + static_cast<uintptr_t>(bytes);
+  return r;
+}
+bool overlap(const Range& a, const Range& b) {
+  if (a.lo == a.hi || b.lo == b.hi) return false;
+  return a.lo < b.hi && b.lo < a.hi;
+}
+
+int status_of(cudaError_t e) {
+  if (e == cudaSuccess) return ATTNRES_OK;
+  cudaGetLastError();  // consume it
+  return e == cudaErrorInvalidValue ? ATTNRES_ERR_UNSUPPORTED : ATTNRES_ERR_CUDA;
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+// Checks and fills the arguments of one full read. Returns a status.
+int make_full(const void* V, int64_t src_stride, int32_t n_src, int64_t T, int32_t d,
+              int32_t v_dtype, const float* w, const float* gamma, float eps, void* out,
+              int32_t out_dtype, FullArgs* a) {
+  if (n_src < 1 || d < 1 || T < 0 || !valid_dtype(v_dtype) || !valid_dtype(out_dtype) ||
+      !valid_eps(eps))
+    return ATTNRES_ERR_INVALID_ARG;
+  if (T == 0) return ATTNRES_OK;
+  if (!V || !w || !gamma || !out) return ATTNRES_ERR_INVALID_ARG;
+  const int64_t E = T * d;
+  if (n_src > 1 && src_stride < E) return ATTNRES_ERR_INVALID_ARG;
+  const int es = elem_size(v_dtype);
+  const Range rv = range_of(V, ((n_src - 1) * (n_src > 1 ? src_stride : 0) + E) * es);
+  const Range ro = range_of(out, E * elem_size(out_dtype));
+  if (overlap(rv, ro)) return ATTNRES_ERR_INVALID_ARG;
+  *a = FullArgs{V, src_stride, n_src, T, d, v_dtype == ATTNRES_BF16, w, gamma, eps, out,
+                out_dtype == ATTNRES_BF16};
+  return ATTNRES_OK;
+}
+
+int run_full(const FullArgs& a, cudaStream_t s) {
+  if (full_fast_ok(a)) return status_of(launch_full_fast(a, s));
+  // General kernel: writes in the storage dtype of the sources.
+  if (a.out_bf16 != a.v_bf16) return ATTNRES_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(a.n_src) * 4 > kGenericScoreLimit) return ATTNRES_ERR_UNSUPPORTED;
+  MultiArgs m{};
+  m.V = a.V;
+  m.src_stride = a.src_stride;
+  m.n_src = a.n_src;
+  m.T = a.T;
+  m.d = a.d;
+  m.bf16 = a.v_bf16;
+  m.W = a.w;
+  m.Gamma = a.gamma;
+  m.S = 1;
+  m.eps = a.eps;
+  m.out[0] = a.out;
+  m.lse = nullptr;
+  return status_of(launch_multi_generic(m, s));
+}
+
+int make_stage1(const void* Src, int64_t src_stride, int32_t n_src, int64_t T, int32_t d,
+                int32_t dtype, const float* W, const float* Gamma, int32_t S, float eps,
+                void* const* O, float* lse, MultiArgs* m) {
+  if (n_src < 1 || d < 1 || T < 0 || !valid_dtype(dtype) || !valid_eps(eps) || S < 1 ||
+      S > ATTNRES_MAX_QUERIES)
+    return ATTNRES_ERR_INVALID_ARG;
+  if (T == 0) return ATTNRES_OK;
+  if (!Src || !W || !Gamma || !O) return ATTNRES_ERR_INVALID_ARG;
+  const int64_t E = T * d;
+  if (n_src > 1 && src_stride < E) return ATTNRES_ERR_INVALID_ARG;
+  const int es = elem_size(dtype);
+  const Range rs = range_of(Src, ((n_src - 1) * (n_src > 1 ? src_stride : 0) + E) * es);
+  const Range rl = lse ? range_of(lse, static_cast<int64_t>(S) * T * 4) : Range{};
+  if (overlap(rs, rl)) return ATTNRES_ERR_INVALID_ARG;
+  for (int j = 0; j < S; ++j) {
+    if (!O[j]) return ATTNRES_ERR_INVALID_ARG;
+    const Range rj = range_of(O[j], E * es);
+    if (overlap(rj, rs) || overlap(rj, rl)) return ATTNRES_ERR_INVALID_ARG;
+    for (int q = 0; q < j; ++q)
+      if (overlap(rj, range_of(O[q], E * es))) return ATTNRES_ERR_INVALID_ARG;
+  }
+  *m = MultiArgs{};
+  m->V = Src;
+  m->src_stride = src_stride;
+  m->n_src = n_src;
+  m->T = T;
+  m->d = d;
+  m->bf16 = dtype == ATTNRES_BF16;
+  m->W = W;
+  m->Gamma = Gamma;
+  m->S = S;
+  m->eps = eps;
+  for (int j = 0; j < S; ++j) m->out[j] = O[j];
+  m->lse = lse;
+  return ATTNRES_OK;
+}
+
+int run_stage1(const MultiArgs& m, cudaStream_t s) {
+  if (stage1_fast_ok(m)) return status_of(launch_stage1_fast(m, s));
+  if (static_cast<int64_t>(m.n_src) * m.S * 4 > kGenericScoreLimit) return ATTNRES_ERR_UNSUPPORTED;
+  return status_of(launch_multi_generic(m, s));
+}
+
+int make_merge(const void* O_j, const float* lse_j, float* P, const void* f_prev, int32_t p_is_empty,
+               const float* w, const float* gamma, float eps, int64_t T, int32_t d, int32_t dtype,
+               void* out, MergeArgs* a) {
+  if (d < 1 || T < 0 || !valid_dtype(dtype) || !valid_eps(eps)) return ATTNRES_ERR_INVALID_ARG;
+  if (!f_prev && p_is_empty) return ATTNRES_ERR_INVALID_ARG;
+  if (T == 0) return ATTNRES_OK;
+  if (!O_j || !lse_j || !P || !w || !gamma || !out) return ATTNRES_ERR_INVALID_ARG;
+  const int64_t E = T * d;
+  const int es = elem_size(dtype);
+  const Range ro = range_of(O_j, E * es), rl = range_of(lse_j, T * 4), rp = range_of(P, E * 4),
+              rf = f_prev ? range_of(f_prev, E * es) : Range{}, rout = range_of(out, E * es);
+  if (overlap(rout, ro) || overlap(rout, rp) || overlap(rout, rf) || overlap(rout, rl) ||
+      overlap(rp, ro) || overlap(rp, rf) || overlap(rp, rl))
+    return ATTNRES_ERR_INVALID_ARG;
+  *a = MergeArgs{O_j, lse_j, P, f_prev, p_is_empty != 0, w, gamma, eps, T, d, dtype == ATTNRES_BF16, out};
+  return ATTNRES_OK;
+}
+
+int make_accum(float* P, const void* f, int32_t p_is_empty, void* summary_out, int64_t T, int32_t d,
+               int32_t dtype, AccumArgs* a) {
+  if (d < 1 || T < 0 || !valid_dtype(dtype)) return ATTNRES_ERR_INVALID_ARG;
+  if (T == 0) return ATTNRES_OK;
+  const bool p_used = !(p_is_empty && summary_out);
+  if (!f || (p_used && !P)) return ATTNRES_ERR_INVALID_ARG;
+  const int64_t E = T * d;
+  const int es = elem_size(dtype);
+  const Range rp = P ? range_of(P, E * 4) : Range{}, rf = range_of(f, E * es),
+              rs = summary_out ? range_of(summary_out, E * es) : Range{};
+  if (overlap(rp, rf) || overlap(rs, rf) || overlap(rs, rp)) return ATTNRES_ERR_INVALID_ARG;
+  *a = AccumArgs{P, f, p_is_empty != 0, summary_out, T, d, dtype == ATTNRES_BF16};
+  return ATTNRES_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attnres_abi_version(void) { return 1; }
+
+const char* attnres_status_string(int32_t status) {
+  switch (status) {
+    case ATTNRES_OK: return "ok";
+    case ATTNRES_ERR_INVALID_ARG: return "invalid argument";
+    case ATTNRES_ERR_UNSUPPORTED: return "unsupported: beyond a stated limit";
+    case ATTNRES_ERR_CUDA: return "CUDA error while launching";
+    case ATTNRES_ERR_TIMEOUT: return "a device-side wait ran out of time";
+    default: return "unknown status";
+  }
+}
+
+int attnres_full_fwd(const void* V, int64_t src_stride, int32_t n_src, int64_t T, int32_t d,
+                     int32_t v_dtype, const float* w, const float* gamma, float eps, void* out,
+                     int32_t out_dtype, void* stream) {
+  FullArgs a{};
+  const int st = make_full(V, src_stride, n_src, T, d, v_dtype, w, gamma, eps, out, out_dtype, &a);
+  if (st != ATTNRES_OK || T == 0) return st;
+  return run_full(a, as_stream(stream));
+}
+
+int attnres_full_pass(const void* V, int64_t src_stride, int32_t R, int64_t T, int32_t d,
+                      int32_t v_dtype, const float* W, const float* Gamma, float eps, void* out,
+                      int64_t out_stride, int32_t out_dtype, void* stream) {
+  if (R < 1 || d < 1 || T < 0 || !valid_dtype(v_dtype) || !valid_dtype(out_dtype) || !valid_eps(eps))
+    return ATTNRES_ERR_INVALID_ARG;
+  if (T == 0) return ATTNRES_OK;
+  if (!V || !W || !Gamma || !out) return ATTNRES_ERR_INVALID_ARG;
+  const int64_t E = T * d;
+  if (src_stride < E || out_stride < E) return ATTNRES_ERR_INVALID_ARG;
+  const Range rv = range_of(V, ((R - 1) * src_stride + E) * elem_size(v_dtype));
+  const Range ro = range_of(out, ((R - 1) * out_stride + E) * elem_size(out_dtype));
+  if (overlap(rv, ro)) return ATTNRES_ERR_INVALID_ARG;
+  const int oes = elem_size(out_dtype);
+  for (int32_t r = 0; r < R; ++r) {
+    const int st = attnres_full_fwd(V, src_stride, r + 1, T, d, v_dtype, W + static_cast<int64_t>(r) * d,
+                                    Gamma + static_cast<int64_t>(r) * d, eps,
+                                    static_cast<char*>(out) + r * out_stride * oes, out_dtype, stream);
+    if (st != ATTNRES_OK) return st;
+  }
+  return ATTNRES_OK;
+}
+
+int attnres_block_stage1(const void* Src, int64_t src_stride, int32_t n_src, int64_t T, int32_t d,
+                         int32_t dtype, const float* W, const float* Gamma, int32_t S, float eps,
+                         void* const* O, float* lse, void* stream) {
+  MultiArgs m{};
+  const int st = make_stage1(Src, src_stride, n_src, T, d, dtype, W, Gamma, S, eps, O, lse, &m);
+  if (st != ATTNRES_OK || T == 0) return st;
+  return run_stage1(m, as_stream(stream));
+}
+
+int attnres_block_merge(const void* O_j, const float* lse_j, float* P, const void* f_prev,
+                        int32_t p_is_empty, const float* w, const float* gamma, float eps, int64_t T,
+                        int32_t d, int32_t dtype, void* out, void* stream) {
+  MergeArgs a{};
+  const int st = make_merge(O_j, lse_j, P, f_prev, p_is_empty, w, gamma, eps, T, d, dtype, out, &a);
+  if (st != ATTNRES_OK || T == 0) return st;
+  return status_of(launch_merge(a, as_stream(stream), merge_fast_ok(a)));
+}
+
+int attnres_block_summary_accumulate(float* P, const void* f, int32_t p_is_empty, void* summary_out,
+                                     int64_t T, int32_t d, int32_t dtype, void* stream) {
+  AccumArgs a{};
+  const int st = make_accum(P, f, p_is_empty, summary_out, T, d, dtype, &a);
+  if (st != ATTNRES_OK || T == 0) return st;
+  return status_of(launch_accum(a, as_stream(stream), accum_fast_ok(a)));
+}
+
+int attnres_block_pass(const void* F, int64_t f_stride, int32_t N, int32_t S, int64_t T, int32_t d,
+                       int32_t dtype, const float* W, const float* Gamma, float eps, void* Src,
+                       int64_t src_stride, int32_t freeze_last, void* O_scratch, float* lse_scratch,
+                       float* P_scratch, void* out, int64_t out_stride, void* stream) {
+  if (N < 1 || S < 1 || S > ATTNRES_MAX_QUERIES || d < 1 || T < 0 || !valid_dtype(dtype) ||
+      !valid_eps(eps))
+    return ATTNRES_ERR_INVALID_ARG;
+  if (T == 0) return ATTNRES_OK;
+  if (!F || !W || !Gamma || !Src || !lse_scratch || !out || (S > 1 && (!O_scratch || !P_scratch)))
+    return ATTNRES_ERR_INVALID_ARG;
+  const int64_t E = T * d;
+  if (f_stride < E || src_stride < E || out_stride < E) return ATTNRES_ERR_INVALID_ARG;
+  const int es = elem_size(dtype);
+  const int64_t L = static_cast<int64_t>(N) * S;
+  const int nsrc_slots = N + (freeze_last ? 1 : 0);
+  const Range rF = range_of(F, ((L - 1) * f_stride + E) * es);
+  const Range rS = range_of(Src, ((nsrc_slots - 1) * src_stride + E) * es);
+  const Range rO = S > 1 ? range_of(O_scratch, (S - 1) * E * es) : Range{};
+  const Range rL = range_of(lse_scratch, S * T * 4);
+  const Range rP = S > 1 || P_scratch ? range_of(P_scratch, E * 4) : Range{};
+  const Range rOut = range_of(out, ((L - 1) * out_stride + E) * es);
+  const Range all[] = {rF, rS, rO, rL, rP, rOut};
+  for (int i = 0; i < 6; ++i)
+    for (int j = i + 1; j < 6; ++j)
+      if (overlap(all[i], all[j])) return ATTNRES_ERR_INVALID_ARG;
+
+  char* outb = static_cast<char*>(out);
+  const char* Fb = static_cast<const char*>(F);
+  char* Srcb = static_cast<char*>(Src);
+  char* Ob = static_cast<char*>(O_scratch);
+  for (int32_t n = 0; n < N; ++n) {
+    const int64_t k0 = static_cast<int64_t>(n) * S;  // first sublayer of the block
+    // Stage 1: the block's S queries over embedding + n completed block sums.
+    void* O[ATTNRES_MAX_QUERIES];
+    O[0] = outb + k0 * out_stride * es;
+    for (int j = 1; j < S; ++j) O[j] = Ob + (j - 1) * E * es;
+    int st = attnres_block_stage1(Src, src_stride, n + 1, T, d, dtype, W + k0 * d, Gamma + k0 * d, S, eps,
+                                  O, lse_scratch, stream);
+    if (st != ATTNRES_OK) return st;
+    // Stage 2: fold the running sum in, one sublayer at a time.
+    for (int j = 1; j < S; ++j) {
+      st = attnres_block_merge(O[j], lse_scratch + j * T, P_scratch, Fb + (k0 + j - 1) * f_stride * es,
+                               j == 1, W + (k0 + j) * d, Gamma + (k0 + j) * d, eps, T, d, dtype,
+                               outb + (k0 + j) * out_stride * es, stream);
+      if (st != ATTNRES_OK) return st;
+    }
+    // Freeze the block summary b_{n+1} = P + f_last into Src[n + 1].
+    if (n + 1 < N || freeze_last) {
+      st = attnres_block_summary_accumulate(P_scratch, Fb + (k0 + S - 1) * f_stride * es, S == 1,
+                                            Srcb + (n + 1) * src_stride * es, T, d, dtype, stream);
+      if (st != ATTNRES_OK) return st;
+    }
+  }
+  return ATTNRES_OK;
+}
+
+int attnres_device_status(void* stream) {
+  cudaError_t e = stream ? cudaStreamSynchronize(as_stream(stream)) : cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return ATTNRES_ERR_CUDA;
+  }
+  unsigned int f1 = 0, f2 = 0;
+  if (take_timeout_full(&f1) != cudaSuccess || take_timeout_stage1(&f2) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTNRES_ERR_CUDA;
+  }
+  if (f1 || f2) return ATTNRES_ERR_TIMEOUT;
+  e = cudaGetLastError();
+  return e == cudaSuccess ? ATTNRES_OK : ATTNRES_ERR_CUDA;
+}
+
+int attnres_kernel_path(int32_t op, const void* src, const void* out, int32_t n_or_s, int32_t s,
+                        int64_t T, int32_t d, int32_t dtype) {
+  if (!valid_dtype(dtype) || d < 1 || T < 0) return -1;
+  // Only alignment is inspected, so an aligned non-null stand-in serves for
+  // the fp32 parameter pointers; it is never dereferenced.
+  const float* wp = reinterpret_cast<const float*>(static_cast<uintptr_t>(256));
+  const int64_t E = T * d;
+  switch (op) {
+    case 0: {
+      FullArgs a{src, E, n_or_s, T, d, dtype == ATTNRES_BF16, wp, wp, 0.f, const_cast<void*>(out),
+                 dtype == ATTNRES_BF16};
+      return full_fast_ok(a) ? 1 : 0;
+    }
+    case 1: {
+      if (s < 1 || s > ATTNRES_MAX_QUERIES) return -1;
+      MultiArgs m{};
+      m.V = src;
+      m.src_stride = E;
+      m.n_src = n_or_s;
+      m.T = T;
+      m.d = d;
+      m.bf16 = dtype == ATTNRES_BF16;
+      m.W = wp;
+      m.Gamma = wp;
+      m.S = s;
+      for (int j = 0; j < s; ++j) m.out[j] = const_cast<void*>(out);
+      return stage1_fast_ok(m) ? 1 : 0;
+    }
+    case 2: {
+      MergeArgs a{src, wp, const_cast<float*>(wp), src, 0, wp, wp, 0.f, T, d, dtype == ATTNRES_BF16,
+                  const_cast<void*>(out)};
+      return merge_fast_ok(a) ? 1 : 0;
+    }
+    case 3: {
+      AccumArgs a{const_cast<float*>(wp), src, 0, const_cast<void*>(out), T, d, dtype == ATTNRES_BF16};
+      return accum_fast_ok(a) ? 1 : 0;
+    }
+    default: return -1;
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,264 @@
+// Full AttnRes read, fast kernel (sm_103a).
+//
+// Computes, per token row t (DepthBench reading notes section 2.3, paper
+// Appendix A; LLMRes blog "Kimi AttnRes"):
+//   e_i = w^T (gamma * v_i / sqrt(mean(v_i^2) + eps)),  z = sum_i softmax_i(e) v_i
+// in one pass over the sources with an online softmax (running max m and mass
+// l; the accumulator is rescaled only when the max grows).
+//
+// Data movement: each CTA owns a contiguous range of token rows and walks it
+// in tiles of kTM rows. For every (tile, source) pair the rows are contiguous
+// in HBM ([n, T, d] layout), so one elected producer thread moves the whole
+// tile with a single 1-D bulk copy (cp.async.bulk, TMA engine) into a ring of
+// shared-memory stages guarded by mbarriers. Eight consumer warps each own
+// one row of the tile: a lane holds d/32 elements (4 consecutive per 128-element
+// chunk, conflict-free 8/16-byte shared loads), the RMS and the score are two
+// butterfly warp sums, and the weighted accumulation stays in fp32 registers.
+// The path is HBM-bound (one pass, about 3 flop per byte), so tensor cores are
+// not used.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace attnres {
+namespace {
+
+__device__ unsigned int g_full_timeout = 0;
+
+constexpr int kNW = 8;               // consumer warps = rows per tile
+constexpr int kTM = kNW;
+constexpr int kThreads = (kNW + 1) * kWarp;
+constexpr int kBarBytes = 128;       // barrier area at the start of shared memory
+constexpr int kMaxStages = 8;
+constexpr int kSmemBudget = 112 * 1024;  // per CTA: two CTAs fit on one SM
+
+template <typename Tin, int CH>
+__global__ void __launch_bounds__(kThreads) full_fwd_bulk_kernel(FullArgs a, int nstage) {
+  constexpr int D = CH * 128;
+  constexpr int NE = CH * 4;         // elements per lane
+  // Keeping the converted row in registers saves a second shared read; for
+  // the widest rows the registers go to the accumulator instead.
+  constexpr bool kKeepX = CH <= 8;
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty_bar = full_bar + kMaxStages;
+  Tin* stages = reinterpret_cast<Tin*>(smem + kBarBytes);
+  constexpr int kStageElems = kTM * D;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t T = a.T;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * T / gridDim.x;
+  const int64_t r1 = static_cast<int64_t>(blockIdx.x + 1) * T / gridDim.x;
+  const int ntiles = static_cast<int>((r1 - r0 + kTM - 1) / kTM);
+  const int n = a.n_src;
+  const int64_t total = static_cast<int64_t>(ntiles) * n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < nstage; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), kNW);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp == kNW) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    const char* V = static_cast<const char*>(a.V);
+    int stage = 0;
+    uint32_t phase = 0;
+    int64_t issued = 0;
+    bool ok = true;
+    for (int64_t it = 0; it < total; ++it) {
+      // A fresh barrier counts its (virtual) previous phase as complete, so
+      // the first round of waits on parity 1 passes at once.
+      if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u)) {
+        ok = false;
+        break;
+      }
+      const int tile = static_cast<int>(it / n);
+      const int src = static_cast<int>(it - static_cast<int64_t>(tile) * n);
+      const int64_t row0 = r0 + static_cast<int64_t>(tile) * kTM;
+      const int rows = static_cast<int>(min(static_cast<int64_t>(kTM), r1 - row0));
+      const uint32_t bytes = static_cast<uint32_t>(rows) * D * sizeof(Tin);
+      const uint32_t fb = smem_u32(&full_bar[stage]);
+      mbar_arrive_expect_tx(fb, bytes);
+      bulk_g2s(smem_u32(stages + static_cast<size_t>(stage) * kStageElems),
+               V + (static_cast<int64_t>(src) * a.src_stride + row0 * D) * sizeof(Tin), bytes, fb);
+      ++issued;
+      if (++stage == nstage) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) {
+      atomicOr(&g_full_timeout, 1u);
+      // Let the copies still in flight land before this CTA's memory goes.
+      for (int64_t it = issued > nstage ? issued - nstage : 0; it < issued; ++it)
+        (void)mbar_wait(smem_u32(&full_bar[it % nstage]), static_cast<uint32_t>((it / nstage) & 1));
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  float2 wq[NE / 2];  // w * gamma for this lane's elements
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int k = (c * kWarp + lane) * 4;
+    const float4 w4 = *reinterpret_cast<const float4*>(a.w + k);
+    const float4 g4 = *reinterpret_cast<const float4*>(a.gamma + k);
+    wq[c * 2] = make_float2(w4.x * g4.x, w4.y * g4.y);
+    wq[c * 2 + 1] = make_float2(w4.z * g4.z, w4.w * g4.w);
+  }
+  const float inv_d = 1.0f / static_cast<float>(D);
+  const float eps = a.eps;
+
+  int stage = 0;
+  uint32_t phase = 0;
+  bool ok = true;
+  for (int tile = 0; tile < ntiles && ok; ++tile) {
+    const int64_t row = r0 + static_cast<int64_t>(tile) * kTM + warp;
+    const bool valid = row < r1;
+    float2 acc[NE / 2];
+#pragma unroll
+    for (int e = 0; e < NE / 2; ++e) acc[e] = make_float2(0.f, 0.f);
+    float m = -INFINITY, l = 0.f;
+
+    for (int src = 0; src < n; ++src) {
+      if (!mbar_wait(smem_u32(&full_bar[stage]), phase)) {
+        ok = false;
+        break;
+      }
+      if (valid) {
+        const Tin* rowp = stages + static_cast<size_t>(stage) * kStageElems + warp * D;
+        float x[NE];
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          float t4[4];
+          lds4(rowp + (c * kWarp + lane) * 4, t4);
+          x[c * 4 + 0] = t4[0]; x[c * 4 + 1] = t4[1]; x[c * 4 + 2] = t4[2]; x[c * 4 + 3] = t4[3];
+        }
+        float2 ss2a = make_float2(0.f, 0.f), ss2b = ss2a, dt2a = ss2a, dt2b = ss2a;
+#pragma unroll
+        for (int e = 0; e < NE / 2; e += 2) {
+          const float2 xa = make_float2(x[2 * e], x[2 * e + 1]);
+          const float2 xb = make_float2(x[2 * e + 2], x[2 * e + 3]);
+          ss2a = ffma2(xa, xa, ss2a);
+          ss2b = ffma2(xb, xb, ss2b);
+          dt2a = ffma2(wq[e], xa, dt2a);
+          dt2b = ffma2(wq[e + 1], xb, dt2b);
+        }
+        const float ss = warp_sum((ss2a.x + ss2b.x) + (ss2a.y + ss2b.y));
+        const float dot = warp_sum((dt2a.x + dt2b.x) + (dt2a.y + dt2b.y));
+        const float s = dot * rsqrtf(ss * inv_d + eps);
+        if (s > m) {  // warp-uniform: s and m are identical on every lane
+          const float c = __expf(m - s);
+          l *= c;
+          const float2 c2 = make_float2(c, c);
+#pragma unroll
+          for (int e = 0; e < NE / 2; ++e) acc[e] = fmul2(acc[e], c2);
+          m = s;
+        }
+        const float p = __expf(s - m);
+        l += p;
+        const float2 p2 = make_float2(p, p);
+        if constexpr (kKeepX) {
+#pragma unroll
+          for (int e = 0; e < NE / 2; ++e) acc[e] = ffma2(p2, make_float2(x[2 * e], x[2 * e + 1]), acc[e]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < CH; ++c) {
+            float t4[4];
+            lds4(rowp + (c * kWarp + lane) * 4, t4);
+            acc[c * 2] = ffma2(p2, make_float2(t4[0], t4[1]), acc[c * 2]);
+            acc[c * 2 + 1] = ffma2(p2, make_float2(t4[2], t4[3]), acc[c * 2 + 1]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty_bar[stage]));
+      if (++stage == nstage) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+
+    if (ok && valid) {
+      const float inv = 1.0f / l;
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int k = (c * kWarp + lane) * 4;
+        const float o[4] = {acc[c * 2].x * inv, acc[c * 2].y * inv, acc[c * 2 + 1].x * inv,
+                            acc[c * 2 + 1].y * inv};
+        if (a.out_bf16)
+          st4(static_cast<bf16*>(a.out) + row * D + k, o);
+        else
+          st4(static_cast<float*>(a.out) + row * D + k, o);
+      }
+    }
+  }
+  if (!ok) atomicOr(&g_full_timeout, 1u);
+}
+
+template <typename Tin, int CH>
+cudaError_t launch_ch(const FullArgs& a, cudaStream_t s) {
+  constexpr int D = CH * 128;
+  const int stage_bytes = kTM * D * static_cast<int>(sizeof(Tin));
+  int nstage = (kSmemBudget - kBarBytes) / stage_bytes;
+  nstage = nstage < 2 ? 2 : (nstage > kMaxStages ? kMaxStages : nstage);
+  const int smem = kBarBytes + nstage * stage_bytes;
+  const void* fn = reinterpret_cast<const void*>(&full_fwd_bulk_kernel<Tin, CH>);
+  cudaError_t e = allow_dynamic_smem(fn, smem);
+  if (e != cudaSuccess) return e;
+  const int per_sm = blocks_per_sm(fn, kThreads, smem);
+  const int64_t tiles = (a.T + kTM - 1) / kTM;
+  int64_t grid = static_cast<int64_t>(sm_count()) * (per_sm > 0 ? per_sm : 1);
+  if (grid > tiles) grid = tiles;
+  full_fwd_bulk_kernel<Tin, CH><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(a, nstage);
+  return cudaGetLastError();
+}
+
+template <typename Tin>
+cudaError_t launch_dtype(const FullArgs& a, cudaStream_t s) {
+  switch (a.d / 128) {
+    case 1: return launch_ch<Tin, 1>(a, s);
+    case 2: return launch_ch<Tin, 2>(a, s);
+    case 3: return launch_ch<Tin, 3>(a, s);
+    case 4: return launch_ch<Tin, 4>(a, s);
+    case 5: return launch_ch<Tin, 5>(a, s);
+    case 6: return launch_ch<Tin, 6>(a, s);
+    case 7: return launch_ch<Tin, 7>(a, s);
+    case 8: return launch_ch<Tin, 8>(a, s);
+    case 10: return launch_ch<Tin, 10>(a, s);
+    case 12: return launch_ch<Tin, 12>(a, s);
+    case 16: return launch_ch<Tin, 16>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+bool full_fast_ok(const FullArgs& a) {
+  const int es = a.v_bf16 ? 2 : 4;
+  const int ch = a.d / 128;
+  const bool ch_ok = (a.d % 128 == 0) && ((ch >= 1 && ch <= 8) || ch == 10 || ch == 12 || ch == 16);
+  return ch_ok && aligned16(a.V) && aligned16(a.out) && aligned16(a.w) && aligned16(a.gamma) &&
+         ((a.src_stride * es) % 16 == 0);
+}
+
+cudaError_t launch_full_fast(const FullArgs& a, cudaStream_t s) {
+  return a.v_bf16 ? launch_dtype<bf16>(a, s) : launch_dtype<float>(a, s);
+}
+
+cudaError_t take_timeout_full(unsigned int* flag) {
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(flag, g_full_timeout, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_full_timeout, &zero, sizeof(unsigned int));
+}
+
+}  // namespace attnres

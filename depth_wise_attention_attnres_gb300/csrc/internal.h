@@ -1,0 +1,92 @@
+// Internal launcher interface between the C ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "attnres.h"
+
+namespace attnres {
+
+// One Full AttnRes read (one query) over n_src sources.
+struct FullArgs {
+  const void* V;
+  int64_t src_stride;  // elements
+  int n_src;
+  int64_t T;
+  int d;
+  int v_bf16;
+  const float* w;
+  const float* gamma;
+  float eps;
+  void* out;
+  int out_bf16;
+};
+
+// S queries over the same n_src sources (stage 1; the general kernel also
+// serves a single Full read with S = 1).
+struct MultiArgs {
+  const void* V;
+  int64_t src_stride;
+  int n_src;
+  int64_t T;
+  int d;
+  int bf16;             // storage dtype of V and of every output
+  const float* W;       // [S, d]
+  const float* Gamma;   // [S, d]
+  int S;
+  float eps;
+  void* out[ATTNRES_MAX_QUERIES];
+  float* lse;           // [S, T] or nullptr
+};
+
+struct MergeArgs {
+  const void* O;
+  const float* lse;
+  float* P;
+  const void* f;        // nullptr: P used as is
+  int p_empty;
+  const float* w;
+  const float* gamma;
+  float eps;
+  int64_t T;
+  int d;
+  int bf16;
+  void* out;
+};
+
+struct AccumArgs {
+  float* P;
+  const void* f;
+  int p_empty;
+  void* summary;        // nullptr: accumulate into P
+  int64_t T;
+  int d;
+  int bf16;
+};
+
+// Kernel selection (pure functions of the arguments).
+bool full_fast_ok(const FullArgs& a);
+bool stage1_fast_ok(const MultiArgs& a);
+bool merge_fast_ok(const MergeArgs& a);
+bool accum_fast_ok(const AccumArgs& a);
+
+// Launchers: enqueue on `s` and return the launch's CUDA error.
+cudaError_t launch_full_fast(const FullArgs& a, cudaStream_t s);
+cudaError_t launch_multi_generic(const MultiArgs& a, cudaStream_t s);
+cudaError_t launch_stage1_fast(const MultiArgs& a, cudaStream_t s);
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s, bool fast);
+cudaError_t launch_accum(const AccumArgs& a, cudaStream_t s, bool fast);
+
+// Device-side timeout records of each kernel file: read and clear (blocking).
+cudaError_t take_timeout_full(unsigned int* flag);
+cudaError_t take_timeout_stage1(unsigned int* flag);
+
+// Shared launch helpers (api.cu).
+int sm_count();
+cudaError_t allow_dynamic_smem(const void* kernel, int bytes);
+int blocks_per_sm(const void* kernel, int threads, int smem_bytes);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace attnres

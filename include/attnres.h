@@ -1,0 +1,217 @@
+/*
+ * attnres.h - C ABI of the GB300 (sm_103a) AttnRes depth-wise aggregation.
+ *
+ * Attention Residuals replace the additive residual of a pre-norm Transformer
+ * with a softmax-weighted sum over depth. For one token and one read (the
+ * input of one sublayer, or of the LM head):
+ *
+ *     e_i = w^T RMSNorm_key(v_i)              (no 1/sqrt(d), temperature 1)
+ *     a_i = exp(e_i) / sum_j exp(e_j)
+ *     z   = sum_i a_i v_i
+ *
+ * (DepthBench reading notes, section 2.3 "Full AttnRes", paper Appendix A;
+ * LLMRes blog, section "Kimi AttnRes": phi(q, k) = exp(q^T RMSNorm(k)),
+ * q = w_l, k_i = v_i, with RMSNorm applied to the keys only.) RMSNorm is not
+ * written out on the pages; this library uses the plain form
+ * RMSNorm(x)_k = gamma_k x_k / sqrt(mean_k x_k^2 + eps).
+ *
+ * Full AttnRes: the sources of read l are the embedding v_0 and every earlier
+ * sublayer output. Block AttnRes (DepthBench reading notes section 2.5; LLMRes
+ * blog "Block Attention Residuals"; datacamp explainer "block attention
+ * residuals"): the sublayers are cut into blocks of S; a read attends over the
+ * embedding, the sums of the completed blocks, and the running sum of the
+ * current block when it is non-empty. The two-stage computation (datacamp
+ * explainer, "two-stage computation") batches the S pseudo-queries of a block
+ * against the cross-block sources (stage 1) and folds in the running sum with
+ * an online-softmax merge (stage 2).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named as device pointers must point to device memory of the
+ *     current CUDA device; the library reads and writes them only from
+ *     kernels. Host arrays are marked "host".
+ *   - The caller owns all memory. The library keeps no per-call state and
+ *     allocates no device memory.
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is
+ *     the legacy default stream) and is asynchronous: the call returns before
+ *     the kernels finish. No call synchronises, except attnres_device_status.
+ *   - Tensors are row-major. A [T, d] tensor has row stride d (contiguous);
+ *     "sources" of a read are consecutive [T, d] slices `src_stride` elements
+ *     apart, src_stride >= T*d.
+ *   - dtype arguments take attnres_dtype values. Storage is fp32 or bf16;
+ *     arithmetic is fp32 throughout; bf16 results are rounded to nearest even.
+ *     w and gamma are always fp32; eps is a host scalar (>= 0).
+ *   - T == 0 is valid and launches nothing.
+ *   - Fast kernels need 16-byte aligned pointers and d a multiple of 128
+ *     (full read), of the per-warp slice (stage 1) or of 8 (merge); any other
+ *     valid input runs on a general kernel with the same results.
+ *   - Errors: ATTNRES_ERR_INVALID_ARG for bad arguments (nothing launched),
+ *     ATTNRES_ERR_UNSUPPORTED for valid requests beyond a stated limit,
+ *     ATTNRES_ERR_CUDA when a launch fails (the CUDA error is consumed).
+ *     Device-side waits are bounded; a wait that runs out makes the kernel
+ *     stop and is reported by attnres_device_status as ATTNRES_ERR_TIMEOUT.
+ *   - Outputs must not overlap inputs unless a function says otherwise.
+ */
+#ifndef ATTNRES_H
+#define ATTNRES_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { ATTNRES_F32 = 0, ATTNRES_BF16 = 1 } attnres_dtype;
+
+typedef enum {
+  ATTNRES_OK = 0,
+  ATTNRES_ERR_INVALID_ARG = 1,
+  ATTNRES_ERR_UNSUPPORTED = 2,
+  ATTNRES_ERR_CUDA = 3,
+  ATTNRES_ERR_TIMEOUT = 4
+} attnres_status;
+
+/* Largest number of pseudo-queries one stage-1 call batches. */
+#define ATTNRES_MAX_QUERIES 16
+
+/*
+ * attnres_full_fwd - one Full AttnRes read (DepthBench reading notes section
+ * 2.3, paper Appendix A; LLMRes blog "Kimi AttnRes", h_l = sum_i alpha_{i->l} v_i).
+ *
+ *   V          device, [n_src, T, d] sources (slice i at V + i*src_stride
+ *              elements), dtype v_dtype. Slice 0 is the embedding.
+ *   src_stride elements between consecutive sources, >= T*d.
+ *   n_src      number of sources, >= 1 (n_src == 1 returns v_0 exactly).
+ *   w, gamma   device, fp32 [d]: the read's pseudo-query and key-RMSNorm gain.
+ *   eps        RMSNorm epsilon, >= 0.
+ *   out        device, [T, d] of out_dtype; must not overlap V.
+ */
+int attnres_full_fwd(const void* V, int64_t src_stride, int32_t n_src, int64_t T,
+                     int32_t d, int32_t v_dtype, const float* w, const float* gamma,
+                     float eps, void* out, int32_t out_dtype, void* stream);
+
+/*
+ * attnres_full_pass - R consecutive Full AttnRes reads over one stored
+ * history: read r aggregates V[0 .. r] (r + 1 sources) with W[r], Gamma[r]
+ * and writes out + r*out_stride. This is the read sequence of a Full AttnRes
+ * model whose sublayer r's output is V[r + 1] (DepthBench reading notes
+ * section 2.3: the first sublayer reads the embedding alone; with R = 2L + 1
+ * the last read is the LM-head read).
+ *
+ *   V        device, [R, T, d] history, dtype v_dtype, src_stride >= T*d.
+ *   W, Gamma device, fp32 [R, d].
+ *   out      device, R outputs [T, d] of out_dtype, out_stride >= T*d
+ *            elements apart; must not overlap V.
+ */
+int attnres_full_pass(const void* V, int64_t src_stride, int32_t R, int64_t T,
+                      int32_t d, int32_t v_dtype, const float* W, const float* Gamma,
+                      float eps, void* out, int64_t out_stride, int32_t out_dtype,
+                      void* stream);
+
+/*
+ * attnres_block_stage1 - stage 1 of the two-stage Block AttnRes computation
+ * (datacamp explainer, "two-stage computation"): the S pseudo-queries of one
+ * block against the cross-block sources, each source row read once for all S.
+ *
+ *   Src        device, [n_src, T, d] cross-block sources (embedding, then the
+ *              completed block sums), dtype, src_stride >= T*d.
+ *   W, Gamma   device, fp32 [S, d], one row per sublayer of the block.
+ *   S          1 <= S <= ATTNRES_MAX_QUERIES.
+ *   O          host array of S device pointers; O[j] receives the normalised
+ *              read of query j over Src, [T, d] of dtype. For the first
+ *              sublayer of a block (empty running sum) O[0] is its final
+ *              output. O[j] must not overlap Src or each other.
+ *   lse        device, fp32 [S, T] (row j at lse + j*T): log sum_i exp(e_ij),
+ *              the softmax mass stage 2 merges on. May be NULL (not written).
+ */
+int attnres_block_stage1(const void* Src, int64_t src_stride, int32_t n_src, int64_t T,
+                         int32_t d, int32_t dtype, const float* W, const float* Gamma,
+                         int32_t S, float eps, void* const* O, float* lse, void* stream);
+
+/*
+ * attnres_block_merge - stage 2 for one sublayer: extend the block's running
+ * sum and merge it, as one more softmax source, with the stage-1 result
+ * (datacamp explainer, "two-stage computation": online-softmax merge of the
+ * intra-block dependency; DepthBench reading notes section 2.5: a read sees
+ * the embedding, the frozen blocks and the current running sum).
+ *
+ *   O_j, lse_j device, stage-1 output [T, d] (dtype) and fp32 [T] of this query.
+ *   P          device, fp32 [T, d] running sum, read and written in place.
+ *   f_prev     device, [T, d] dtype, or NULL. Non-NULL: P <- P + f_prev first
+ *              (P <- f_prev when p_is_empty != 0). NULL: P is used as it is
+ *              and is not written; p_is_empty must then be 0.
+ *   w, gamma   device, fp32 [d] of this sublayer.
+ *   out        device, [T, d] dtype: the sublayer's aggregated input.
+ *              out must not overlap O_j, P or f_prev.
+ */
+int attnres_block_merge(const void* O_j, const float* lse_j, float* P, const void* f_prev,
+                        int32_t p_is_empty, const float* w, const float* gamma, float eps,
+                        int64_t T, int32_t d, int32_t dtype, void* out, void* stream);
+
+/*
+ * attnres_block_summary_accumulate - running sum of a block and the block
+ * summary (LLMRes blog "Block Attention Residuals": a block is represented by
+ * the sum of its sublayer outputs; datacamp explainer: b_n = sum of the
+ * outputs of the layers in block n, with b_0 the embedding).
+ *
+ *   P            device, fp32 [T, d] running sum.
+ *   f            device, [T, d] dtype: a sublayer output to add.
+ *   p_is_empty   non-zero: the running sum is empty (treated as 0, P not read).
+ *   summary_out  NULL: accumulate, P <- P + f.
+ *                non-NULL: freeze, summary_out <- P + f rounded to dtype
+ *                ([T, d] dtype, device); P is then not written.
+ */
+int attnres_block_summary_accumulate(float* P, const void* f, int32_t p_is_empty,
+                                     void* summary_out, int64_t T, int32_t d, int32_t dtype,
+                                     void* stream);
+
+/*
+ * attnres_block_pass - the reads of N blocks of S sublayers by the two-stage
+ * computation, for stored sublayer outputs F (the synthetic sequencing a
+ * model would interleave with its sublayers). Block n (0-based) runs stage 1
+ * over Src[0 .. n], S - 1 merges and, unless it is the last block and
+ * freeze_last == 0, freezes its summary into Src[n + 1].
+ *
+ *   F           device, [N*S, T, d] sublayer outputs, dtype, f_stride >= T*d.
+ *   W, Gamma    device, fp32 [N*S, d].
+ *   Src         device, [N + freeze_last, T, d] dtype, src_stride >= T*d.
+ *               Src[0] holds the embedding (input); Src[1 ..] are written.
+ *   O_scratch   device, [max(S-1,1), T, d] dtype workspace (stage-1 results).
+ *   lse_scratch device, fp32 [S, T] workspace.
+ *   P_scratch   device, fp32 [T, d] workspace (running sum).
+ *   out         device, N*S outputs [T, d] dtype, out_stride >= T*d apart.
+ */
+int attnres_block_pass(const void* F, int64_t f_stride, int32_t N, int32_t S, int64_t T,
+                       int32_t d, int32_t dtype, const float* W, const float* Gamma,
+                       float eps, void* Src, int64_t src_stride, int32_t freeze_last,
+                       void* O_scratch, float* lse_scratch, float* P_scratch,
+                       void* out, int64_t out_stride, void* stream);
+
+/*
+ * attnres_device_status - synchronise `stream` and report device-side
+ * failures of earlier calls on the current device: ATTNRES_ERR_TIMEOUT if a
+ * kernel gave up a bounded wait since the last call (the record is then
+ * cleared), ATTNRES_ERR_CUDA on a pending CUDA error, else ATTNRES_OK.
+ */
+int attnres_device_status(void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* attnres_status_string(int32_t status);
+
+/*
+ * attnres_kernel_path - which kernel a call with these arguments would use:
+ * 1 = the fast kernel, 0 = the general kernel, negative = invalid arguments.
+ * op: 0 full read, 1 stage 1, 2 merge, 3 accumulate. Pointers are only
+ * inspected for alignment; n_or_s is n_src for op 0 and 1, ignored otherwise;
+ * s is S for op 1.
+ */
+int attnres_kernel_path(int32_t op, const void* src, const void* out, int32_t n_or_s,
+                        int32_t s, int64_t T, int32_t d, int32_t dtype);
+
+/* ABI version of this header: 1. */
+int attnres_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTNRES_H */

@@ -1,0 +1,91 @@
+"""The C ABI library builds, loads and exports every declared symbol (no GPU).
+
+Only host-side logic runs here: argument validation returns its status codes
+before any CUDA call, and kernel selection is a pure function of the
+arguments.
+"""
+import ctypes
+
+import pytest
+
+from depth_wise_attention_attnres_gb300 import binding, build
+
+INVALID, UNSUPPORTED = 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = binding.header_functions()
+    assert len(names) >= 10
+    handle = ctypes.CDLL(build.LIB)
+    missing = [n for n in names if not hasattr(handle, n)]
+    assert not missing, f"not exported: {missing}"
+    assert set(names) == set(binding._SIGNATURES)
+
+
+def test_version_and_status_strings(lib):
+    assert binding.attnres_abi_version() == 1
+    for code in range(5):
+        assert binding.status_string(code)
+    assert binding.status_string(99) == "unknown status"
+
+
+P = 1 << 20  # aligned stand-in pointers: validation never dereferences them
+
+
+@pytest.mark.parametrize("args,expect", [
+    # (V, stride, n_src, T, d, dtype, w, gamma, eps, out, out_dtype)
+    ((P, 64, 0, 4, 16, 1, P, P, 1e-6, 8 * P, 1), INVALID),          # n_src = 0
+    ((P, 64, 2, 4, 16, 1, P, P, -1.0, 8 * P, 1), INVALID),          # eps < 0
+    ((P, 64, 2, 4, 16, 7, P, P, 1e-6, 8 * P, 1), INVALID),          # bad dtype
+    ((P, 63, 2, 4, 16, 1, P, P, 1e-6, 8 * P, 1), INVALID),          # stride < T*d
+    ((P, 64, 2, 4, 16, 1, P, P, 1e-6, P + 64, 1), INVALID),         # out overlaps V
+    ((None, 64, 2, 4, 16, 1, P, P, 1e-6, 8 * P, 1), INVALID),       # null V
+    ((None, 0, 3, 0, 16, 1, None, None, 1e-6, None, 1), 0),         # T = 0: nothing to do
+])
+def test_full_fwd_validation(lib, args, expect):
+    assert lib.attnres_full_fwd(*args, None) == expect
+
+
+def test_other_entry_validation(lib):
+    ptrs = (ctypes.c_void_p * 2)(P * 8, P * 16)
+    # stage 1: S out of range, overlapping outputs
+    assert lib.attnres_block_stage1(P, 64, 2, 4, 16, 1, P, P, 0, 1e-6, ptrs, None, None) == INVALID
+    assert lib.attnres_block_stage1(P, 64, 2, 4, 16, 1, P, P, 17, 1e-6, ptrs, None, None) == INVALID
+    same = (ctypes.c_void_p * 2)(P * 8, P * 8)
+    assert lib.attnres_block_stage1(P, 64, 2, 4, 16, 1, P, P, 2, 1e-6, same, None, None) == INVALID
+    # merge: empty running sum needs f_prev; out must not alias P
+    assert lib.attnres_block_merge(P, 2 * P, 3 * P, None, 1, P, P, 1e-6, 4, 16, 1, 5 * P, None) == INVALID
+    assert lib.attnres_block_merge(P, 2 * P, 3 * P, None, 0, P, P, 1e-6, 4, 16, 1, 3 * P, None) == INVALID
+    # accumulate: summary aliasing f
+    assert lib.attnres_block_summary_accumulate(P, 2 * P, 0, 2 * P, 4, 16, 1, None) == INVALID
+    # passes
+    assert lib.attnres_full_pass(P, 64, 0, 4, 16, 1, P, P, 1e-6, 8 * P, 64, 1, None) == INVALID
+    assert lib.attnres_block_pass(P, 64, 0, 2, 4, 16, 1, P, P, 1e-6, 2 * P, 64, 0, 3 * P, 4 * P,
+                                  5 * P, 6 * P, 64, None) == INVALID
+
+
+def test_kernel_selection(lib):
+    A = 1 << 20
+    # Full read: d multiple of 128 and 16-byte alignment -> fast kernel.
+    assert binding.attnres_kernel_path(0, A, 2 * A, 8, 0, 8192, 896, 1) == 1
+    assert binding.attnres_kernel_path(0, A, 2 * A, 141, 0, 32768, 640, 1) == 1
+    assert binding.attnres_kernel_path(0, A, 2 * A, 8, 0, 256, 256, 0) == 1
+    assert binding.attnres_kernel_path(0, A + 2, 2 * A, 8, 0, 256, 256, 1) == 0   # misaligned
+    assert binding.attnres_kernel_path(0, A, 2 * A, 8, 0, 256, 100, 1) == 0       # d % 128
+    # Stage 1 at the block shapes of the standard workloads.
+    for n in range(1, 10):
+        assert binding.attnres_kernel_path(1, A, 2 * A, n, 8, 16384, 1024, 1) == 1
+        assert binding.attnres_kernel_path(1, A, 2 * A, n, 6, 131072, 2048, 1) == 1
+    assert binding.attnres_kernel_path(1, A, 2 * A, 4, 9, 16384, 1024, 1) == 0    # S > 8
+    # Merge and accumulate.
+    assert binding.attnres_kernel_path(2, A, 2 * A, 0, 0, 16384, 1024, 1) == 1
+    assert binding.attnres_kernel_path(2, A, 2 * A, 0, 0, 131072, 2048, 1) == 1
+    assert binding.attnres_kernel_path(3, A, 2 * A, 0, 0, 16384, 1024, 1) == 1
+    assert binding.attnres_kernel_path(2, A, 2 * A, 0, 0, 10, 3, 1) == 0
+    assert binding.attnres_kernel_path(9, A, 2 * A, 0, 0, 10, 3, 1) == -1
