@@ -36,16 +36,24 @@ int sm_count() {
   return n;
 }
 
+// Lets `kernel` use `bytes` of dynamic shared memory and asks for the largest
+// shared-memory carveout, so that the CTAs the occupancy allows fit. Done
+// once per (kernel, device); later calls only look the answer up.
 cudaError_t allow_dynamic_smem(const void* kernel, int bytes) {
-  if (bytes <= 48 * 1024) return cudaSuccess;
   const int dev = current_device();
   std::lock_guard<std::mutex> lk(g_mu);
   auto key = std::make_pair(kernel, dev);
   auto it = g_smem_set.find(key);
   if (it != g_smem_set.end() && it->second >= bytes) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) g_smem_set[key] = bytes;
-  return e;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  if (bytes > 48 * 1024) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+  }
+  g_smem_set[key] = bytes;
+  return cudaSuccess;
 }
 
 int blocks_per_sm(const void* kernel, int threads, int smem_bytes) {

@@ -128,6 +128,17 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream is still
+// running; pdl_wait() blocks until that kernel has completed and its memory
+// is visible, so every global access of a kernel comes after it. pdl_trigger()
+// lets the next kernel's CTAs be scheduled as this grid's CTAs retire.
+// Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Named barrier among `count` threads (a multiple of 32), id 1..15.
 __device__ __forceinline__ void named_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -143,6 +154,17 @@ __device__ __forceinline__ void lds4(const float* p, float (&x)[4]) {
 __device__ __forceinline__ void lds4(const bf16* p, float (&x)[4]) {
   uint2 v = *reinterpret_cast<const uint2*>(p);
   x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+}
+
+// 16 bytes (8 bf16 or 4 fp32) as floats from shared memory.
+__device__ __forceinline__ void lds16(const bf16* p, float (&x)[8]) {
+  const uint4 v = *reinterpret_cast<const uint4*>(p);
+  x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+  x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+}
+__device__ __forceinline__ void lds16(const float* p, float (&x)[4]) {
+  const float4 v = *reinterpret_cast<const float4*>(p);
+  x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
 }
 
 // Store 4 consecutive fp32 values as fp32 or bf16 (global memory).

@@ -33,29 +33,43 @@ constexpr int kBarBytes = 128;       // barrier area at the start of shared memo
 constexpr int kMaxStages = 8;
 constexpr int kSmemBudget = 112 * 1024;  // per CTA: two CTAs fit on one SM
 
+// Rows up to 1024 wide run two CTAs per SM (16 consumer warps hide the
+// latency of the per-source reduction chain); that caps registers at 112.
+template <int CH>
+struct FullTraits {
+  static constexpr int kMinBlocks = CH <= 8 ? 2 : 1;
+  // Keeping the converted row in registers saves a second shared read; for
+  // wider rows the registers go to the accumulator instead.
+  static constexpr bool kKeepX = CH <= 8;
+};
+
 template <typename Tin, int CH>
-__global__ void __launch_bounds__(kThreads) full_fwd_bulk_kernel(FullArgs a, int nstage) {
+__global__ void __launch_bounds__(kThreads, FullTraits<CH>::kMinBlocks)
+    full_fwd_bulk_kernel(FullArgs a, int nstage) {
   constexpr int D = CH * 128;
   constexpr int NE = CH * 4;         // elements per lane
-  // Keeping the converted row in registers saves a second shared read; for
-  // the widest rows the registers go to the accumulator instead.
-  constexpr bool kKeepX = CH <= 8;
+  constexpr bool kKeepX = FullTraits<CH>::kKeepX;
 
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty_bar = full_bar + kMaxStages;
-  Tin* stages = reinterpret_cast<Tin*>(smem + kBarBytes);
+  float* wq = reinterpret_cast<float*>(smem + kBarBytes);  // w * gamma, [D]
+  Tin* stages = reinterpret_cast<Tin*>(smem + kBarBytes + D * sizeof(float));
   constexpr int kStageElems = kTM * D;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t T = a.T;
+  // Contiguous rows [r0, r1) per CTA, cut into ntiles tiles whose sizes
+  // differ by at most one row (tile t starts at r0 + t * R / ntiles).
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * T / gridDim.x;
   const int64_t r1 = static_cast<int64_t>(blockIdx.x + 1) * T / gridDim.x;
-  const int ntiles = static_cast<int>((r1 - r0 + kTM - 1) / kTM);
+  const int R = static_cast<int>(r1 - r0);
+  const int ntiles = (R + kTM - 1) / kTM;
   const int n = a.n_src;
   const int64_t total = static_cast<int64_t>(ntiles) * n;
 
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < nstage; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
@@ -64,6 +78,7 @@ __global__ void __launch_bounds__(kThreads) full_fwd_bulk_kernel(FullArgs a, int
     mbar_fence_init();
   }
   __syncthreads();
+  pdl_wait();  // everything below may read what the previous kernel wrote
 
   if (warp == kNW) {
     // ------------------------------------------------------------ producer
@@ -82,8 +97,8 @@ __global__ void __launch_bounds__(kThreads) full_fwd_bulk_kernel(FullArgs a, int
       }
       const int tile = static_cast<int>(it / n);
       const int src = static_cast<int>(it - static_cast<int64_t>(tile) * n);
-      const int64_t row0 = r0 + static_cast<int64_t>(tile) * kTM;
-      const int rows = static_cast<int>(min(static_cast<int64_t>(kTM), r1 - row0));
+      const int64_t row0 = r0 + tile * R / ntiles;
+      const int rows = static_cast<int>(r0 + (tile + 1) * R / ntiles - row0);
       const uint32_t bytes = static_cast<uint32_t>(rows) * D * sizeof(Tin);
       const uint32_t fb = smem_u32(&full_bar[stage]);
       mbar_arrive_expect_tx(fb, bytes);
@@ -105,15 +120,13 @@ __global__ void __launch_bounds__(kThreads) full_fwd_bulk_kernel(FullArgs a, int
   }
 
   // -------------------------------------------------------------- consumers
-  float2 wq[NE / 2];  // w * gamma for this lane's elements
-#pragma unroll
-  for (int c = 0; c < CH; ++c) {
-    const int k = (c * kWarp + lane) * 4;
-    const float4 w4 = *reinterpret_cast<const float4*>(a.w + k);
-    const float4 g4 = *reinterpret_cast<const float4*>(a.gamma + k);
-    wq[c * 2] = make_float2(w4.x * g4.x, w4.y * g4.y);
-    wq[c * 2 + 1] = make_float2(w4.z * g4.z, w4.w * g4.w);
+  // w * gamma into shared memory; the producer is already streaming meanwhile.
+  for (int i = threadIdx.x; i < D / 4; i += kNW * kWarp) {
+    const float4 w4 = reinterpret_cast<const float4*>(a.w)[i];
+    const float4 g4 = reinterpret_cast<const float4*>(a.gamma)[i];
+    reinterpret_cast<float4*>(wq)[i] = make_float4(w4.x * g4.x, w4.y * g4.y, w4.z * g4.z, w4.w * g4.w);
   }
+  named_sync(1, kNW * kWarp);
   const float inv_d = 1.0f / static_cast<float>(D);
   const float eps = a.eps;
 
@@ -121,8 +134,9 @@ __global__ void __launch_bounds__(kThreads) full_fwd_bulk_kernel(FullArgs a, int
   uint32_t phase = 0;
   bool ok = true;
   for (int tile = 0; tile < ntiles && ok; ++tile) {
-    const int64_t row = r0 + static_cast<int64_t>(tile) * kTM + warp;
-    const bool valid = row < r1;
+    const int64_t row0 = r0 + tile * R / ntiles;
+    const int64_t row = row0 + warp;
+    const bool valid = row < r0 + (tile + 1) * R / ntiles;
     float2 acc[NE / 2];
 #pragma unroll
     for (int e = 0; e < NE / 2; ++e) acc[e] = make_float2(0.f, 0.f);
@@ -135,23 +149,24 @@ __global__ void __launch_bounds__(kThreads) full_fwd_bulk_kernel(FullArgs a, int
       }
       if (valid) {
         const Tin* rowp = stages + static_cast<size_t>(stage) * kStageElems + warp * D;
-        float x[NE];
+        float x[kKeepX ? NE : 4];
+        float2 ss2a = make_float2(0.f, 0.f), ss2b = ss2a, dt2a = ss2a, dt2b = ss2a;
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
           float t4[4];
           lds4(rowp + (c * kWarp + lane) * 4, t4);
-          x[c * 4 + 0] = t4[0]; x[c * 4 + 1] = t4[1]; x[c * 4 + 2] = t4[2]; x[c * 4 + 3] = t4[3];
-        }
-        float2 ss2a = make_float2(0.f, 0.f), ss2b = ss2a, dt2a = ss2a, dt2b = ss2a;
-#pragma unroll
-        for (int e = 0; e < NE / 2; e += 2) {
-          const float2 xa = make_float2(x[2 * e], x[2 * e + 1]);
-          const float2 xb = make_float2(x[2 * e + 2], x[2 * e + 3]);
+          if constexpr (kKeepX) {
+            x[c * 4 + 0] = t4[0]; x[c * 4 + 1] = t4[1]; x[c * 4 + 2] = t4[2]; x[c * 4 + 3] = t4[3];
+          }
+          const float2 xa = make_float2(t4[0], t4[1]);
+          const float2 xb = make_float2(t4[2], t4[3]);
           ss2a = ffma2(xa, xa, ss2a);
           ss2b = ffma2(xb, xb, ss2b);
-          dt2a = ffma2(wq[e], xa, dt2a);
-          dt2b = ffma2(wq[e + 1], xb, dt2b);
+          const float4 w4 = *reinterpret_cast<const float4*>(wq + (c * kWarp + lane) * 4);
+          dt2a = ffma2(make_float2(w4.x, w4.y), xa, dt2a);
+          dt2b = ffma2(make_float2(w4.z, w4.w), xb, dt2b);
         }
+        (void)x;
         const float ss = warp_sum((ss2a.x + ss2b.x) + (ss2a.y + ss2b.y));
         const float dot = warp_sum((dt2a.x + dt2b.x) + (dt2a.y + dt2b.y));
         const float s = dot * rsqrtf(ss * inv_d + eps);
@@ -208,9 +223,10 @@ template <typename Tin, int CH>
 cudaError_t launch_ch(const FullArgs& a, cudaStream_t s) {
   constexpr int D = CH * 128;
   const int stage_bytes = kTM * D * static_cast<int>(sizeof(Tin));
-  int nstage = (kSmemBudget - kBarBytes) / stage_bytes;
+  const int fixed = kBarBytes + D * static_cast<int>(sizeof(float));
+  int nstage = (kSmemBudget - fixed) / stage_bytes;
   nstage = nstage < 2 ? 2 : (nstage > kMaxStages ? kMaxStages : nstage);
-  const int smem = kBarBytes + nstage * stage_bytes;
+  const int smem = fixed + nstage * stage_bytes;
   const void* fn = reinterpret_cast<const void*>(&full_fwd_bulk_kernel<Tin, CH>);
   cudaError_t e = allow_dynamic_smem(fn, smem);
   if (e != cudaSuccess) return e;
@@ -218,8 +234,8 @@ cudaError_t launch_ch(const FullArgs& a, cudaStream_t s) {
   const int64_t tiles = (a.T + kTM - 1) / kTM;
   int64_t grid = static_cast<int64_t>(sm_count()) * (per_sm > 0 ? per_sm : 1);
   if (grid > tiles) grid = tiles;
-  full_fwd_bulk_kernel<Tin, CH><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(a, nstage);
-  return cudaGetLastError();
+  return launch_pdl(full_fwd_bulk_kernel<Tin, CH>, static_cast<unsigned>(grid), kThreads, smem, s, a,
+                    nstage);
 }
 
 template <typename Tin>

@@ -70,11 +70,15 @@ __device__ __forceinline__ void store_f32(float* p, const float (&x)[N]) {
   for (int q = 0; q < N; q += 4) *reinterpret_cast<float4*>(p + q) = make_float4(x[q], x[q + 1], x[q + 2], x[q + 3]);
 }
 
-// wpr: warps per row (power of two, <= 8); rows per block iteration = 8 / wpr.
+// wpr: warps per row (power of two, <= 8). A block iteration covers
+// kRows * (8 / wpr) rows; each thread handles one 16-byte chunk in kRows rows,
+// so all their loads are in flight before the reduction barrier.
+constexpr int kRows = 2;
+
 template <typename T>
 __global__ void __launch_bounds__(kBlock) merge_fast_kernel(MergeArgs a, int wpr) {
   constexpr int N = Chunk<T>::N;
-  __shared__ float red[2][kWarps][2];
+  __shared__ float red[2][kRows][kWarps][2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rpb = kWarps / wpr;
   const int slot = warp / wpr;
@@ -85,6 +89,8 @@ __global__ void __launch_bounds__(kBlock) merge_fast_kernel(MergeArgs a, int wpr
   const bool active = c < nchunk;
   const int k = c * N;
 
+  pdl_trigger();
+  pdl_wait();
   float wq[N];
   if (active) {
 #pragma unroll
@@ -92,48 +98,61 @@ __global__ void __launch_bounds__(kBlock) merge_fast_kernel(MergeArgs a, int wpr
   }
   const float inv_d = 1.0f / static_cast<float>(d);
   int par = 0;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * rpb; base < a.T;
-       base += static_cast<int64_t>(gridDim.x) * rpb, par ^= 1) {
-    const int64_t row = base + slot;
-    const bool live = active && row < a.T;
-    float p[N], o[N];
-    float ss = 0.f, dot = 0.f;
-    if (live) {
-      const int64_t off = row * d + k;
-      if (a.f) {
-        float f[N];
-        Chunk<T>::load(static_cast<const T*>(a.f) + off, f);
-        if (a.p_empty) {
+  const int64_t step = static_cast<int64_t>(gridDim.x) * rpb * kRows;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * rpb * kRows; base < a.T; base += step, par ^= 1) {
+    float p[kRows][N], o[kRows][N];
+    bool live[kRows];
 #pragma unroll
-          for (int q = 0; q < N; ++q) p[q] = f[q];
+    for (int r = 0; r < kRows; ++r) {
+      const int64_t row = base + r * rpb + slot;
+      live[r] = active && row < a.T;
+      if (live[r]) {
+        const int64_t off = row * d + k;
+        Chunk<T>::load(static_cast<const T*>(a.O) + off, o[r]);
+        if (a.f) {
+          float f[N];
+          Chunk<T>::load(static_cast<const T*>(a.f) + off, f);
+          if (a.p_empty) {
+#pragma unroll
+            for (int q = 0; q < N; ++q) p[r][q] = f[q];
+          } else {
+            load_f32<N>(a.P + off, p[r]);
+#pragma unroll
+            for (int q = 0; q < N; ++q) p[r][q] += f[q];
+          }
         } else {
-          load_f32<N>(a.P + off, p);
-#pragma unroll
-          for (int q = 0; q < N; ++q) p[q] += f[q];
+          load_f32<N>(a.P + off, p[r]);
         }
-        store_f32<N>(a.P + off, p);
-      } else {
-        load_f32<N>(a.P + off, p);
-      }
-      Chunk<T>::load(static_cast<const T*>(a.O) + off, o);
-#pragma unroll
-      for (int q = 0; q < N; ++q) {
-        ss = fmaf(p[q], p[q], ss);
-        dot = fmaf(wq[q], p[q], dot);
       }
     }
-    ss = warp_sum(ss);
-    dot = warp_sum(dot);
-    if (lane == 0) {
-      red[par][warp][0] = ss;
-      red[par][warp][1] = dot;
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      float ss = 0.f, dot = 0.f;
+      if (live[r]) {
+        const int64_t off = (base + r * rpb + slot) * d + k;
+        if (a.f) store_f32<N>(a.P + off, p[r]);
+#pragma unroll
+        for (int q = 0; q < N; ++q) {
+          ss = fmaf(p[r][q], p[r][q], ss);
+          dot = fmaf(wq[q], p[r][q], dot);
+        }
+      }
+      ss = warp_sum(ss);
+      dot = warp_sum(dot);
+      if (lane == 0) {
+        red[par][r][warp][0] = ss;
+        red[par][r][warp][1] = dot;
+      }
     }
     __syncthreads();
-    if (live) {
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      if (!live[r]) continue;
+      const int64_t row = base + r * rpb + slot;
       float tss = 0.f, tdot = 0.f;
       for (int w = 0; w < wpr; ++w) {
-        tss += red[par][slot * wpr + w][0];
-        tdot += red[par][slot * wpr + w][1];
+        tss += red[par][r][slot * wpr + w][0];
+        tdot += red[par][r][slot * wpr + w][1];
       }
       const float s = tdot * rsqrtf(tss * inv_d + a.eps);
       const float lse = a.lse[row];
@@ -141,10 +160,10 @@ __global__ void __launch_bounds__(kBlock) merge_fast_kernel(MergeArgs a, int wpr
       const float ea = __expf(lse - M), eb = __expf(s - M);
       const float inv = 1.0f / (ea + eb);
       const float ca = ea * inv, cb = eb * inv;
-      float r[N];
+      float res[N];
 #pragma unroll
-      for (int q = 0; q < N; ++q) r[q] = fmaf(ca, o[q], cb * p[q]);
-      Chunk<T>::store(static_cast<T*>(a.out) + row * d + k, r);
+      for (int q = 0; q < N; ++q) res[q] = fmaf(ca, o[r][q], cb * p[r][q]);
+      Chunk<T>::store(static_cast<T*>(a.out) + row * d + k, res);
     }
   }
 }
@@ -192,6 +211,8 @@ __global__ void __launch_bounds__(kBlock) merge_generic_kernel(MergeArgs a) {
 template <typename T>
 __global__ void __launch_bounds__(kBlock) accum_fast_kernel(AccumArgs a, int64_t nchunks) {
   constexpr int N = Chunk<T>::N;
+  pdl_trigger();
+  pdl_wait();
   for (int64_t c = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x; c < nchunks;
        c += static_cast<int64_t>(gridDim.x) * kBlock) {
     const int64_t off = c * N;
@@ -233,9 +254,10 @@ int merge_wpr(int d, int bf16) {
   return wpr;
 }
 
-unsigned grid_for(int64_t work_items, int per_block) {
+// Enough blocks for the work, at most one resident wave of `kernel`.
+unsigned grid_for(int64_t work_items, int per_block, const void* kernel) {
   int64_t blocks = (work_items + per_block - 1) / per_block;
-  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * blocks_per_sm(kernel, kBlock, 0);
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   return static_cast<unsigned>(blocks);
@@ -258,17 +280,20 @@ bool accum_fast_ok(const AccumArgs& a) {
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s, bool fast) {
   if (fast) {
     const int wpr = merge_wpr(a.d, a.bf16);
-    const unsigned grid = grid_for(a.T, kWarps / wpr);
-    if (a.bf16)
-      merge_fast_kernel<bf16><<<grid, kBlock, 0, s>>>(a, wpr);
-    else
-      merge_fast_kernel<float><<<grid, kBlock, 0, s>>>(a, wpr);
+    const int rows_per_block = kWarps / wpr * kRows;
+    if (a.bf16) {
+      auto k = merge_fast_kernel<bf16>;
+      return launch_pdl(k, grid_for(a.T, rows_per_block, reinterpret_cast<const void*>(k)), kBlock, 0, s, a, wpr);
+    }
+    auto k = merge_fast_kernel<float>;
+    return launch_pdl(k, grid_for(a.T, rows_per_block, reinterpret_cast<const void*>(k)), kBlock, 0, s, a, wpr);
+  }
+  if (a.bf16) {
+    auto k = merge_generic_kernel<bf16>;
+    k<<<grid_for(a.T, kWarps, reinterpret_cast<const void*>(k)), kBlock, 0, s>>>(a);
   } else {
-    const unsigned grid = grid_for(a.T, kWarps);
-    if (a.bf16)
-      merge_generic_kernel<bf16><<<grid, kBlock, 0, s>>>(a);
-    else
-      merge_generic_kernel<float><<<grid, kBlock, 0, s>>>(a);
+    auto k = merge_generic_kernel<float>;
+    k<<<grid_for(a.T, kWarps, reinterpret_cast<const void*>(k)), kBlock, 0, s>>>(a);
   }
   return cudaGetLastError();
 }
@@ -276,19 +301,20 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s, bool fast) {
 cudaError_t launch_accum(const AccumArgs& a, cudaStream_t s, bool fast) {
   const int64_t total = a.T * a.d;
   if (fast) {
-    const int n = a.bf16 ? 8 : 4;
-    const int64_t nchunks = total / n;
-    const unsigned grid = grid_for(nchunks, kBlock);
-    if (a.bf16)
-      accum_fast_kernel<bf16><<<grid, kBlock, 0, s>>>(a, nchunks);
-    else
-      accum_fast_kernel<float><<<grid, kBlock, 0, s>>>(a, nchunks);
+    const int64_t nchunks = total / (a.bf16 ? 8 : 4);
+    if (a.bf16) {
+      auto k = accum_fast_kernel<bf16>;
+      return launch_pdl(k, grid_for(nchunks, kBlock, reinterpret_cast<const void*>(k)), kBlock, 0, s, a, nchunks);
+    }
+    auto k = accum_fast_kernel<float>;
+    return launch_pdl(k, grid_for(nchunks, kBlock, reinterpret_cast<const void*>(k)), kBlock, 0, s, a, nchunks);
+  }
+  if (a.bf16) {
+    auto k = accum_generic_kernel<bf16>;
+    k<<<grid_for(total, kBlock, reinterpret_cast<const void*>(k)), kBlock, 0, s>>>(a, total);
   } else {
-    const unsigned grid = grid_for(total, kBlock);
-    if (a.bf16)
-      accum_generic_kernel<bf16><<<grid, kBlock, 0, s>>>(a, total);
-    else
-      accum_generic_kernel<float><<<grid, kBlock, 0, s>>>(a, total);
+    auto k = accum_generic_kernel<float>;
+    k<<<grid_for(total, kBlock, reinterpret_cast<const void*>(k)), kBlock, 0, s>>>(a, total);
   }
   return cudaGetLastError();
 }

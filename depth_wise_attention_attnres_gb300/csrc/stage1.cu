@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_kernel(MultiArgs a, Stage1
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * ntiles_total / gridDim.x;
   const int64_t t1 = static_cast<int64_t>(blockIdx.x + 1) * ntiles_total / gridDim.x;
 
+  pdl_trigger();
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&full_bar[b]), 1);
@@ -93,6 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_kernel(MultiArgs a, Stage1
     *reinterpret_cast<int*>(full_bar + 4) = 0;  // consumer abort flag
     mbar_fence_init();
   }
+  pdl_wait();  // global reads below may depend on the previous kernel
   // w * gamma for the S queries of the block.
   for (int idx = tid; idx < S * d / 4; idx += kThreads) {
     const float4 w4 = reinterpret_cast<const float4*>(a.W)[idx];
@@ -170,12 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_kernel(MultiArgs a, Stage1
       for (int j = 0; j < S; ++j) dt2[j] = make_float2(0.f, 0.f);
       for (int kk = 0; kk < KW; kk += VEC) {
         float x[VEC];
-#pragma unroll
-        for (int q = 0; q < VEC; q += 4) {
-          float t4[4];
-          lds4(rowp + kk + q, t4);
-          x[q] = t4[0]; x[q + 1] = t4[1]; x[q + 2] = t4[2]; x[q + 3] = t4[3];
-        }
+        lds16(rowp + kk, x);  // one 16-byte load: 8 lanes per wavefront, no conflicts
 #pragma unroll
         for (int q = 0; q < VEC; q += 2) ss2 = ffma2(make_float2(x[q], x[q + 1]), make_float2(x[q], x[q + 1]), ss2);
 #pragma unroll
@@ -289,10 +286,8 @@ cudaError_t launch_s(const MultiArgs& a, const Stage1Geom& g, cudaStream_t s) {
   int64_t grid = sm_count();
   if (grid > tiles) grid = tiles;
   if (cpt == 1)
-    stage1_kernel<Tin, S, 1><<<static_cast<unsigned>(grid), kThreads, g.total, s>>>(a, g);
-  else
-    stage1_kernel<Tin, S, 2><<<static_cast<unsigned>(grid), kThreads, g.total, s>>>(a, g);
-  return cudaGetLastError();
+    return launch_pdl(stage1_kernel<Tin, S, 1>, static_cast<unsigned>(grid), kThreads, g.total, s, a, g);
+  return launch_pdl(stage1_kernel<Tin, S, 2>, static_cast<unsigned>(grid), kThreads, g.total, s, a, g);
 }
 
 template <typename Tin>
