@@ -34,6 +34,8 @@ _SIGNATURES = {
     "attnres_block_summary_accumulate": [_VP, _VP, _I32, _VP, _I64, _I32, _I32, _VP],
     "attnres_block_pass": [_VP, _I64, _I32, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _I64,
                            _I32, _VP, _VP, _VP, _VP, _I64, _VP],
+    "attnres_block_pass_noalloc": [_VP, _I64, _I32, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP,
+                                   _I64, _I32, _VP, _I64, _VP],
     "attnres_device_status": [_VP],
     "attnres_status_string": [_I32],
     "attnres_kernel_path": [_I32, _VP, _VP, _I32, _I32, _I64, _I32, _I32],
@@ -197,6 +199,19 @@ def attnres_block_pass(F: torch.Tensor, N: int, S: int, W: torch.Tensor, Gamma: 
         _ptr(F), fstride, N, S, T, d, _dtype(F), _ptr(W), _ptr(Gamma), eps, _ptr(Src), sstride,
         int(bool(freeze_last)), _ptr(O_scratch), _ptr(lse_scratch), _ptr(P_scratch), _ptr(out),
         ostride, _stream(stream)))
+    return out
+
+
+def attnres_block_pass_noalloc(F: torch.Tensor, N: int, S: int, W: torch.Tensor,
+                               Gamma: torch.Tensor, eps: float, Src: torch.Tensor, out: torch.Tensor,
+                               freeze_last: bool = False, stream=None) -> torch.Tensor:
+    """The Block pass with the library's own fixed workspace (no allocation)."""
+    _, T, d, fstride = _slices(F)
+    _, _, _, sstride = _slices(Src)
+    _, _, _, ostride = _slices(out)
+    _check("attnres_block_pass_noalloc", lib().attnres_block_pass_noalloc(
+        _ptr(F), fstride, N, S, T, d, _dtype(F), _ptr(W), _ptr(Gamma), eps, _ptr(Src), sstride,
+        int(bool(freeze_last)), _ptr(out), ostride, _stream(stream)))
     return out
 
 

@@ -187,6 +187,45 @@ int attnres_block_pass(const void* F, int64_t f_stride, int32_t N, int32_t S, in
                        void* out, int64_t out_stride, void* stream);
 
 /*
+ * attnres_block_pass_noalloc - attnres_block_pass for callers that cannot
+ * allocate device memory. (The pages have no counterpart: this is a library
+ * convenience, not part of the method.)
+ *
+ * Some callers have no device memory to lend as workspace and may not call
+ * cudaMalloc: a serving process that reserves and budgets all device memory
+ * up front and forbids allocation afterwards, or a caller running on a thread
+ * that must never make a call that can implicitly synchronise the device,
+ * which cudaMalloc and cudaFree can do. This entry point takes the same
+ * inputs and outputs as attnres_block_pass (F, W, Gamma, Src, out) but no
+ * workspace: the stage-1 results, their log-masses and the fp32 running sum
+ * live in one array of ATTNRES_NOALLOC_SCRATCH_BYTES bytes that the library
+ * defines at file scope. It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ *   - Size limit: the workspace of a call needs
+ *     (S > 1 ? (S-1)*T*d*es + 4*T*d : 0) + 4*S*T bytes (es = 2 for bf16, 4
+ *     for fp32; each part rounded up to 256 bytes). A call that needs more
+ *     than ATTNRES_NOALLOC_SCRATCH_BYTES returns ATTNRES_ERR_UNSUPPORTED and
+ *     launches nothing. Example: bf16, d = 1024, S = 8 fits up to T = 3600.
+ *   - Memory: every GPU on which the library is used holds the array
+ *     (64 MiB) from the first use until the process exits.
+ *   - Set-up: the first call on a device, with that device current, looks up
+ *     the array's device address (cudaGetSymbolAddress) and caches it. Make
+ *     that first call before any stream capture begins.
+ *   - Sharing: all calls on a device share the one array, and it keeps the
+ *     contents of the last call. Nothing in it needs to start at zero (every
+ *     byte a call reads was written earlier in the same call). Calls whose
+ *     work overlaps on the GPU (for example on two streams) race on the
+ *     array: order them on one stream or with events.
+ *   - Otherwise as attnres_block_pass (same arguments, checks and statuses).
+ */
+#define ATTNRES_NOALLOC_SCRATCH_BYTES (64ull * 1024ull * 1024ull)
+int attnres_block_pass_noalloc(const void* F, int64_t f_stride, int32_t N, int32_t S, int64_t T,
+                               int32_t d, int32_t dtype, const float* W, const float* Gamma,
+                               float eps, void* Src, int64_t src_stride, int32_t freeze_last,
+                               void* out, int64_t out_stride, void* stream);
+
+/*
  * attnres_device_status - synchronise `stream` and report device-side
  * failures of earlier calls on the current device: ATTNRES_ERR_TIMEOUT if a
  * kernel gave up a bounded wait since the last call (the record is then
