@@ -83,6 +83,7 @@ cudaError_t launch_accum(const AccumArgs& a, cudaStream_t s, bool fast);
 // Device-side timeout records of each kernel file: read and clear (blocking).
 cudaError_t take_timeout_full(unsigned int* flag);
 cudaError_t take_timeout_stage1(unsigned int* flag);
+cudaError_t take_timeout_merge(unsigned int* flag);
 
 // Shared launch helpers (api.cu).
 int sm_count();

@@ -12,10 +12,18 @@
 // block is represented by the sum of its outputs): P <- P + f, or
 // summary <- round(P + f).
 //
-// Both are HBM-bound streaming kernels (a few flops per byte). The fast merge
-// gives each thread one 16-byte chunk of a row (8 bf16 or 4 fp32 features),
-// reduces the two row sums over the row's warps through shared memory and
-// writes P and out with 16-byte stores.
+// Both are HBM-bound streaming kernels (a few flops per byte).
+//
+// The fast merge uses the same pipeline as the Full read: per CTA a producer
+// warp moves tiles of TM consecutive token rows of O, f and P (each tile of
+// each stream is one contiguous byte range, so one 1-D bulk copy on the TMA
+// engine) into a ring of shared-memory stages guarded by mbarriers; bulk
+// copies keep far more bytes in flight than per-thread loads can. Eight
+// consumer warps split the tile: 8/TM warps per row, each owning a contiguous
+// part of the row, lane l holding its 4-feature chunks l, l+32, ... (8-byte
+// bf16 and 16-byte fp32 shared loads, free of bank conflicts). The parts of a
+// row combine their two sums through shared memory behind a named barrier of
+// just that row's warps. P and out leave with coalesced 16/8-byte stores.
 #include <math.h>
 
 #include "common.cuh"
@@ -29,143 +37,214 @@ constexpr int kWarps = kBlock / 32;
 
 // ------------------------------------------------------------- fast merge --
 
-template <typename T>
-struct Chunk;
-template <>
-struct Chunk<bf16> {
-  static constexpr int N = 8;
-  __device__ static void load(const void* p, float (&x)[8]) {
-    const uint4 v = *reinterpret_cast<const uint4*>(p);
-    x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
-    x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
-  }
-  __device__ static void store(void* p, const float (&x)[8]) {
-    *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
-                                              pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
-  }
-};
-template <>
-struct Chunk<float> {
-  static constexpr int N = 4;
-  __device__ static void load(const void* p, float (&x)[4]) {
-    const float4 v = *reinterpret_cast<const float4*>(p);
-    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-  }
-  __device__ static void store(void* p, const float (&x)[4]) {
-    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
-  }
-};
-
-template <int N>
-__device__ __forceinline__ void load_f32(const float* p, float (&x)[N]) {
-#pragma unroll
-  for (int q = 0; q < N; q += 4) {
-    const float4 v = *reinterpret_cast<const float4*>(p + q);
-    x[q] = v.x; x[q + 1] = v.y; x[q + 2] = v.z; x[q + 3] = v.w;
-  }
+// 4 consecutive features: bf16 as 8 bytes, fp32 as 16 bytes (global memory).
+__device__ __forceinline__ void ldg4(const bf16* p, float (&x)[4]) {
+  const uint2 v = *reinterpret_cast<const uint2*>(p);
+  x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
 }
-template <int N>
-__device__ __forceinline__ void store_f32(float* p, const float (&x)[N]) {
-#pragma unroll
-  for (int q = 0; q < N; q += 4) *reinterpret_cast<float4*>(p + q) = make_float4(x[q], x[q + 1], x[q + 2], x[q + 3]);
+__device__ __forceinline__ void ldg4(const float* p, float (&x)[4]) {
+  const float4 v = *reinterpret_cast<const float4*>(p);
+  x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
 }
 
-// wpr: warps per row (power of two, <= 8). A block iteration covers
-// kRows * (8 / wpr) rows; each thread handles one 16-byte chunk in kRows rows,
-// so all their loads are in flight before the reduction barrier.
-constexpr int kRows = 2;
+__device__ unsigned int g_merge_timeout = 0;
 
-template <typename T>
-__global__ void __launch_bounds__(kBlock) merge_fast_kernel(MergeArgs a, int wpr) {
-  constexpr int N = Chunk<T>::N;
-  __shared__ float red[2][kRows][kWarps][2];
+constexpr int kMNW = 8;                      // consumer warps
+constexpr int kMThreads = (kMNW + 1) * 32;   // + producer warp
+constexpr int kMStages = 3;
+constexpr int kMBar = 128;                   // barrier area
+constexpr int kMStageBudget = 34 * 1024;     // bytes of one stage (TM rows)
+
+struct MergeGeom {
+  int TM;          // rows per tile (1, 2, 4 or 8)
+  int wpr;         // consumer warps per row = 8 / TM
+  int stage_bytes;
+  int wq_off, red_off, stage_off, total;
+};
+
+inline MergeGeom merge_geom(int d, int es) {
+  MergeGeom g{};
+  const int row_bytes = d * (2 * es + 4);
+  g.TM = 8;
+  while (g.TM > 1 && g.TM * row_bytes > kMStageBudget) g.TM >>= 1;
+  g.wpr = kMNW / g.TM;
+  g.stage_bytes = g.TM * row_bytes;
+  g.wq_off = kMBar;
+  g.red_off = g.wq_off + d * 4;
+  g.stage_off = (g.red_off + kMNW * 3 * 4 + 127) / 128 * 128;
+  g.total = g.stage_off + kMStages * g.stage_bytes;
+  return g;
+}
+
+// Q = 4-feature chunks per lane (a warp covers at most 128 * Q features).
+template <typename T, int Q>
+__global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, MergeGeom g) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty_bar = full_bar + kMStages;
+  float* wq = reinterpret_cast<float*>(smem + g.wq_off);
+  float* red = reinterpret_cast<float*>(smem + g.red_off);  // [kMNW][3]
+  unsigned char* stages = smem + g.stage_off;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rpb = kWarps / wpr;
-  const int slot = warp / wpr;
-  const int wr = warp - slot * wpr;
-  const int d = a.d;
-  const int nchunk = d / N;
-  const int c = wr * 32 + lane;
-  const bool active = c < nchunk;
-  const int k = c * N;
+  const int d = a.d, TM = g.TM;
+  const uint32_t row_t = static_cast<uint32_t>(d) * sizeof(T);
+  const uint32_t row_p = static_cast<uint32_t>(d) * 4u;
+  const bool with_f = a.f != nullptr;
+  const bool with_p = !(with_f && a.p_empty);
+  const int64_t ntok = a.T;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * ntok / gridDim.x;
+  const int64_t r1 = static_cast<int64_t>(blockIdx.x + 1) * ntok / gridDim.x;
+  const int R = static_cast<int>(r1 - r0);
+  const int ntiles = (R + TM - 1) / TM;
 
   pdl_trigger();
-  pdl_wait();
-  float wq[N];
-  if (active) {
-#pragma unroll
-    for (int q = 0; q < N; ++q) wq[q] = a.w[k + q] * a.gamma[k + q];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMStages; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), kMNW);
+    }
+    mbar_fence_init();
   }
+  __syncthreads();
+  pdl_wait();
+
+  if (warp == kMNW) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    int s = 0;
+    uint32_t phase = 0;
+    int issued = 0;
+    bool ok = true;
+    for (int t = 0; t < ntiles; ++t) {
+      if (!mbar_wait(smem_u32(&empty_bar[s]), phase ^ 1u)) {
+        ok = false;
+        break;
+      }
+      const int64_t row0 = r0 + static_cast<int64_t>(t) * R / ntiles;
+      const uint32_t rows = static_cast<uint32_t>(r0 + static_cast<int64_t>(t + 1) * R / ntiles - row0);
+      unsigned char* st = stages + static_cast<size_t>(s) * g.stage_bytes;
+      const uint32_t fb = smem_u32(&full_bar[s]);
+      mbar_arrive_expect_tx(fb, rows * (row_t + (with_f ? row_t : 0u) + (with_p ? row_p : 0u)));
+      bulk_g2s(smem_u32(st), static_cast<const T*>(a.O) + row0 * d, rows * row_t, fb);
+      if (with_f)
+        bulk_g2s(smem_u32(st + TM * row_t), static_cast<const T*>(a.f) + row0 * d, rows * row_t, fb);
+      if (with_p) bulk_g2s(smem_u32(st + 2 * TM * row_t), a.P + row0 * d, rows * row_p, fb);
+      ++issued;
+      if (++s == kMStages) {
+        s = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) {
+      atomicOr(&g_merge_timeout, 1u);
+      for (int it = issued > kMStages ? issued - kMStages : 0; it < issued; ++it)
+        (void)mbar_wait(smem_u32(&full_bar[it % kMStages]), static_cast<uint32_t>((it / kMStages) & 1));
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  for (int i = threadIdx.x; i < d; i += kMNW * 32) wq[i] = a.w[i] * a.gamma[i];
+  named_sync(1, kMNW * 32);
+  const int wpr = g.wpr;
+  const int rslot = warp / wpr;                     // row of the tile
+  const int part = warp - rslot * wpr;              // part of the row
+  const int span = (d + wpr - 1) / wpr;             // features per part
+  const int kbeg = part * span;
+  const int kend = min(d, kbeg + span);
   const float inv_d = 1.0f / static_cast<float>(d);
-  int par = 0;
-  const int64_t step = static_cast<int64_t>(gridDim.x) * rpb * kRows;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * rpb * kRows; base < a.T; base += step, par ^= 1) {
-    float p[kRows][N], o[kRows][N];
-    bool live[kRows];
+  int s = 0;
+  uint32_t phase = 0;
+  bool ok = true;
+  for (int t = 0; t < ntiles; ++t) {
+    const int64_t row0 = r0 + static_cast<int64_t>(t) * R / ntiles;
+    const int rows = static_cast<int>(r0 + static_cast<int64_t>(t + 1) * R / ntiles - row0);
+    const bool live = rslot < rows;
+    const int64_t row = row0 + rslot;
+    const float lse = live ? a.lse[row] : 0.f;
+    // A wait that runs out is first decided per warp; the warps of a row
+    // publish their outcome with their sums, so that they stop together after
+    // this tile and none is left waiting at the row's named barrier.
+    const bool wok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[s]), phase));
+    const unsigned char* st = stages + static_cast<size_t>(s) * g.stage_bytes;
+    const T* so = reinterpret_cast<const T*>(st) + rslot * d;
+    const T* sf = reinterpret_cast<const T*>(st + TM * row_t) + rslot * d;
+    const float* sp = reinterpret_cast<const float*>(st + 2 * TM * row_t) + rslot * d;
+    float p[Q][4];
+    float ss = 0.f, dot = 0.f;
+    if (wok && live) {
 #pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-      const int64_t row = base + r * rpb + slot;
-      live[r] = active && row < a.T;
-      if (live[r]) {
-        const int64_t off = row * d + k;
-        Chunk<T>::load(static_cast<const T*>(a.O) + off, o[r]);
-        if (a.f) {
-          float f[N];
-          Chunk<T>::load(static_cast<const T*>(a.f) + off, f);
-          if (a.p_empty) {
-#pragma unroll
-            for (int q = 0; q < N; ++q) p[r][q] = f[q];
+      for (int q = 0; q < Q; ++q) {
+        const int k = kbeg + (q * 32 + lane) * 4;
+        if (k < kend) {
+          if (with_p) {
+            lds4(sp + k, p[q]);
           } else {
-            load_f32<N>(a.P + off, p[r]);
-#pragma unroll
-            for (int q = 0; q < N; ++q) p[r][q] += f[q];
+            p[q][0] = p[q][1] = p[q][2] = p[q][3] = 0.f;
           }
-        } else {
-          load_f32<N>(a.P + off, p[r]);
+          if (with_f) {
+            float f[4];
+            lds4(sf + k, f);
+            p[q][0] += f[0]; p[q][1] += f[1]; p[q][2] += f[2]; p[q][3] += f[3];
+            st4(a.P + row * d + k, p[q]);
+          }
+          const float4 w4 = *reinterpret_cast<const float4*>(wq + k);
+          ss = fmaf(p[q][0], p[q][0], ss); ss = fmaf(p[q][1], p[q][1], ss);
+          ss = fmaf(p[q][2], p[q][2], ss); ss = fmaf(p[q][3], p[q][3], ss);
+          dot = fmaf(w4.x, p[q][0], dot); dot = fmaf(w4.y, p[q][1], dot);
+          dot = fmaf(w4.z, p[q][2], dot); dot = fmaf(w4.w, p[q][3], dot);
         }
       }
     }
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-      float ss = 0.f, dot = 0.f;
-      if (live[r]) {
-        const int64_t off = (base + r * rpb + slot) * d + k;
-        if (a.f) store_f32<N>(a.P + off, p[r]);
-#pragma unroll
-        for (int q = 0; q < N; ++q) {
-          ss = fmaf(p[r][q], p[r][q], ss);
-          dot = fmaf(wq[q], p[r][q], dot);
-        }
-      }
-      ss = warp_sum(ss);
-      dot = warp_sum(dot);
+    ss = warp_sum(ss);
+    dot = warp_sum(dot);
+    bool rok = wok;
+    if (wpr > 1) {
       if (lane == 0) {
-        red[par][r][warp][0] = ss;
-        red[par][r][warp][1] = dot;
+        red[warp * 3] = ss;
+        red[warp * 3 + 1] = dot;
+        red[warp * 3 + 2] = wok ? 1.f : 0.f;
+      }
+      named_sync(2 + rslot, wpr * 32);   // only the warps of this row
+      ss = 0.f;
+      dot = 0.f;
+      for (int w = 0; w < wpr; ++w) {
+        ss += red[(rslot * wpr + w) * 3];
+        dot += red[(rslot * wpr + w) * 3 + 1];
+        rok = rok && red[(rslot * wpr + w) * 3 + 2] != 0.f;
       }
     }
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-      if (!live[r]) continue;
-      const int64_t row = base + r * rpb + slot;
-      float tss = 0.f, tdot = 0.f;
-      for (int w = 0; w < wpr; ++w) {
-        tss += red[par][r][slot * wpr + w][0];
-        tdot += red[par][r][slot * wpr + w][1];
-      }
-      const float s = tdot * rsqrtf(tss * inv_d + a.eps);
-      const float lse = a.lse[row];
-      const float M = fmaxf(lse, s);
-      const float ea = __expf(lse - M), eb = __expf(s - M);
+    if (rok && live) {
+      const float sP = dot * rsqrtf(ss * inv_d + a.eps);
+      const float M = fmaxf(lse, sP);
+      const float ea = __expf(lse - M), eb = __expf(sP - M);
       const float inv = 1.0f / (ea + eb);
       const float ca = ea * inv, cb = eb * inv;
-      float res[N];
 #pragma unroll
-      for (int q = 0; q < N; ++q) res[q] = fmaf(ca, o[r][q], cb * p[r][q]);
-      Chunk<T>::store(static_cast<T*>(a.out) + row * d + k, res);
+      for (int q = 0; q < Q; ++q) {
+        const int k = kbeg + (q * 32 + lane) * 4;
+        if (k < kend) {
+          float x[4];
+          lds4(so + k, x);
+          const float r[4] = {fmaf(ca, x[0], cb * p[q][0]), fmaf(ca, x[1], cb * p[q][1]),
+                              fmaf(ca, x[2], cb * p[q][2]), fmaf(ca, x[3], cb * p[q][3])};
+          st4(static_cast<T*>(a.out) + row * d + k, r);
+        }
+      }
+    }
+    if (wpr > 1) named_sync(2 + rslot, wpr * 32);  // partners are done reading red[]
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
+    if (++s == kMStages) {
+      s = 0;
+      phase ^= 1u;
+    }
+    if (!rok) {
+      ok = false;
+      break;
     }
   }
+  if (!ok && lane == 0) atomicOr(&g_merge_timeout, 1u);
 }
 
 // ---------------------------------------------------------- general merge --
@@ -194,7 +273,7 @@ __global__ void __launch_bounds__(kBlock) merge_generic_kernel(MergeArgs a) {
     ss = warp_sum(ss);
     dot = warp_sum(dot);
     const float s = dot * rsqrtf(ss * inv_d + a.eps);
-    const float lse = a.lse[row];
+    const float lse = a.lse[row];  // general path: simplicity over latency
     const float M = fmaxf(lse, s);
     const float ea = __expf(lse - M), eb = __expf(s - M);
     const float inv = 1.0f / (ea + eb);
@@ -210,26 +289,23 @@ __global__ void __launch_bounds__(kBlock) merge_generic_kernel(MergeArgs a) {
 
 template <typename T>
 __global__ void __launch_bounds__(kBlock) accum_fast_kernel(AccumArgs a, int64_t nchunks) {
-  constexpr int N = Chunk<T>::N;
   pdl_trigger();
   pdl_wait();
   for (int64_t c = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x; c < nchunks;
        c += static_cast<int64_t>(gridDim.x) * kBlock) {
-    const int64_t off = c * N;
-    float f[N], p[N];
-    Chunk<T>::load(static_cast<const T*>(a.f) + off, f);
+    const int64_t off = c * 4;
+    float f[4], p[4];
+    ldg4(static_cast<const T*>(a.f) + off, f);
     if (a.p_empty) {
-#pragma unroll
-      for (int q = 0; q < N; ++q) p[q] = f[q];
+      p[0] = f[0]; p[1] = f[1]; p[2] = f[2]; p[3] = f[3];
     } else {
-      load_f32<N>(a.P + off, p);
-#pragma unroll
-      for (int q = 0; q < N; ++q) p[q] += f[q];
+      ldg4(a.P + off, p);
+      p[0] += f[0]; p[1] += f[1]; p[2] += f[2]; p[3] += f[3];
     }
     if (a.summary)
-      Chunk<T>::store(static_cast<T*>(a.summary) + off, p);
+      st4(static_cast<T*>(a.summary) + off, p);
     else
-      store_f32<N>(a.P + off, p);
+      st4(a.P + off, p);
   }
 }
 
@@ -246,14 +322,6 @@ __global__ void __launch_bounds__(kBlock) accum_generic_kernel(AccumArgs a, int6
   }
 }
 
-int merge_wpr(int d, int bf16) {
-  const int n = bf16 ? 8 : 4;
-  const int warps = (d / n + 31) / 32;
-  int wpr = 1;
-  while (wpr < warps) wpr <<= 1;
-  return wpr;
-}
-
 // Enough blocks for the work, at most one resident wave of `kernel`.
 unsigned grid_for(int64_t work_items, int per_block, const void* kernel) {
   int64_t blocks = (work_items + per_block - 1) / per_block;
@@ -266,28 +334,56 @@ unsigned grid_for(int64_t work_items, int per_block, const void* kernel) {
 }  // namespace
 
 bool merge_fast_ok(const MergeArgs& a) {
-  const int n = a.bf16 ? 8 : 4;
-  if (a.d % n != 0 || merge_wpr(a.d, a.bf16) > kWarps) return false;
+  const int es = a.bf16 ? 2 : 4;
+  if (a.d % 4 != 0 || (a.d * es) % 16 != 0) return false;
+  const MergeGeom g = merge_geom(a.d, es);
+  const int per_warp = (a.d + g.wpr - 1) / g.wpr;
+  if (per_warp > 8 * 128 || g.total > 227 * 1024) return false;
   return aligned16(a.O) && aligned16(a.P) && aligned16(a.out) && (a.f == nullptr || aligned16(a.f));
 }
 
 bool accum_fast_ok(const AccumArgs& a) {
-  const int n = a.bf16 ? 8 : 4;
-  if (a.d % n != 0) return false;
+  if (a.d % 4 != 0) return false;
   return aligned16(a.P) && aligned16(a.f) && (a.summary == nullptr || aligned16(a.summary));
 }
 
-cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s, bool fast) {
-  if (fast) {
-    const int wpr = merge_wpr(a.d, a.bf16);
-    const int rows_per_block = kWarps / wpr * kRows;
-    if (a.bf16) {
-      auto k = merge_fast_kernel<bf16>;
-      return launch_pdl(k, grid_for(a.T, rows_per_block, reinterpret_cast<const void*>(k)), kBlock, 0, s, a, wpr);
-    }
-    auto k = merge_fast_kernel<float>;
-    return launch_pdl(k, grid_for(a.T, rows_per_block, reinterpret_cast<const void*>(k)), kBlock, 0, s, a, wpr);
+namespace {
+template <typename T, int Q>
+cudaError_t launch_merge_tiles(const MergeArgs& a, const MergeGeom& g, cudaStream_t s) {
+  auto k = merge_tile_kernel<T, Q>;
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(k), g.total);
+  if (e != cudaSuccess) return e;
+  int64_t grid = (a.T + g.TM - 1) / g.TM;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * blocks_per_sm(reinterpret_cast<const void*>(k), kMThreads, g.total);
+  if (grid > cap) grid = cap;
+  return launch_pdl(k, static_cast<unsigned>(grid), kMThreads, g.total, s, a, g);
+}
+
+template <typename T>
+cudaError_t launch_merge_dtype(const MergeArgs& a, cudaStream_t s) {
+  const MergeGeom g = merge_geom(a.d, sizeof(T));
+  const int per_warp = (a.d + g.wpr - 1) / g.wpr;
+  int q = 1;
+  while (q * 128 < per_warp) q <<= 1;
+  switch (q) {
+    case 1: return launch_merge_tiles<T, 1>(a, g, s);
+    case 2: return launch_merge_tiles<T, 2>(a, g, s);
+    case 4: return launch_merge_tiles<T, 4>(a, g, s);
+    case 8: return launch_merge_tiles<T, 8>(a, g, s);
+    default: return cudaErrorInvalidValue;
   }
+}
+}  // namespace
+
+cudaError_t take_timeout_merge(unsigned int* flag) {
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(flag, g_merge_timeout, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_merge_timeout, &zero, sizeof(unsigned int));
+}
+
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s, bool fast) {
+  if (fast) return a.bf16 ? launch_merge_dtype<bf16>(a, s) : launch_merge_dtype<float>(a, s);
   if (a.bf16) {
     auto k = merge_generic_kernel<bf16>;
     k<<<grid_for(a.T, kWarps, reinterpret_cast<const void*>(k)), kBlock, 0, s>>>(a);
@@ -301,7 +397,7 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s, bool fast) {
 cudaError_t launch_accum(const AccumArgs& a, cudaStream_t s, bool fast) {
   const int64_t total = a.T * a.d;
   if (fast) {
-    const int64_t nchunks = total / (a.bf16 ? 8 : 4);
+    const int64_t nchunks = total / 4;
     if (a.bf16) {
       auto k = accum_fast_kernel<bf16>;
       return launch_pdl(k, grid_for(nchunks, kBlock, reinterpret_cast<const void*>(k)), kBlock, 0, s, a, nchunks);
