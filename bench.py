@@ -416,7 +416,7 @@ def ours(args):
         top = max(kernels, key=lambda k: kernels[k]["ms"])
         g = kernels[top]["gbs"]
         line["roofline"] = {
-            "kernel": {"stage1": "stage1_kernel", "merge": "merge_tile_kernel",
+            "kernel": {"stage1": "stage1_tc_kernel", "merge": "merge_tile_kernel",
                        "freeze": "accum_fast_kernel"}[top],
             "bound": "hbm", "achieved": g, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": g / peaks["hbm_gbs"], "peak_source": peaks["source"], "traffic": None,

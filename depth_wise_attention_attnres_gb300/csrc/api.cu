@@ -359,13 +359,13 @@ int attnres_device_status(void* stream) {
     cudaGetLastError();
     return ATTNRES_ERR_CUDA;
   }
-  unsigned int f1 = 0, f2 = 0, f3 = 0;
+  unsigned int f1 = 0, f2 = 0, f3 = 0, f4 = 0;
   if (take_timeout_full(&f1) != cudaSuccess || take_timeout_stage1(&f2) != cudaSuccess ||
-      take_timeout_merge(&f3) != cudaSuccess) {
+      take_timeout_merge(&f3) != cudaSuccess || take_timeout_stage1tc(&f4) != cudaSuccess) {
     cudaGetLastError();
     return ATTNRES_ERR_CUDA;
   }
-  if (f1 || f2 || f3) return ATTNRES_ERR_TIMEOUT;
+  if (f1 || f2 || f3 || f4) return ATTNRES_ERR_TIMEOUT;
   e = cudaGetLastError();
   return e == cudaSuccess ? ATTNRES_OK : ATTNRES_ERR_CUDA;
 }

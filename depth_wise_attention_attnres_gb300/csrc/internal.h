@@ -70,6 +70,7 @@ struct AccumArgs {
 // Kernel selection (pure functions of the arguments).
 bool full_fast_ok(const FullArgs& a);
 bool stage1_fast_ok(const MultiArgs& a);
+bool stage1_tc_ok(const MultiArgs& a);
 bool merge_fast_ok(const MergeArgs& a);
 bool accum_fast_ok(const AccumArgs& a);
 
@@ -77,6 +78,7 @@ bool accum_fast_ok(const AccumArgs& a);
 cudaError_t launch_full_fast(const FullArgs& a, cudaStream_t s);
 cudaError_t launch_multi_generic(const MultiArgs& a, cudaStream_t s);
 cudaError_t launch_stage1_fast(const MultiArgs& a, cudaStream_t s);
+cudaError_t launch_stage1_tc(const MultiArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s, bool fast);
 cudaError_t launch_accum(const AccumArgs& a, cudaStream_t s, bool fast);
 
@@ -84,6 +86,7 @@ cudaError_t launch_accum(const AccumArgs& a, cudaStream_t s, bool fast);
 cudaError_t take_timeout_full(unsigned int* flag);
 cudaError_t take_timeout_stage1(unsigned int* flag);
 cudaError_t take_timeout_merge(unsigned int* flag);
+cudaError_t take_timeout_stage1tc(unsigned int* flag);
 
 // Shared launch helpers (api.cu).
 int sm_count();

@@ -307,7 +307,9 @@ cudaError_t launch_dtype(const MultiArgs& a, const Stage1Geom& g, cudaStream_t s
 
 }  // namespace
 
-bool stage1_fast_ok(const MultiArgs& a) {
+// CUDA-core stage 1 (any storage dtype); the tensor-core kernel of
+// stage1_tc.cu takes bf16 shapes it supports.
+static bool stage1_cc_ok(const MultiArgs& a) {
   const int es = a.bf16 ? 2 : 4;
   const int vec = 16 / es;
   if (a.S < 1 || a.S > 8 || a.n_src < 1) return false;
@@ -320,7 +322,10 @@ bool stage1_fast_ok(const MultiArgs& a) {
   return g.TM >= 1 && g.total <= kSmemLimit;
 }
 
+bool stage1_fast_ok(const MultiArgs& a) { return stage1_tc_ok(a) || stage1_cc_ok(a); }
+
 cudaError_t launch_stage1_fast(const MultiArgs& a, cudaStream_t s) {
+  if (stage1_tc_ok(a)) return launch_stage1_tc(a, s);
   const Stage1Geom g = stage1_geom(a.n_src, a.d, a.S, a.bf16 ? 2 : 4);
   return a.bf16 ? launch_dtype<bf16>(a, g, s) : launch_dtype<float>(a, g, s);
 }
