@@ -37,6 +37,7 @@ _SIGNATURES = {
     "attnres_block_pass_noalloc": [_VP, _I64, _I32, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP,
                                    _I64, _I32, _VP, _I64, _VP],
     "attnres_device_status": [_VP],
+    "attnres_selftest_wait_timeout": [_VP],
     "attnres_status_string": [_I32],
     "attnres_kernel_path": [_I32, _VP, _VP, _I32, _I32, _I64, _I32, _I32],
     "attnres_abi_version": [],
@@ -217,6 +218,11 @@ def attnres_block_pass_noalloc(F: torch.Tensor, N: int, S: int, W: torch.Tensor,
 
 def attnres_device_status(stream=None) -> int:
     return int(lib().attnres_device_status(_stream(stream)))
+
+
+def attnres_selftest_wait_timeout(stream=None) -> None:
+    """Run the bounded-wait self-test kernel (its wait runs out after ~2 s)."""
+    _check("attnres_selftest_wait_timeout", lib().attnres_selftest_wait_timeout(_stream(stream)))
 
 
 def status_string(status: int) -> str:

@@ -370,6 +370,10 @@ int attnres_device_status(void* stream) {
   return e == cudaSuccess ? ATTNRES_OK : ATTNRES_ERR_CUDA;
 }
 
+int attnres_selftest_wait_timeout(void* stream) {
+  return status_of(launch_wait_timeout_selftest(as_stream(stream)));
+}
+
 int attnres_kernel_path(int32_t op, const void* src, const void* out, int32_t n_or_s, int32_t s,
                         int64_t T, int32_t d, int32_t dtype) {
   if (!valid_dtype(dtype) || d < 1 || T < 0) return -1;

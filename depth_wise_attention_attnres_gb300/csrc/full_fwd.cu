@@ -256,7 +256,24 @@ cudaError_t launch_dtype(const FullArgs& a, cudaStream_t s) {
   }
 }
 
+// One mbarrier that nothing ever arrives on: the bounded wait must give up,
+// record the timeout and let the kernel return.
+__global__ void wait_timeout_selftest_kernel() {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (!mbar_wait(smem_u32(&bar), 0u)) atomicOr(&g_full_timeout, 1u);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_timeout_selftest(cudaStream_t s) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, s>>>();
+  return cudaGetLastError();
+}
 
 bool full_fast_ok(const FullArgs& a) {
   const int es = a.v_bf16 ? 2 : 4;

@@ -81,6 +81,7 @@ cudaError_t launch_stage1_fast(const MultiArgs& a, cudaStream_t s);
 cudaError_t launch_stage1_tc(const MultiArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s, bool fast);
 cudaError_t launch_accum(const AccumArgs& a, cudaStream_t s, bool fast);
+cudaError_t launch_wait_timeout_selftest(cudaStream_t s);
 
 // Device-side timeout records of each kernel file: read and clear (blocking).
 cudaError_t take_timeout_full(unsigned int* flag);

@@ -233,6 +233,16 @@ int attnres_block_pass_noalloc(const void* F, int64_t f_stride, int32_t N, int32
  */
 int attnres_device_status(void* stream);
 
+/*
+ * attnres_selftest_wait_timeout - checks the bounded-wait failure path on the
+ * current device: launches one CTA whose mbarrier wait is never satisfied (no
+ * thread arrives and no copy is issued), so the wait runs out after its limit
+ * (about 2 s), records a timeout and returns. A following
+ * attnres_device_status(stream) reports ATTNRES_ERR_TIMEOUT and clears the
+ * record; the context stays usable. Returns the launch status.
+ */
+int attnres_selftest_wait_timeout(void* stream);
+
 /* Static description of a status code (never NULL). */
 const char* attnres_status_string(int32_t status);
 

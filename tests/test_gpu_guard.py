@@ -83,3 +83,18 @@ def test_status_error_raised_from_binding():
     with pytest.raises(ar.AttnResError) as ei:
         ar.attnres_full_fwd(V, 0, torch.ones(128, device=dev()), torch.ones(128, device=dev()), 1e-6, out)
     assert ei.value.status == 1
+
+
+def test_bounded_wait_runs_out_and_reports_timeout():
+    """A device wait that nothing satisfies gives up, is reported as
+    ATTNRES_ERR_TIMEOUT, and leaves the context usable (no GPU fault)."""
+    assert ar.attnres_device_status() == 0
+    ar.attnres_selftest_wait_timeout()
+    assert ar.attnres_device_status() == 4          # ATTNRES_ERR_TIMEOUT
+    assert ar.attnres_device_status() == 0          # the record was cleared
+    g = inputs.generator(24, dev())
+    V = inputs.history(3, 16, 256, "bf16", g, dev())
+    out = torch.empty(16, 256, device=dev(), dtype=torch.bfloat16)
+    ar.attnres_full_fwd(V, 3, torch.zeros(256, device=dev()), torch.ones(256, device=dev()), 1e-6, out)
+    assert torch.allclose(out.float(), V.float().mean(0), rtol=1e-2, atol=1e-2)
+    assert ar.attnres_device_status() == 0
