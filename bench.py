@@ -154,14 +154,20 @@ def kernel_digest(name: str) -> str:
 
 # ------------------------------------------------------------ distributed ----
 
-def dist_setup(n_gpus: int):
+def dist_setup(n_gpus: int, backend: str | None = None):
+    """Join the process group torchrun set up (one rank per GPU; NCCL on GPUs,
+    gloo otherwise). Returns (rank, world, local_rank)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        backend = backend or ("nccl" if torch.cuda.is_available() else "gloo")
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
     return rank, world, local
 
 
@@ -172,12 +178,19 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest per-rank value (the job's step time is its slowest rank's)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], device="cuda", dtype=torch.float64)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], device=dev, dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every rank processes its own batch (weak scaling)."""
+    return tokens_per_rank * world / (ms_per_step / 1e3)
 
 
 # ---------------------------------------------------------------- our arm ----
@@ -379,7 +392,7 @@ def ours(args):
         ms, graph = time_graph(step, args.steps, args.warmup, world, stream)
     ms = max_over_ranks(ms, world)
     tokens = wl.T * world
-    value = tokens / (ms / 1e3)
+    value = job_throughput(wl.T, world, ms)
     gbs = step.bytes / (ms / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
