@@ -26,26 +26,30 @@ namespace {
 
 __device__ unsigned int g_full_timeout = 0;
 
-constexpr int kNW = 8;               // consumer warps = rows per tile
-constexpr int kTM = kNW;
-constexpr int kThreads = (kNW + 1) * kWarp;
 constexpr int kBarBytes = 128;       // barrier area at the start of shared memory
 constexpr int kMaxStages = 8;
-constexpr int kSmemBudget = 112 * 1024;  // per CTA: two CTAs fit on one SM
+constexpr int kSmemPerSM = 224 * 1024;  // shared memory the CTAs of one SM split
 
 // Rows up to 1024 wide run two CTAs per SM (16 consumer warps hide the
 // latency of the per-source reduction chain); that caps registers at 112.
+// Per row width (CH = d / 128): NW consumer warps per CTA (= rows per tile)
+// and CTAs per SM. Several CTAs per SM run independent pipelines, so their
+// warps do not all wait and reduce in lockstep; the register budget (all
+// CTAs' threads share 64K registers) decides how many fit.
 template <int CH>
 struct FullTraits {
-  static constexpr int kMinBlocks = CH <= 8 ? 2 : 1;
-  // Keeping the converted row in registers saves a second shared read; for
-  // wider rows the registers go to the accumulator instead.
-  static constexpr bool kKeepX = CH <= 8;
+  static constexpr int kNW = 8;
+  static constexpr int kMinBlocks = CH <= 5 ? 3 : (CH <= 8 ? 2 : 1);
+  // Keeping the converted row in registers saves a second shared read when
+  // the registers allow it.
+  static constexpr bool kKeepX = CH <= 4 || (CH >= 6 && CH <= 8);
 };
 
 template <typename Tin, int CH>
-__global__ void __launch_bounds__(kThreads, FullTraits<CH>::kMinBlocks)
+__global__ void __launch_bounds__((FullTraits<CH>::kNW + 1) * kWarp, FullTraits<CH>::kMinBlocks)
     full_fwd_bulk_kernel(FullArgs a, int nstage) {
+  constexpr int kNW = FullTraits<CH>::kNW;  // consumer warps = rows per tile
+  constexpr int kTM = kNW;
   constexpr int D = CH * 128;
   constexpr int NE = CH * 4;         // elements per lane
   constexpr bool kKeepX = FullTraits<CH>::kKeepX;
@@ -222,9 +226,11 @@ __global__ void __launch_bounds__(kThreads, FullTraits<CH>::kMinBlocks)
 template <typename Tin, int CH>
 cudaError_t launch_ch(const FullArgs& a, cudaStream_t s) {
   constexpr int D = CH * 128;
+  constexpr int kTM = FullTraits<CH>::kNW;
+  constexpr int kThreads = (kTM + 1) * kWarp;
   const int stage_bytes = kTM * D * static_cast<int>(sizeof(Tin));
   const int fixed = kBarBytes + D * static_cast<int>(sizeof(float));
-  int nstage = (kSmemBudget - fixed) / stage_bytes;
+  int nstage = (kSmemPerSM / FullTraits<CH>::kMinBlocks - 1024 - fixed) / stage_bytes;
   nstage = nstage < 2 ? 2 : (nstage > kMaxStages ? kMaxStages : nstage);
   const int smem = fixed + nstage * stage_bytes;
   const void* fn = reinterpret_cast<const void*>(&full_fwd_bulk_kernel<Tin, CH>);
