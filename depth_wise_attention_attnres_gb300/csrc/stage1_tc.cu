@@ -1,4 +1,4 @@
-// Block AttnRes stage 1 with the scores on the tensor cores (bf16 storage).
+// Block AttnRes stage 1 on the tensor cores (bf16 storage), warp-specialized.
 //
 // Same job as stage1.cu (datacamp explainer, "two-stage computation": the S
 // pseudo-queries of a block against the cross-block sources, each source row
@@ -6,274 +6,685 @@
 // exp(e_ij), e_ij = w_j^T RMSNorm_j(v_i[t]) (DepthBench reading notes section
 // 2.3 / 2.5).
 //
-// The scores of a tile are a small dense contraction: with the tile's
-// (source, row) pairs as the rows of A (16 x d, bf16, as staged) and the
-// pseudo-queries as B (d x 8), e = A B / rms. It runs as warp-level m16n8k16
-// MMAs: A comes from the staged rows with ldmatrix, and w * gamma (fp32) is
-// split into bf16 hi + lo parts so the product keeps about 16 mantissa bits,
-// accumulated in fp32. The sums of squares come from the same A fragments as
-// the diagonal of A A^T (two more MMAs per step). The eight consumer warps
-// split d; their partials meet in shared memory. The softmax over depth and
-// the weighted accumulation of the S outputs (fp32 registers, packed fp32x2
-// FMAs) run on the CUDA cores, as in stage1.cu. Rows arrive by per-row 1-D
-// bulk copies into a padded pitch, double-buffered; two CTAs per SM overlap
-// each other's barrier waits.
+// A tile is the n source rows of TM consecutive tokens (P = TM * n <= 16
+// (source, token) pairs). Three roles work on different tiles at once and hand
+// over through shared memory guarded by mbarriers, with no CTA-wide barrier in
+// the steady state:
+//   producer warp: one TMA tensor copy per tile (box {64 features, n sources,
+//     TM rows, d / 64 chunks} of the [n, T, d] sources), up to six tiles in
+//     flight. The tile lands as 128-byte lines ordered (chunk, row, source)
+//     with the 128-byte swizzle, so the 8 pairs an ldmatrix reads at one
+//     feature offset sit in 8 different bank groups;
+//   4 score warps, tile t+1: the scores are a small dense contraction with the
+//     pairs as the rows of A (16 x d) and w * gamma as B (d x 8 queries, split
+//     into bf16 hi + lo so the product keeps about 16 mantissa bits), run as
+//     m16n8k16 MMAs with fp32 accumulation; the sums of squares come from the
+//     same A fragments as the diagonal of A A^T (with at most 8 pairs the
+//     roles swap: w * gamma hi and lo rows are A, the pairs the 8 columns of B,
+//     halving the MMAs). The warps split d by 64-feature
+//     chunks; their partials meet in shared memory, then a group of lanes per
+//     (row, query) takes the softmax over depth with shuffles and writes the
+//     weights (double-buffered) and lse;
+//   8 output warps, tile t: the S weighted sums of every row. With many
+//     sources and queries (S * n > 32) they run on the tensor cores: per row,
+//     D[16 features x 8 queries] = V^T W, A = V^T taken from the tile with
+//     ldmatrix.trans and K holding the 8 sources twice against the weights'
+//     bf16 hi and lo parts, D transposed into a small staging area with
+//     stmatrix.trans and written with 16-byte stores. With few of them the
+//     CUDA cores are cheaper: 8 features per thread, packed fp32x2 FMAs.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math.h>
+
 #include "common.cuh"
 #include "internal.h"
+
 namespace attnres {
 namespace {
+
 __device__ unsigned int g_stage1tc_timeout = 0;
-constexpr int kNW = 8;                        // consumer warps
-constexpr int kConsumers = kNW * kWarp;       // 256
-constexpr int kThreads = kConsumers + kWarp;  // + producer warp
-constexpr int kPairs = 16;                    // (source, row) pairs per tile: one m16 tile
-constexpr int kQ = 8;                         // MMA query columns (queries >= S are zero)
-constexpr int kBarBytes = 128;
+
+constexpr int kSW = 4;                              // score warps
+constexpr int kOW = 8;                              // output warps
+constexpr int kScoreThreads = kSW * kWarp;
+constexpr int kOutThreads = kOW * kWarp;
+constexpr int kThreads = (kSW + kOW + 1) * kWarp;   // + producer warp
+constexpr int kMaxPairs = 16;                       // pairs of a tile: one m16 MMA tile
+constexpr int kQ = 8;                               // MMA query columns (queries >= S are zero)
+constexpr int kF = 8;                               // features per thread on the CUDA-core output path
+constexpr int kMaxBuf = 6;                          // tile buffers
+constexpr int kBarBytes = 256;
+constexpr int kSmemLimit = 227 * 1024;
+constexpr int kBtBytes = 16 * 256;                  // MMA weight fragments of a tile: TM * ceil(n / 8) <= 16 blocks
+// full + empty per buffer, two weight handovers each way, then the abort flag
+static_assert((2 * kMaxBuf + 4) * 8 + 4 <= kBarBytes, "barrier area too small");
+
 struct TcGeom {
-  int TM;          // rows per tile (kPairs / n)
-  int pitch;       // bytes between staged rows (d * 2 + 16)
-  int buf_bytes;   // one buffer: kPairs rows
-  int w_off, red_off, alpha_off, buf_off, total;
+  int npair;       // pairs a tile buffer holds (16 or 8)
+  int TM;          // tokens per tile (npair / n)
+  int P;           // pairs of a tile (TM * n)
+  int pitch;       // bytes between the rows of w * gamma (d * 2 + 16)
+  int spitch;      // bytes between the query rows of an output warp's staging area
+  int buf_bytes;   // one tile buffer (npair rows of d bf16 in swizzled 128-byte lines)
+  int nbuf;        // tile buffers
+  int w_off, red_off, al_off, bt_off, stg_off, buf_off, total;
 };
+
 inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
-inline TcGeom tc_geom(int n, int d, int S) {
+
+inline TcGeom tc_geom_for(int n, int d, int S, int npair) {
   TcGeom g{};
+  g.npair = npair;
   g.pitch = d * 2 + 16;
-  g.TM = n > 0 ? kPairs / n : 0;
-  g.w_off = kBarBytes;                      // bf16 hi rows [kQ], then lo rows [kQ]
-  g.red_off = g.w_off + 2 * kQ * g.pitch;   // fp32 [kNW][kPairs][S+1] warp partials
-  g.alpha_off = g.red_off + kNW * kPairs * (S + 1) * 4;
-  g.buf_off = round_up(g.alpha_off + kPairs * round_up(S, 4) * 4, 128);
-  g.buf_bytes = kPairs * g.pitch;
-  g.total = g.buf_off + 2 * g.buf_bytes;
+  g.spitch = ((d / 64 + kOW - 1) / kOW) * 128 + 16;
+  g.TM = n > 0 ? npair / n : 0;
+  g.P = g.TM * n;
+  g.w_off = kBarBytes;                                  // bf16 hi rows [kQ], then lo rows [kQ]
+  g.red_off = g.w_off + 2 * kQ * g.pitch;               // fp32 [npair][S + 1][kSW] partials
+  g.al_off = g.red_off + kSW * npair * (S + 1) * 4;     // float2 [2][npair][S2] weights as (a, a)
+  g.bt_off = g.al_off + 2 * npair * round_up(S, 2) * 8;  // bf16 MMA weight fragments [2][kBtBytes]
+  g.stg_off = g.bt_off + 2 * kBtBytes;                  // bf16 [kOW][kQ][spitch] output staging
+  g.buf_off = round_up(g.stg_off + kOW * kQ * g.spitch, 1024);
+  g.buf_bytes = npair * d * 2;
+  g.nbuf = (kSmemLimit - 1024 - g.buf_off) / g.buf_bytes;  // 1 KB slack to align the base
+  if (g.nbuf > kMaxBuf) g.nbuf = kMaxBuf;
+  g.total = g.buf_off + g.nbuf * g.buf_bytes + 1024;
   return g;
 }
+
+// 16-pair tiles when three buffers fit, else 8-pair tiles when they hold a
+// row of every source and three of them fit, else 16-pair tiles in two.
+inline TcGeom tc_geom(int n, int d, int S) {
+  const TcGeom g = tc_geom_for(n, d, S, 16);
+  if (g.TM >= 1 && g.nbuf >= 3) return g;
+  const TcGeom h = tc_geom_for(n, d, S, 8);
+  if (h.TM >= 1 && h.nbuf >= 3) return h;
+  return g;
+}
+
+// Which output path a launch takes (the tensor cores pay off from about 32
+// multiply-adds per feature and row).
+inline bool outputs_on_tensor_cores(int n, int S) { return S * n > 32; }
+
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];" : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
 }
+
+__device__ __forceinline__ void ldsm_x2_trans(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
+__device__ __forceinline__ void stsm_x2_trans(uint32_t addr, uint32_t r0, uint32_t r1) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x2.trans.shared.b16 [%0], {%1,%2};" ::"r"(addr), "r"(r0), "r"(r1)
+               : "memory");
+}
+
+// c += A (16x16, row-major fragments a) * B (16x8, col-major fragments b0 b1).
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3]) : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-template <int S, int CPT>
-__global__ void __launch_bounds__(kThreads, CPT == 1 ? 2 : 1) stage1_tc_kernel(MultiArgs a, TcGeom g) {
-  constexpr int S4 = (S + 3) / 4 * 4;
+
+// The whole tile in one tensor copy; completion is signalled on `bar`.
+__device__ __forceinline__ void tma_load_tile(uint32_t dst, const CUtensorMap* map, int row0, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(row0), "r"(0), "r"(bar)
+      : "memory");
+}
+
+// Shared address of 128-byte line L of a 1 KB-aligned tile with its swizzle
+// phase folded in: the 16-byte unit u of the line is then at line_base ^ (u << 4)
+// (the swizzle stores unit u at u ^ (L & 7) and only touches address bits 4..6).
+__device__ __forceinline__ uint32_t line_base(uint32_t tile, int L) {
+  return tile + static_cast<uint32_t>(L) * 128u + static_cast<uint32_t>((L & 7) << 4);
+}
+
+template <int S, bool kTC>
+__global__ void __launch_bounds__(kThreads, 1)
+    stage1_tc_kernel(MultiArgs a, TcGeom g, const __grid_constant__ CUtensorMap tmap) {
+  constexpr int S2 = (S + 1) / 2 * 2;  // CUDA-core path: weights as (a, a) pairs, S2 per (token, source)
+  constexpr int SC = S + 1;            // partial columns per pair: sum of squares, then the S dots
   extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty_bar = full_bar + 2;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(full_bar + 4);
-  unsigned char* wsm = smem + g.w_off;                          // w * gamma, bf16 hi / lo rows
-  float* red = reinterpret_cast<float*>(smem + g.red_off);      // partial sums of squares / dots
-  float* alpha = reinterpret_cast<float*>(smem + g.alpha_off);  // [TM][n][S4] scores, then weights
-  unsigned char* bufs = smem + g.buf_off;                       // 2 tiles of staged rows
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem);  // [kMaxBuf] tile landed
+  uint64_t* empty_bar = full_bar + kMaxBuf;                 // [kMaxBuf] tile consumed
+  uint64_t* afull = empty_bar + kMaxBuf;                    // [2] weights ready
+  uint64_t* aempty = afull + 2;                             // [2] weights consumed
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(aempty + 2);
+  unsigned char* wsm = smem + g.w_off;
+  float* red = reinterpret_cast<float*>(smem + g.red_off);  // [npair][SC][kSW] partials
+  float2* alpha = reinterpret_cast<float2*>(smem + g.al_off);
+  unsigned char* btab = smem + g.bt_off;  // [2][TM][ceil(n/8)][8 queries][4] uint2 {hi pair, lo pair}
+  unsigned char* bufs = smem + g.buf_off;
+  bufs += (1024u - (smem_u32(bufs) & 1023u)) & 1023u;  // the swizzle wants 1 KB alignment
+
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int n = a.n_src, d = a.d, TM = g.TM;
-  const int P = TM * n;
+  const int P = g.P;  // pair m = r * n + i (token r of the tile, source i)
   const int64_t ntok = a.T;
   const int64_t ntiles_total = (ntok + TM - 1) / TM;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * ntiles_total / gridDim.x;
   const int64_t t1 = static_cast<int64_t>(blockIdx.x + 1) * ntiles_total / gridDim.x;
+  const int nbuf = g.nbuf;
+  const int nchunk = d >> 6;  // 64-feature chunks: one 128-byte line per pair
+
   pdl_trigger();
   if (tid == 0) {
-    for (int b = 0; b < 2; ++b) { mbar_init(smem_u32(&full_bar[b]), 1); mbar_init(smem_u32(&empty_bar[b]), kNW); }
-    *reinterpret_cast<int*>(full_bar + 4) = 0;
+    for (int b = 0; b < nbuf; ++b) {
+      mbar_init(smem_u32(&full_bar[b]), 1);
+      mbar_init(smem_u32(&empty_bar[b]), kSW + kOW);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(smem_u32(&afull[k]), kScoreThreads);
+      mbar_init(smem_u32(&aempty[k]), kOW);
+    }
+    *reinterpret_cast<int*>(aempty + 2) = 0;
     mbar_fence_init();
   }
-  pdl_wait();
-  // w * gamma as bf16 hi + lo rows (queries >= S are zero).
-  for (int idx = tid; idx < kQ * d; idx += kThreads) {
-    const int q = idx / d, k = idx - (idx / d) * d;
-    const float w = q < S ? a.W[q * d + k] * a.Gamma[q * d + k] : 0.f;
-    const bf16 hi = __float2bfloat16_rn(w);
-    const bf16 lo = __float2bfloat16_rn(w - __bfloat162float(hi));
-    reinterpret_cast<bf16*>(wsm + q * g.pitch)[k] = hi;
-    reinterpret_cast<bf16*>(wsm + (kQ + q) * g.pitch)[k] = lo;
-  }
   __syncthreads();
-  if (warp == kNW) {
-    // Producer: one bulk copy per (source, row) of the tile into a padded pitch.
+  pdl_wait();  // everything below may read what the previous kernel wrote
+
+  bool ok = true;
+  if (warp == kSW + kOW) {
+    // ------------------------------------------------------------ producer
     if (lane != 0) return;
-    const char* src = static_cast<const char*>(a.V);
-    const uint32_t row_bytes = static_cast<uint32_t>(d) * 2u;
-    int b = 0; uint32_t phase = 0; int64_t issued = 0; bool ok = true;
+    const uint32_t box_bytes = static_cast<uint32_t>(P) * static_cast<uint32_t>(d) * 2u;
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
+    int b = 0;
+    uint32_t phase = 0;
+    int64_t issued = 0;
     for (int64_t tile = t0; tile < t1; ++tile) {
-      if (!mbar_wait(smem_u32(&empty_bar[b]), phase ^ 1u)) { ok = false; break; }
-      const int64_t row0 = tile * TM;
-      const int rows = static_cast<int>(min(static_cast<int64_t>(TM), ntok - row0));
+      // A fresh barrier counts its (virtual) previous phase as complete, so
+      // the first round of waits on parity 1 passes at once.
+      if (!mbar_wait(smem_u32(&empty_bar[b]), phase ^ 1u)) {
+        ok = false;
+        break;
+      }
+      // Rows past T are zero-filled; the transaction always counts the whole box.
       const uint32_t fb = smem_u32(&full_bar[b]);
-      mbar_arrive_expect_tx(fb, row_bytes * rows * n);
-      const uint32_t dst0 = smem_u32(bufs + b * g.buf_bytes);
-      for (int i = 0; i < n; ++i)
-        for (int r = 0; r < rows; ++r)
-          bulk_g2s(dst0 + (i * TM + r) * g.pitch, src + (i * a.src_stride + (row0 + r) * d) * 2, row_bytes, fb);
+      mbar_arrive_expect_tx(fb, box_bytes);
+      tma_load_tile(smem_u32(bufs + b * g.buf_bytes), &tmap, static_cast<int>(tile * TM), fb);
       ++issued;
-      if (++b == 2) { b = 0; phase ^= 1u; }
+      if (++b == nbuf) {
+        b = 0;
+        phase ^= 1u;
+      }
     }
     if (!ok) {
       atomicOr(&g_stage1tc_timeout, 1u);
-      for (int64_t it = issued > 2 ? issued - 2 : 0; it < issued; ++it)
-        (void)mbar_wait(smem_u32(&full_bar[it % 2]), static_cast<uint32_t>((it / 2) & 1));
+      // Let the copies still in flight land before this CTA's memory goes.
+      for (int64_t it = issued > nbuf ? issued - nbuf : 0; it < issued; ++it)
+        (void)mbar_wait(smem_u32(&full_bar[it % nbuf]), static_cast<uint32_t>((it / nbuf) & 1));
     }
     return;
   }
-  // Consumers.
-  const float inv_d = 1.0f / static_cast<float>(d);
-  const int KW = d / kNW;  // features of this warp's slice in the score pass
-  const int a_row = (lane & 7) + ((lane >> 3) & 1) * 8;
-  const int a_koff = (lane >> 4) * 8;
-  const int b_row = (lane & 7) + ((lane >> 4) & 1) * kQ;
-  const int b_koff = ((lane >> 3) & 1) * 8;
-  const uint32_t b_base = smem_u32(wsm + b_row * g.pitch) + (warp * KW + b_koff) * 2;
-  const int gid = lane >> 2, tig = lane & 3;
-  int b = 0; uint32_t phase = 0; bool ok = true;
-  for (int64_t tile = t0; tile < t1; ++tile) {
-    // Giving up a wait is a joint decision (the consumers meet at barriers).
-    if (!mbar_wait(smem_u32(&full_bar[b]), phase)) *abort_flag = 1;
-    named_sync(1, kConsumers);
-    if (*abort_flag) { ok = false; break; }
-    const unsigned char* buf = bufs + b * g.buf_bytes;
-    const int64_t row0 = tile * TM;
-    const int rows = static_cast<int>(min(static_cast<int64_t>(TM), ntok - row0));
-    // A. partial scores and sums of squares over this warp's slice (MMA).
-    {
-      const int pair = a_row < P ? a_row : 0;  // rows past P only pad the m16 tile
-      const uint32_t a_base = smem_u32(buf + pair * g.pitch) + (warp * KW + a_koff) * 2;
-      float sc[4] = {0.f, 0.f, 0.f, 0.f}, s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-      for (int k0 = 0; k0 < KW; k0 += 16) {
-        uint32_t av[4], bv[4];
-        ldsm_x4(a_base + k0 * 2, av);
-        ldsm_x4(b_base + k0 * 2, bv);
-        mma16816(sc, av, bv[0], bv[1]);  // hi part of w * gamma
-        mma16816(sc, av, bv[2], bv[3]);  // lo part
-        mma16816(s0, av, av[0], av[2]);  // A A^T, columns 0..7
-        mma16816(s1, av, av[1], av[3]);  // A A^T, columns 8..15
-      }
+
+  // w * gamma as bf16 hi + lo rows (queries >= S are zero), by the score and
+  // output warps while the producer already fills the pipeline; loads are
+  // issued in groups of four per thread before any of them is used.
+  {
+    constexpr int kCT = kScoreThreads + kOutThreads;
+    const int nv = kQ * d / 4;
+    for (int base = tid; base < nv; base += 4 * kCT) {
+      float4 wv[4];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int q = 2 * tig + e;
+      for (int u = 0; u < 4; ++u) {
+        const int v = base + u * kCT;
+        const int q = v < nv ? (v * 4) / d : kQ;
+        wv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (q < S) {
-          if (gid < P) red[(warp * kPairs + gid) * (S + 1) + 1 + q] = sc[e];
-          if (gid + 8 < P) red[(warp * kPairs + gid + 8) * (S + 1) + 1 + q] = sc[2 + e];
+          const float4 x = *reinterpret_cast<const float4*>(a.W + v * 4);
+          const float4 y = *reinterpret_cast<const float4*>(a.Gamma + v * 4);
+          wv[u] = make_float4(x.x * y.x, x.y * y.y, x.z * y.z, x.w * y.w);
         }
       }
-      // Diagonal of A A^T: row gid in s0[gid & 1], row gid + 8 in s1[2 + (gid & 1)],
-      // held by the lane whose 2 tig + e equals gid (selects keep registers).
-      if (tig == (gid >> 1)) {
-        const bool odd = gid & 1;
-        if (gid < P) red[(warp * kPairs + gid) * (S + 1)] = odd ? s0[1] : s0[0];
-        if (gid + 8 < P) red[(warp * kPairs + gid + 8) * (S + 1)] = odd ? s1[3] : s1[2];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = base + u * kCT;
+        if (v < nv) {
+          const int q = (v * 4) / d, k = v * 4 - q * d;
+          const float w[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+          float hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            hi[e] = __bfloat162float(__float2bfloat16_rn(w[e]));
+            lo[e] = w[e] - hi[e];
+          }
+          st4(reinterpret_cast<bf16*>(wsm + q * g.pitch) + k, hi);
+          st4(reinterpret_cast<bf16*>(wsm + (kQ + q) * g.pitch) + k, lo);
+        }
       }
     }
-    named_sync(1, kConsumers);
-    // Scores e_ij = dot_ij / rms_i, summed over the warps' partials.
-    for (int item = tid; item < P * S; item += kConsumers) {
-      const int p = item / S, j = item - (item / S) * S;
-      float ss = 0.f, dot = 0.f;
+    // MMA weight fragments of sources >= n and of queries >= S stay zero.
+    for (int v = tid; v < 2 * kBtBytes / 16; v += kCT) reinterpret_cast<uint4*>(btab)[v] = make_uint4(0u, 0u, 0u, 0u);
+    named_sync(2, kCT);
+  }
+
+  if (warp < kSW) {
+    // ------------------------------------------------------------- scores
+    const float inv_d = 1.0f / static_cast<float>(d);
+    const int cb = warp * nchunk / kSW, ce = (warp + 1) * nchunk / kSW;  // this warp's chunks
+    const int a_row = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int a_koff = (lane >> 4) * 8;
+    const int b_row = (lane & 7) + ((lane >> 4) & 1) * kQ;  // hi rows, then lo rows
+    const int b_koff = ((lane >> 3) & 1) * 8;
+    const uint32_t b_base = smem_u32(wsm + b_row * g.pitch) + (cb * 64 + b_koff) * 2;
+    const uint32_t a_x = static_cast<uint32_t>(a_koff) * 2u;  // this lane's 16-byte unit within a k-step
+    const int m = a_row < P ? a_row : 0;                      // rows past P only pad the m16 tile
+    const int gid = lane >> 2, tig = lane & 3;
+    // Softmax: a group of G lanes (n rounded up to a power of two) per (token, query).
+    int lgG = 0;
+    while ((1 << lgG) < n) ++lgG;
+    const int G = 1 << lgG;
+    const int sm_items = TM * S * G;
+    const int nk = (n + 7) >> 3;
+    int b = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    for (int64_t tile = t0; tile < t1; ++tile, ++it) {
+      const int ab = it & 1;
+      const uint32_t aph = static_cast<uint32_t>((it >> 1) & 1);
+      // The tile must have landed and weights buffer ab must be free. The
+      // score warps meet at a named barrier, so giving up is decided jointly.
+      if (!mbar_wait(smem_u32(&full_bar[b]), phase) || !mbar_wait(smem_u32(&aempty[ab]), aph ^ 1u))
+        *abort_flag = 1;
+      named_sync(1, kScoreThreads);
+      if (*abort_flag) {
+        ok = false;
+        break;
+      }
+      const uint32_t bb = smem_u32(bufs + b * g.buf_bytes);
+      const int64_t row0 = tile * TM;
+      const int rows = static_cast<int>(min(static_cast<int64_t>(TM), ntok - row0));
+      {
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        // Per chunk: the line of pair m, then its four k-steps (one XOR each).
+        // All fragments of a chunk are loaded before its MMAs, since the asm
+        // statements issue in program order.
+        if (P <= 8) {
+          // Up to 8 pairs: w * gamma is A (rows: the hi parts of the 8 queries,
+          // then their lo parts) and the pairs are the 8 columns of B = V^T,
+          // so one MMA gives hi and lo dots; one more gives the A A^T block
+          // with the sums of squares.
+          float sw[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int c = cb; c < ce; ++c) {
+            const uint32_t off = line_base(bb, c * P + m) ^ a_x;
+            const uint32_t bo = b_base + static_cast<uint32_t>(c - cb) * 128u;
+            uint32_t av[4][4], bv[4][4];
 #pragma unroll
-      for (int w = 0; w < kNW; ++w) { const float* rp = red + (w * kPairs + p) * (S + 1); ss += rp[0]; dot += rp[1 + j]; }
-      const int i = p / TM, r = p - (p / TM) * TM;
-      alpha[(r * n + i) * S4 + j] = dot * rsqrtf(ss * inv_d + a.eps);
-    }
-    named_sync(1, kConsumers);
-    // B. softmax over the n sources for each (row, query): weights and lse.
-    for (int item = tid; item < TM * S; item += kConsumers) {
-      const int r = item / S, j = item - (item / S) * S;
-      float* e = alpha + r * n * S4 + j;
-      float m = e[0];
-      for (int i = 1; i < n; ++i) m = fmaxf(m, e[i * S4]);
-      float z = 0.f;
-      for (int i = 0; i < n; ++i) z += __expf(e[i * S4] - m);
-      const float inv = 1.0f / z;
-      for (int i = 0; i < n; ++i) e[i * S4] = __expf(e[i * S4] - m) * inv;
-      if (a.lse && r < rows) a.lse[j * ntok + row0 + r] = m + __logf(z);
-    }
-    named_sync(1, kConsumers);
-    // C. the S outputs of every row from the staged rows (CUDA cores).
-    for (int r = 0; r < rows; ++r) {
-      float2 acc[S][CPT * 2];
+            for (int u = 0; u < 4; ++u) {
+              ldsm_x4(off ^ (32u * u), av[u]);
+              ldsm_x4(bo + 32u * u, bv[u]);
+            }
 #pragma unroll
-      for (int j = 0; j < S; ++j)
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t wa[4] = {bv[u][0], bv[u][2], bv[u][1], bv[u][3]};
+              mma16816(sw, wa, av[u][0], av[u][2]);     // [hi; lo] dots x 8 pairs
+              mma16816(s0, av[u], av[u][0], av[u][2]);  // A A^T, columns 0..7
+            }
+          }
+          // This warp is done with the tile's rows.
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&empty_bar[b]));
+          // Lane (gid, tig) holds the dots of query gid with pairs 2 tig, 2 tig + 1.
+          if (gid < S) {
 #pragma unroll
-        for (int q = 0; q < CPT * 2; ++q) acc[j][q] = make_float2(0.f, 0.f);
-      for (int i = 0; i < n; ++i) {
-        const bf16* rowp = reinterpret_cast<const bf16*>(buf + (i * TM + r) * g.pitch);
-        const float* al = alpha + (r * n + i) * S4;
-        float aw[S4];
+            for (int e = 0; e < 2; ++e) {
+              const int pp = 2 * tig + e;
+              if (pp < P) red[(pp * SC + 1 + gid) * kSW + warp] = sw[e] + sw[2 + e];
+            }
+          }
+        } else {
+          float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int c = cb; c < ce; ++c) {
+            const uint32_t off = line_base(bb, c * P + m) ^ a_x;
+            const uint32_t bo = b_base + static_cast<uint32_t>(c - cb) * 128u;
+            uint32_t av[4][4], bv[4][4];
 #pragma unroll
-        for (int j = 0; j < S4; j += 4) { const float4 a4 = *reinterpret_cast<const float4*>(al + j); aw[j] = a4.x; aw[j + 1] = a4.y; aw[j + 2] = a4.z; aw[j + 3] = a4.w; }
+            for (int u = 0; u < 4; ++u) {
+              ldsm_x4(off ^ (32u * u), av[u]);
+              ldsm_x4(bo + 32u * u, bv[u]);
+            }
 #pragma unroll
-        for (int q = 0; q < CPT; ++q) {
-          const int k = (tid + q * kConsumers) * 4;
-          if (k < d) {
-            float x[4];
-            lds4(rowp + k, x);
+            for (int u = 0; u < 4; ++u) {
+              mma16816(sh, av[u], bv[u][0], bv[u][1]);  // hi part of w * gamma
+              mma16816(sl, av[u], bv[u][2], bv[u][3]);  // lo part
+              mma16816(s0, av[u], av[u][0], av[u][2]);  // A A^T, columns 0..7
+              mma16816(s1, av[u], av[u][1], av[u][3]);  // A A^T, columns 8..15
+            }
+          }
+          // This warp is done with the tile's rows.
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&empty_bar[b]));
+          // Lane (gid, tig) holds the dots of pairs gid, gid + 8 with queries 2 tig, 2 tig + 1.
 #pragma unroll
-            for (int j = 0; j < S; ++j) {
-              const float2 a2 = make_float2(aw[j], aw[j]);
-              acc[j][q * 2] = ffma2(a2, make_float2(x[0], x[1]), acc[j][q * 2]);
-              acc[j][q * 2 + 1] = ffma2(a2, make_float2(x[2], x[3]), acc[j][q * 2 + 1]);
+          for (int e = 0; e < 2; ++e) {
+            const int q = 2 * tig + e;
+            if (q < S) {
+              if (gid < P) red[(gid * SC + 1 + q) * kSW + warp] = sh[e] + sl[e];
+              if (gid + 8 < P) red[((gid + 8) * SC + 1 + q) * kSW + warp] = sh[2 + e] + sl[2 + e];
             }
           }
         }
+        // Diagonal of A A^T: row gid in s0[gid & 1], row gid + 8 in s1[2 + (gid & 1)],
+        // held by the lane whose 2 tig + e equals gid (selects keep registers).
+        if (tig == (gid >> 1)) {
+          const bool odd = gid & 1;
+          if (gid < P) red[(gid * SC) * kSW + warp] = odd ? s0[1] : s0[0];
+          if (gid + 8 < P) red[((gid + 8) * SC) * kSW + warp] = odd ? s1[3] : s1[2];
+        }
       }
-      const int64_t row = row0 + r;
+      named_sync(1, kScoreThreads);
+      // Softmax over depth, one lane per source: max and mass by shuffles
+      // within the group.
+      float2* al = alpha + ab * g.npair * S2;
+      unsigned char* bt = btab + ab * kBtBytes;
+      for (int base = 0; base < sm_items; base += kScoreThreads) {
+        const int item = base + tid;
+        const int i = item & (G - 1);
+        const int rj = item >> lgG;
+        const int r = rj / S, j = rj - (rj / S) * S;
+        const bool valid = item < sm_items && i < n;
+        float e = -INFINITY;
+        if (valid) {
+          const int p = r * n + i;
+          // The four warps' partials of pair p sit side by side.
+          const float4 sq = *reinterpret_cast<const float4*>(red + (p * SC) * kSW);
+          const float4 dt = *reinterpret_cast<const float4*>(red + (p * SC + 1 + j) * kSW);
+          const float ss = ((sq.x + sq.y) + sq.z) + sq.w;
+          const float dot = ((dt.x + dt.y) + dt.z) + dt.w;
+          e = dot * rsqrtf(ss * inv_d + a.eps);
+        }
+        float mx = e;
+        for (int off = 1; off < G; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float x = valid ? __expf(e - mx) : 0.f;
+        float z = x;
+        for (int off = 1; off < G; off <<= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+        if (valid) {
+          const float wgt = x * (1.0f / z);
+          if constexpr (kTC) {
+            // B fragment of the output MMA for token r, source block i / 8 and
+            // query j: {hi(a[2t]), hi(a[2t+1])}, {lo(a[2t]), lo(a[2t+1])}, t = (i % 8) / 2.
+            const bf16 hi = __float2bfloat16_rn(wgt);
+            const bf16 lo = __float2bfloat16_rn(wgt - __bfloat162float(hi));
+            bf16* ep = reinterpret_cast<bf16*>(bt + (((r * nk + (i >> 3)) * 8 + j) * 4 + ((i & 7) >> 1)) * 8);
+            ep[i & 1] = hi;
+            ep[2 + (i & 1)] = lo;
+          } else {
+            al[(r * n + i) * S2 + j] = make_float2(wgt, wgt);
+          }
+          if (i == 0 && a.lse && r < rows) a.lse[j * ntok + row0 + r] = mx + __logf(z);
+        }
+      }
+      // Weights of this tile are ready (each score thread arrives). red[] is
+      // rewritten by the next tile only after every score thread has passed
+      // the named barrier at its top.
+      mbar_arrive(smem_u32(&afull[ab]));
+      if (++b == nbuf) {
+        b = 0;
+        phase ^= 1u;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- outputs
+    const int ow = warp - kSW;
+    int b = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    if constexpr (kTC) {
+      // Output warp ow owns a run of chunks. Per token and block of 16
+      // features: D[16 features x 8 queries] = A B with A = V^T from
+      // ldmatrix.trans (the k columns repeat the 8 sources twice) and B = the
+      // weights' bf16 hi parts for k < 8 and lo parts for k >= 8 (one MMA per
+      // 8 sources). D goes through stmatrix.trans into the warp's staging rows
+      // (one per query), then out with 16-byte stores.
+      const int cb = ow * nchunk / kOW, ce = (ow + 1) * nchunk / kOW;
+      const int ncw = ce - cb;
+      const int f_beg = cb * 64;
+      const int nk = (n + 7) >> 3;
+      unsigned char* stg = smem + g.stg_off + ow * kQ * g.spitch;
+      const int l8 = lane & 7, lhalf = (lane >> 3) & 1;
+      const uint32_t st_base = smem_u32(stg) + l8 * g.spitch + lhalf * 16;
+      const uint32_t lx = static_cast<uint32_t>(lhalf) << 4;
+      const int pq = ncw * 8;  // 16-byte pieces of one query row of this warp
+      int lg_pq = -1;
+      if ((pq & (pq - 1)) == 0) {
+        lg_pq = 0;
+        while ((1 << lg_pq) < pq) ++lg_pq;
+      }
+      for (int64_t tile = t0; tile < t1; ++tile, ++it) {
+        const int ab = it & 1;
+        const uint32_t aph = static_cast<uint32_t>((it >> 1) & 1);
+        // Weights ready; waiting on the tile's own barrier as well makes the
+        // copied rows visible to this warp.
+        const bool got = mbar_wait(smem_u32(&afull[ab]), aph) && mbar_wait(smem_u32(&full_bar[b]), phase);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        const uint32_t bb = smem_u32(bufs + b * g.buf_bytes);
+        const uint2* bt = reinterpret_cast<const uint2*>(btab + ab * kBtBytes);
+        const int64_t row0 = tile * TM;
+        const int rows = static_cast<int>(min(static_cast<int64_t>(TM), ntok - row0));
+        for (int r = 0; r < rows; ++r) {
+          uint2 bf[2];
 #pragma unroll
-      for (int q = 0; q < CPT; ++q) {
-        const int k = (tid + q * kConsumers) * 4;
-        if (k < d) {
+          for (int kb = 0; kb < 2; ++kb) bf[kb] = kb < nk ? bt[(r * nk + kb) * 32 + lane] : make_uint2(0u, 0u);
+          // Two chunks (8 blocks) at a time: all fragment loads, then the
+          // independent MMAs, then the transposing stores.
+          for (int c = 0; c < ncw; c += 2) {
+            float acc[8][4];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
+            const bool two = c + 1 < ncw;
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+              if (kb < nk) {
+                // Lanes past the last source point at source 0; its weights are zero.
+                const int i = kb * 8 + l8;
+                const int pr = r * n + (i < n ? i : 0);
+                uint32_t mv[8][2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  if (h == 0 || two) {
+                    const uint32_t off = line_base(bb, (cb + c + h) * P + pr) ^ lx;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) ldsm_x2_trans(off ^ (32u * u), mv[h * 4 + u][0], mv[h * 4 + u][1]);
+                  }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                  if (u < 4 || two) {
+                    const uint32_t av[4] = {mv[u][0], mv[u][1], mv[u][0], mv[u][1]};
+                    mma16816(acc[u], av, bf[kb].x, bf[kb].y);
+                  }
+                }
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              if (u < 4 || two)
+                stsm_x2_trans(st_base + static_cast<uint32_t>(c * 128 + u * 32), pack_bf16x2(acc[u][0], acc[u][1]),
+                              pack_bf16x2(acc[u][2], acc[u][3]));
+          }
+          __syncwarp();
+          const int64_t row = row0 + r;
+          for (int idx = lane; idx < S * pq; idx += kWarp) {
+            const int q = lg_pq >= 0 ? idx >> lg_pq : idx / pq;
+            const int ch = idx - q * pq;
+            const uint4 v = *reinterpret_cast<const uint4*>(stg + q * g.spitch + ch * 16);
+            *reinterpret_cast<uint4*>(static_cast<bf16*>(a.out[q]) + row * d + f_beg + ch * 8) = v;
+          }
+          __syncwarp();
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&aempty[ab]));
+          mbar_arrive(smem_u32(&empty_bar[b]));
+        }
+        if (++b == nbuf) {
+          b = 0;
+          phase ^= 1u;
+        }
+      }
+    } else {
+      // Groups of d / 8 threads, one token of the tile per group at a time, 8
+      // features per thread, packed fp32x2 FMAs with the weights stored as
+      // (a, a) pairs.
+      const int otid = tid - kScoreThreads;
+      const int tpr = d / kF;
+      const int ngrp = kOutThreads / tpr;
+      const int grp = otid / tpr;
+      const int k = (otid - grp * tpr) * kF;
+      const uint32_t kx = static_cast<uint32_t>((k >> 3) & 7) << 4;
+      const int kc = k >> 6;
+      for (int64_t tile = t0; tile < t1; ++tile, ++it) {
+        const int ab = it & 1;
+        const uint32_t aph = static_cast<uint32_t>((it >> 1) & 1);
+        const bool got = mbar_wait(smem_u32(&afull[ab]), aph) && mbar_wait(smem_u32(&full_bar[b]), phase);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        const uint32_t bb = smem_u32(bufs + b * g.buf_bytes);
+        const float2* al = alpha + ab * g.npair * S2;
+        const int64_t row0 = tile * TM;
+        const int rows = static_cast<int>(min(static_cast<int64_t>(TM), ntok - row0));
+        // Threads past the last group idle.
+        for (int r = grp < ngrp ? grp : TM; r < rows; r += ngrp) {
+          float2 acc[S][kF / 2];
+#pragma unroll
+          for (int j = 0; j < S; ++j)
+#pragma unroll
+            for (int e = 0; e < kF / 2; ++e) acc[j][e] = make_float2(0.f, 0.f);
+          for (int i = 0; i < n; ++i) {
+            uint4 xv;
+            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(xv.x), "=r"(xv.y), "=r"(xv.z), "=r"(xv.w)
+                         : "r"(line_base(bb, kc * P + r * n + i) ^ kx));
+            const float2 x2[4] = {make_float2(bf16_lo(xv.x), bf16_hi(xv.x)), make_float2(bf16_lo(xv.y), bf16_hi(xv.y)),
+                                  make_float2(bf16_lo(xv.z), bf16_hi(xv.z)), make_float2(bf16_lo(xv.w), bf16_hi(xv.w))};
+            const float4* ai = reinterpret_cast<const float4*>(al + (r * n + i) * S2);
+#pragma unroll
+            for (int jj = 0; jj < S2 / 2; ++jj) {
+              const float4 a4 = ai[jj];
+              const float2 a0 = make_float2(a4.x, a4.y), a1 = make_float2(a4.z, a4.w);
+#pragma unroll
+              for (int e = 0; e < kF / 2; ++e) {
+                acc[2 * jj][e] = ffma2(a0, x2[e], acc[2 * jj][e]);
+                if (2 * jj + 1 < S) acc[2 * jj + 1][e] = ffma2(a1, x2[e], acc[2 * jj + 1][e]);
+              }
+            }
+          }
+          const int64_t row = row0 + r;
 #pragma unroll
           for (int j = 0; j < S; ++j) {
-            const float o[4] = {acc[j][q * 2].x, acc[j][q * 2].y, acc[j][q * 2 + 1].x, acc[j][q * 2 + 1].y};
-            st4(static_cast<bf16*>(a.out[j]) + row * d + k, o);
+            const uint4 o = make_uint4(pack_bf16x2(acc[j][0].x, acc[j][0].y), pack_bf16x2(acc[j][1].x, acc[j][1].y),
+                                       pack_bf16x2(acc[j][2].x, acc[j][2].y), pack_bf16x2(acc[j][3].x, acc[j][3].y));
+            *reinterpret_cast<uint4*>(static_cast<bf16*>(a.out[j]) + row * d + k) = o;
           }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&aempty[ab]));
+          mbar_arrive(smem_u32(&empty_bar[b]));
+        }
+        if (++b == nbuf) {
+          b = 0;
+          phase ^= 1u;
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&empty_bar[b]));
-    if (++b == 2) { b = 0; phase ^= 1u; }
   }
   if (!ok) atomicOr(&g_stage1tc_timeout, 1u);
 }
-template <int S, int CPT>
-cudaError_t launch_sc(const MultiArgs& a, const TcGeom& g, cudaStream_t s) {
-  auto k = stage1_tc_kernel<S, CPT>;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// The sources as a 4-d tensor (feature within chunk, source, token, chunk) and
+// the tile box {64, n, TM, d / 64}, 128-byte swizzle.
+bool encode_tile_map(const MultiArgs& a, const TcGeom& g, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(a.n_src), static_cast<cuuint64_t>(a.T),
+                              static_cast<cuuint64_t>(a.d / 64)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(a.src_stride) * 2, static_cast<cuuint64_t>(a.d) * 2, 128};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(a.n_src), static_cast<cuuint32_t>(g.TM),
+                             static_cast<cuuint32_t>(a.d / 64)};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.V), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int S, bool kTC>
+cudaError_t launch_s(const MultiArgs& a, const TcGeom& g, cudaStream_t s) {
+  auto k = stage1_tc_kernel<S, kTC>;
   cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(k), g.total);
   if (e != cudaSuccess) return e;
+  alignas(64) CUtensorMap map;
+  if (!encode_tile_map(a, g, &map)) return cudaErrorInvalidValue;
   const int64_t tiles = (a.T + g.TM - 1) / g.TM;
   int64_t grid = static_cast<int64_t>(sm_count()) * blocks_per_sm(reinterpret_cast<const void*>(k), kThreads, g.total);
   if (grid > tiles) grid = tiles;
-  return launch_pdl(k, static_cast<unsigned>(grid), kThreads, g.total, s, a, g);
+  return launch_pdl(k, static_cast<unsigned>(grid), kThreads, g.total, s, a, g, map);
 }
+
 template <int S>
-cudaError_t launch_s(const MultiArgs& a, const TcGeom& g, cudaStream_t s) {
-  return (a.d / 4 <= kConsumers) ? launch_sc<S, 1>(a, g, s) : launch_sc<S, 2>(a, g, s);
+cudaError_t launch_q(const MultiArgs& a, const TcGeom& g, cudaStream_t s) {
+  return outputs_on_tensor_cores(a.n_src, S) ? launch_s<S, true>(a, g, s) : launch_s<S, false>(a, g, s);
 }
+
 }  // namespace
+
 bool stage1_tc_ok(const MultiArgs& a) {
-  if (!a.bf16 || a.S < 1 || a.S > 8 || a.n_src < 1 || a.n_src > kPairs) return false;
-  if (a.d % (kNW * 16) != 0 || a.d > 2048) return false;
+  if (!a.bf16 || a.S < 1 || a.S > kQ || a.n_src < 1 || a.n_src > kMaxPairs) return false;
+  if (a.d % 64 != 0 || a.d > kF * kOutThreads || a.T >= (int64_t(1) << 31)) return false;
   if (!aligned16(a.V) || ((a.src_stride * 2) % 16) != 0) return false;
-  for (int j = 0; j < a.S; ++j) if (!aligned16(a.out[j])) return false;
-  return tc_geom(a.n_src, a.d, a.S).total <= 227 * 1024;
+  if (!aligned16(a.W) || !aligned16(a.Gamma)) return false;
+  for (int j = 0; j < a.S; ++j)
+    if (!aligned16(a.out[j])) return false;
+  const TcGeom g = tc_geom(a.n_src, a.d, a.S);
+  return g.TM >= 1 && g.nbuf >= 2 && g.total <= kSmemLimit && encode_fn() != nullptr;
 }
+
 cudaError_t launch_stage1_tc(const MultiArgs& a, cudaStream_t s) {
   const TcGeom g = tc_geom(a.n_src, a.d, a.S);
   switch (a.S) {
-    case 1: return launch_s<1>(a, g, s); case 2: return launch_s<2>(a, g, s);
-    case 3: return launch_s<3>(a, g, s); case 4: return launch_s<4>(a, g, s);
-    case 5: return launch_s<5>(a, g, s); case 6: return launch_s<6>(a, g, s);
-    case 7: return launch_s<7>(a, g, s); case 8: return launch_s<8>(a, g, s);
+    case 1: return launch_q<1>(a, g, s);
+    case 2: return launch_q<2>(a, g, s);
+    case 3: return launch_q<3>(a, g, s);
+    case 4: return launch_q<4>(a, g, s);
+    case 5: return launch_q<5>(a, g, s);
+    case 6: return launch_q<6>(a, g, s);
+    case 7: return launch_q<7>(a, g, s);
+    case 8: return launch_q<8>(a, g, s);
     default: return cudaErrorInvalidValue;
   }
 }
+
 cudaError_t take_timeout_stage1tc(unsigned int* flag) {
   unsigned int zero = 0;
   cudaError_t e = cudaMemcpyFromSymbol(flag, g_stage1tc_timeout, sizeof(unsigned int));
   if (e != cudaSuccess) return e;
   return cudaMemcpyToSymbol(g_stage1tc_timeout, &zero, sizeof(unsigned int));
 }
+
 }  // namespace attnres
