@@ -141,9 +141,9 @@ def measured_peaks() -> dict:
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) over algorithmic
 # bytes, from one ncu capture of the kernel, keyed by the sha256 prefix of the
 # kernel source it was taken with: reported as null once the source changes.
-# full_fwd_bulk_kernel: 64-source read of the 8192 x 896 pass, 939.59 MB read
-# + 14.50 MB written for 954.21 MB algorithmic.
-NCU_TRAFFIC = {("full_fwd_bulk_kernel", "f57c210b551aea4d"): (939.591 + 14.496) / 954.205}
+# full_fwd_bulk_kernel: the 21-source read (sublayer 20) of the 8192 x 896 pass,
+# 308.31 MB read + 11.26 MB written for 322.96 MB algorithmic.
+NCU_TRAFFIC = {("full_fwd_bulk_kernel", "8f802c69d1942f4b"): (308.311808 + 11.255040) / 322.961408}
 
 
 def kernel_digest(name: str) -> str:

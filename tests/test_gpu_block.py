@@ -20,7 +20,11 @@ def _built():
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("n,S,T,d", [(1, 8, 100, 1024), (4, 8, 77, 1024), (8, 8, 130, 1024),
                                      (9, 3, 41, 512), (3, 6, 50, 2048), (8, 6, 19, 2048),
-                                     (2, 1, 64, 256), (5, 5, 33, 896)])
+                                     (2, 1, 64, 256), (5, 5, 33, 896),
+                                     # bf16 tensor-core outputs: two source blocks, ragged
+                                     # tails, one 64-feature chunk, odd query counts
+                                     (12, 8, 37, 1024), (6, 8, 45, 640), (7, 8, 23, 64),
+                                     (16, 3, 29, 192)])
 def test_stage1_vs_oracle(dt, n, S, T, d):
     g = inputs.generator(10, dev())
     Src = inputs.history(n, T, d, dt, g, dev(), depth_scaled=True)
