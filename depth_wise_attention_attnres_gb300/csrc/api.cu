@@ -122,7 +122,7 @@ int make_full(const void* V, int64_t src_stride, int32_t n_src, int64_t T, int32
   const Range ro = range_of(out, E * elem_size(out_dtype));
   if (overlap(rv, ro)) return ATTNRES_ERR_INVALID_ARG;
   *a = FullArgs{V, src_stride, n_src, T, d, v_dtype == ATTNRES_BF16, w, gamma, eps, out,
-                out_dtype == ATTNRES_BF16};
+                out_dtype == ATTNRES_BF16, 0};
   return ATTNRES_OK;
 }
 
@@ -262,10 +262,19 @@ int attnres_full_pass(const void* V, int64_t src_stride, int32_t R, int64_t T, i
   const Range ro = range_of(out, ((R - 1) * out_stride + E) * elem_size(out_dtype));
   if (overlap(rv, ro)) return ATTNRES_ERR_INVALID_ARG;
   const int oes = elem_size(out_dtype);
+  // When no read writes what a later read reads (sources, W and Gamma apart
+  // from the outputs), reads after the first overlap the one before them.
+  const Range rw = range_of(W, static_cast<int64_t>(R) * d * 4);
+  const Range rg = range_of(Gamma, static_cast<int64_t>(R) * d * 4);
+  const bool independent = !overlap(rw, ro) && !overlap(rg, ro);
   for (int32_t r = 0; r < R; ++r) {
-    const int st = attnres_full_fwd(V, src_stride, r + 1, T, d, v_dtype, W + static_cast<int64_t>(r) * d,
-                                    Gamma + static_cast<int64_t>(r) * d, eps,
-                                    static_cast<char*>(out) + r * out_stride * oes, out_dtype, stream);
+    FullArgs a{};
+    int st = make_full(V, src_stride, r + 1, T, d, v_dtype, W + static_cast<int64_t>(r) * d,
+                       Gamma + static_cast<int64_t>(r) * d, eps, static_cast<char*>(out) + r * out_stride * oes,
+                       out_dtype, &a);
+    if (st != ATTNRES_OK) return st;
+    a.late_wait = independent && r > 0;
+    st = run_full(a, as_stream(stream));
     if (st != ATTNRES_OK) return st;
   }
   return ATTNRES_OK;

@@ -73,7 +73,10 @@ __global__ void __launch_bounds__((FullTraits<CH>::kNW + 1) * kWarp, FullTraits<
   const int n = a.n_src;
   const int64_t total = static_cast<int64_t>(ntiles) * n;
 
-  pdl_trigger();
+  // A read that waits for the previous kernel at its start lets the next one
+  // launch only after that wait: a later read of the same pass (which does not
+  // wait at its start) then never runs ahead of whatever wrote the sources.
+  if (a.late_wait) pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < nstage; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
@@ -82,7 +85,13 @@ __global__ void __launch_bounds__((FullTraits<CH>::kNW + 1) * kWarp, FullTraits<
     mbar_fence_init();
   }
   __syncthreads();
-  pdl_wait();  // everything below may read what the previous kernel wrote
+  // Everything below may read what the previous kernel wrote, unless this is
+  // a later read of a pass, whose inputs the previous read does not write (it
+  // then waits before it ends, so reads still complete in order).
+  if (!a.late_wait) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   if (warp == kNW) {
     // ------------------------------------------------------------ producer
@@ -221,6 +230,7 @@ __global__ void __launch_bounds__((FullTraits<CH>::kNW + 1) * kWarp, FullTraits<
     }
   }
   if (!ok) atomicOr(&g_full_timeout, 1u);
+  if (a.late_wait) pdl_wait();
 }
 
 template <typename Tin, int CH>

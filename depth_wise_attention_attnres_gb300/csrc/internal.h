@@ -23,6 +23,11 @@ struct FullArgs {
   float eps;
   void* out;
   int out_bf16;
+  // Reads of one pass after the first: none of their inputs is written by the
+  // read before them, so they wait for it (griddepcontrol.wait) at their end
+  // instead of their start, which keeps the reads completing in order while a
+  // read's loads overlap the tail of the previous one.
+  int late_wait;
 };
 
 // S queries over the same n_src sources (stage 1; the general kernel also
