@@ -74,6 +74,8 @@ def load_library(path: str):
         ctypes.c_void_p]
     lib.attnres_oracle_threads.restype = ctypes.c_int
     lib.attnres_oracle_threads.argtypes = []
+    lib.attnres_oracle_set_threads.restype = None
+    lib.attnres_oracle_set_threads.argtypes = [ctypes.c_int]
     return lib
 
 
@@ -88,6 +90,11 @@ def _load():
 def threads() -> int:
     """OpenMP threads one oracle call uses."""
     return int(_load().attnres_oracle_threads())
+
+
+def set_threads(n: int) -> None:
+    """Threads later oracle calls use (results do not depend on it)."""
+    _load().attnres_oracle_set_threads(int(n))
 
 
 # ---------------------------------------------------------------- storage ----

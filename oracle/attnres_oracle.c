@@ -139,3 +139,13 @@ int attnres_oracle_threads(void) {
   return 1;
 #endif
 }
+
+/* Threads later calls use (n >= 1); scheduling only, the arithmetic per token
+   does not depend on it. */
+void attnres_oracle_set_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
