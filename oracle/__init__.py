@@ -20,6 +20,9 @@ This module adds the sequencing the pages describe on top of it:
   the plain sum of block m's member outputs and P_k the sum of the outputs of
   the earlier sublayers of the current block. An empty running sum (j = 0) is
   not a source. Sums are exact fp64 additions of the stored outputs.
+* ``prenorm``: the consuming sublayer's pre-norm of an aggregated row,
+  RMSNorm_pre(z) (DepthBench reading notes section 2.3: f_l =
+  F_l(RMSNorm_pre,l(z_l))), which the library can emit next to z.
 * ``block_stage1`` / ``block_merge`` / ``block_accumulate``: the per-operation
   references for the two-stage computation (datacamp explainer, "two-stage
   computation"), each written as the plain read over the source set the
@@ -253,6 +256,20 @@ def block_stage1(Src, n_src, W, Gamma, eps, rows=None):
         outs.append(o)
         lses.append(l)
     return np.stack(outs), np.stack(lses)
+
+
+def prenorm(z, gamma, eps):
+    """RMSNorm_pre of each row of z: gamma * z / sqrt(mean_k z_k^2 + eps).
+
+    DepthBench reading notes section 2.3: the sublayer reads
+    F_l(RMSNorm_pre,l(z_l)); RMSNorm is read as for the keys (learned gain,
+    mean of squares over d, eps inside the root). z is fp64 (an oracle
+    result) or a stored tensor (widened exactly); gamma is [d].
+    """
+    z64 = np.asarray(z, dtype=np.float64) if isinstance(z, np.ndarray) else widen(z)
+    g = np.asarray(gamma, dtype=np.float64).reshape(-1)
+    ms = np.mean(z64 * z64, axis=-1, keepdims=True)
+    return g * z64 / np.sqrt(ms + eps)
 
 
 def block_accumulate(P, f, first):

@@ -262,10 +262,53 @@ def pin_bruteforce(orc):
         _close(fp[:, t, :], ref, 1e-12, "brute force full pass")
 
 
+# ----------------------------------------------------------------- pre-norm ----
+
+def pin_prenorm_constant_row(orc):
+    """A constant row c * 1: out_k = gamma_k * c / sqrt(c^2 + eps) (closed form)."""
+    d, c, eps = 5, -3.5, 0.25
+    gamma = np.array([1.0, 0.5, -2.0, 3.0, 0.125])
+    z = np.full((1, d), c)
+    expect = gamma * c / math.sqrt(c * c + eps)
+    _close(orc.prenorm(z, gamma, eps)[0], expect, 1e-14, "pre-norm of a constant row")
+
+
+def pin_prenorm_unit_rms(orc):
+    """gamma = 1, eps = 0: each output row is a positive multiple of its input
+    with mean square exactly 1."""
+    z = _rng(41).normal(size=(6, 9)) * np.arange(1, 7).reshape(6, 1)
+    out = orc.prenorm(z, np.ones(9), 0.0)
+    _close(np.mean(out * out, axis=1), np.ones(6), 1e-13, "mean square of the pre-norm")
+    ratio = out / z
+    _close(ratio, np.repeat(ratio[:, :1], 9, axis=1), 1e-12, "pre-norm is a per-row scaling")
+    assert np.all(ratio > 0), "pre-norm flips signs"
+
+
+def pin_prenorm_scale_invariance(orc):
+    """eps = 0: RMSNorm_pre(c z) = RMSNorm_pre(z) for c > 0, and it is odd in z."""
+    rng = _rng(42)
+    z = rng.normal(size=(4, 7))
+    gamma = rng.normal(size=7)
+    base = orc.prenorm(z, gamma, 0.0)
+    _close(orc.prenorm(13.0 * z, gamma, 0.0), base, 1e-12, "pre-norm scale invariance")
+    _close(orc.prenorm(-z, gamma, 0.0), -base, 1e-14, "pre-norm is odd")
+
+
+def pin_prenorm_of_zero_query_read(orc):
+    """w = 0 read then pre-norm: the pre-norm of the plain mean of the sources,
+    for a two-source hand case: sources (1, 3) and (3, 5), mean (2, 4), mean
+    square 10, so with eps = 6 the row is (2, 4) / 4 scaled by gamma (0.5, 2)."""
+    srcs = [np.array([[1.0, 3.0]]), np.array([[3.0, 5.0]])]
+    z, _ = orc.read(srcs, np.zeros(2), np.ones(2), 1e-6)
+    out = orc.prenorm(z, np.array([0.5, 2.0]), 6.0)
+    _close(out[0], np.array([0.25, 2.0]), 1e-9, "pre-norm of the mean")
+
+
 ALL_PINS = [
     pin_golden, pin_bf16_widening, pin_zero_query_is_mean, pin_single_source_identity,
     pin_two_sources_logistic, pin_equal_sources, pin_hardmax_limit,
     pin_permutation_invariance, pin_key_scale_invariance, pin_split_merge,
     pin_block_s1_equals_full, pin_block_zero_query_means, pin_stage1_and_merge_reference,
-    pin_bruteforce,
+    pin_bruteforce, pin_prenorm_constant_row, pin_prenorm_unit_rms,
+    pin_prenorm_scale_invariance, pin_prenorm_of_zero_query_read,
 ]

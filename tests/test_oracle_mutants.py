@@ -84,3 +84,31 @@ def _block_mutant(kind):
 def test_block_mutant_is_caught(kind, monkeypatch, oracle_mod):
     monkeypatch.setattr(oracle, "block_sources", _block_mutant(kind))
     assert _run_pins(oracle), f"block mutant {kind} passed every pin"
+
+
+def _prenorm_mutant(kind):
+    def prenorm(z, gamma, eps):
+        z64 = np.asarray(z, dtype=np.float64) if isinstance(z, np.ndarray) else oracle.widen(z)
+        g = np.asarray(gamma, dtype=np.float64).reshape(-1)
+        ms = np.mean(z64 * z64, axis=-1, keepdims=True)
+        if kind == "sum_not_mean":
+            return g * z64 / np.sqrt(ms * z64.shape[-1] + eps)
+        if kind == "eps_outside_root":
+            return g * z64 / (np.sqrt(ms) + eps)
+        if kind == "no_gain":
+            return z64 / np.sqrt(ms + eps)
+        if kind == "gain_squared":
+            return g * g * z64 / np.sqrt(ms + eps)
+        if kind == "no_root":
+            return g * z64 / (ms + eps)
+        if kind == "mean_over_rows":
+            return g * z64 / np.sqrt(np.mean(z64 * z64, axis=0, keepdims=True) + eps)
+        raise ValueError(kind)
+    return prenorm
+
+
+@pytest.mark.parametrize("kind", ["sum_not_mean", "eps_outside_root", "no_gain", "gain_squared",
+                                  "no_root", "mean_over_rows"])
+def test_prenorm_mutant_is_caught(kind, monkeypatch, oracle_mod):
+    monkeypatch.setattr(oracle, "prenorm", _prenorm_mutant(kind))
+    assert _run_pins(oracle), f"pre-norm mutant {kind} passed every pin"
