@@ -197,18 +197,34 @@ def job_throughput(tokens_per_rank: int, world: int, ms_per_step: float) -> floa
 # ---------------------------------------------------------------- our arm ----
 
 class FullPassStep:
-    def __init__(self, wl, dev):
+    """One Full pass. op "read": the reads alone; "prenorm": each read emits
+    the sublayer pre-norm of its result instead of the result (the same bytes);
+    "prenorm_both": the result and its pre-norm (one more row write per read)."""
+
+    def __init__(self, wl, dev, op="read"):
         from depth_wise_attention_attnres_gb300 import binding
         self.ar = binding
         self.wl = wl
+        self.op = op
         self.V, self.W, self.G = inputs.full_inputs(wl, dev)
-        self.out = torch.empty(wl.R, wl.T, wl.d, device=dev, dtype=inputs.DTYPES[wl.dtype])
-        self.launches = wl.R
+        dt = inputs.DTYPES[wl.dtype]
+        self.out = torch.empty(wl.R, wl.T, wl.d, device=dev, dtype=dt)
         es = 2 if wl.dtype == "bf16" else 4
         self.bytes = full_pass_bytes(wl.R, wl.T, wl.d, es)
+        if op != "read":
+            g = inputs.generator(wl.seed + 1, dev)
+            self.Gpre = 1 + 0.1 * inputs.queries(wl.R, wl.d, 1.0, g, dev)
+            self.normed = torch.empty(wl.R, wl.T, wl.d, device=dev, dtype=dt)
+            if op == "prenorm_both":
+                self.bytes += wl.R * wl.T * wl.d * es
+        self.launches = wl.R
 
     def __call__(self):
-        self.ar.attnres_full_pass(self.V, self.W, self.G, self.wl.eps, self.out)
+        if self.op == "read":
+            self.ar.attnres_full_pass(self.V, self.W, self.G, self.wl.eps, self.out)
+        else:
+            self.ar.attnres_full_pass_prenorm(self.V, self.W, self.G, self.wl.eps, self.Gpre, self.wl.eps,
+                                              self.out if self.op == "prenorm_both" else None, self.normed)
 
 
 class BlockPassStep:
@@ -235,10 +251,12 @@ class BlockPassStep:
                                    self.Src, self.O, self.lse, self.P, self.out)
 
 
-def make_step(name, dev):
+def make_step(name, dev, op="read"):
     wl = inputs.WORKLOADS[name]
     if wl.kind == "full_pass":
-        return FullPassStep(wl, dev)
+        return FullPassStep(wl, dev, op)
+    if op != "read":
+        raise ValueError("--op applies to Full-pass workloads")
     if wl.kind == "block_pass":
         return BlockPassStep(wl, dev)
     raise ValueError(f"{name} is a parity case, not a benchmark workload")
@@ -451,7 +469,7 @@ def ours(args):
     peaks = measured_peaks()
     stream = torch.cuda.Stream(device=dev)
     wl = inputs.WORKLOADS[args.workload]
-    step = make_step(args.workload, dev)
+    step = make_step(args.workload, dev, args.op)
 
     with ClockSampler(local) as clocks:
         ms, graph = time_graph(step, args.steps, args.warmup, world, stream)
@@ -466,6 +484,7 @@ def ours(args):
         "config": {"workload": wl.name, "kind": wl.kind, "T": wl.T, "d": wl.d,
                    "reads" if wl.kind == "full_pass" else "blocks": wl.R if wl.kind == "full_pass" else wl.N,
                    **({"S": wl.S} if wl.kind == "block_pass" else {}),
+                   **({"op": args.op} if args.op != "read" else {}),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (129 MB); no flush",
                    "timing": "CUDA graph of one step, CUDA events on the launching stream"},
@@ -568,11 +587,17 @@ def main():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(
         n for n, w in inputs.WORKLOADS.items() if w.kind != "full_read"))
+    p.add_argument("--op", choices=["read", "prenorm", "prenorm_both"], default="read",
+                   help="Full pass only: plain reads, reads emitting the sublayer pre-norm instead of "
+                        "their result, or both")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-block", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     args = p.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    if args.op != "read":
+        # The variants are measured on the device alone.
+        args.no_e2e = args.no_block = args.no_cpu_baseline = True
     if args.impl == "reference":
         reference(args)
     else:

@@ -8,13 +8,17 @@ from .binding import (  # noqa: F401
     AttnResError,
     attnres_abi_version,
     attnres_block_merge,
+    attnres_block_merge_prenorm,
     attnres_block_pass,
     attnres_block_stage1,
     attnres_block_summary_accumulate,
     attnres_device_status,
     attnres_full_fwd,
+    attnres_full_fwd_prenorm,
     attnres_full_pass,
+    attnres_full_pass_prenorm,
     attnres_kernel_path,
+    attnres_rmsnorm,
     attnres_status_string,
     lib,
 )

@@ -28,9 +28,16 @@ _VP, _I32, _I64, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_
 _SIGNATURES = {
     "attnres_full_fwd": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _I32, _VP],
     "attnres_full_pass": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _I64, _I32, _VP],
+    "attnres_full_fwd_prenorm": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _F, _VP, _VP,
+                                 _I32, _VP],
+    "attnres_full_pass_prenorm": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _F, _VP,
+                                  _VP, _I64, _I32, _VP],
+    "attnres_rmsnorm": [_VP, _I64, _I32, _I32, _VP, _F, _VP, _VP],
     "attnres_block_stage1": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _I32, _F,
                              ctypes.POINTER(_VP), _VP, _VP],
     "attnres_block_merge": [_VP, _VP, _VP, _VP, _I32, _VP, _VP, _F, _I64, _I32, _I32, _VP, _VP],
+    "attnres_block_merge_prenorm": [_VP, _VP, _VP, _VP, _I32, _VP, _VP, _F, _VP, _F, _I64, _I32, _I32,
+                                    _VP, _VP, _VP],
     "attnres_block_summary_accumulate": [_VP, _VP, _I32, _VP, _I64, _I32, _I32, _VP],
     "attnres_block_pass": [_VP, _I64, _I32, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _I64,
                            _I32, _VP, _VP, _VP, _VP, _I64, _VP],
@@ -157,6 +164,54 @@ def attnres_full_pass(V: torch.Tensor, W: torch.Tensor, Gamma: torch.Tensor, eps
     return out
 
 
+def attnres_full_fwd_prenorm(V: torch.Tensor, n_src: int, w: torch.Tensor, gamma: torch.Tensor,
+                             eps: float, gamma_pre: torch.Tensor, eps_pre: float,
+                             out: torch.Tensor | None, out_normed: torch.Tensor,
+                             stream=None) -> torch.Tensor:
+    """A Full read that also writes the sublayer pre-norm of its result into
+    out_normed [T, d]; out (z itself) may be None."""
+    _, T, d, stride = _slices(V)
+    if _rows(out_normed) != (T, d) or (out is not None and _rows(out) != (T, d)):
+        raise ValueError("out and out_normed must be [T, d]")
+    if out is not None and out.dtype != out_normed.dtype:
+        raise ValueError("out and out_normed must have one dtype")
+    _check("attnres_full_fwd_prenorm", lib().attnres_full_fwd_prenorm(
+        _ptr(V), stride, n_src, T, d, _dtype(V), _ptr(w), _ptr(gamma), eps, _ptr(gamma_pre),
+        eps_pre, _ptr(out), _ptr(out_normed), _dtype(out_normed), _stream(stream)))
+    return out_normed
+
+
+def attnres_full_pass_prenorm(V: torch.Tensor, W: torch.Tensor, Gamma: torch.Tensor, eps: float,
+                              Gamma_pre: torch.Tensor, eps_pre: float, out: torch.Tensor | None,
+                              out_normed: torch.Tensor, R: int | None = None,
+                              stream=None) -> torch.Tensor:
+    """R reads over history V [R, T, d], read r also writing the pre-norm of its
+    result (with Gamma_pre[r]) into out_normed[r]; out may be None."""
+    n, T, d, stride = _slices(V)
+    R = n if R is None else R
+    on, oT, od, ostride = _slices(out_normed)
+    if (oT, od) != (T, d) or on < R:
+        raise ValueError("out_normed must be [R, T, d]")
+    if out is not None:
+        if _slices(out)[1:] != (T, d, ostride) or out.shape[0] < R or out.dtype != out_normed.dtype:
+            raise ValueError("out must match out_normed")
+    _check("attnres_full_pass_prenorm", lib().attnres_full_pass_prenorm(
+        _ptr(V), stride, R, T, d, _dtype(V), _ptr(W), _ptr(Gamma), eps, _ptr(Gamma_pre), eps_pre,
+        _ptr(out), _ptr(out_normed), ostride, _dtype(out_normed), _stream(stream)))
+    return out_normed
+
+
+def attnres_rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float, out: torch.Tensor,
+                    stream=None) -> torch.Tensor:
+    """out = gamma * x / sqrt(mean(x^2) + eps) per row of x [T, d] (out may be x)."""
+    T, d = _rows(x)
+    if _rows(out) != (T, d) or out.dtype != x.dtype:
+        raise ValueError("out must be like x")
+    _check("attnres_rmsnorm", lib().attnres_rmsnorm(
+        _ptr(x), T, d, _dtype(x), _ptr(gamma), eps, _ptr(out), _stream(stream)))
+    return out
+
+
 def attnres_block_stage1(Src: torch.Tensor, n_src: int, W: torch.Tensor, Gamma: torch.Tensor,
                          eps: float, O: list, lse: torch.Tensor | None, stream=None) -> None:
     """Stage 1: the S = len(O) queries of W [S, d] over Src[0 .. n_src)."""
@@ -177,6 +232,20 @@ def attnres_block_merge(O_j: torch.Tensor, lse_j: torch.Tensor, P: torch.Tensor,
         _ptr(O_j), _ptr(lse_j), _ptr(P), _ptr(f_prev), int(bool(p_is_empty)), _ptr(w),
         _ptr(gamma), eps, T, d, _dtype(O_j), _ptr(out), _stream(stream)))
     return out
+
+
+def attnres_block_merge_prenorm(O_j: torch.Tensor, lse_j: torch.Tensor, P: torch.Tensor, f_prev,
+                                p_is_empty: bool, w: torch.Tensor, gamma: torch.Tensor, eps: float,
+                                gamma_pre: torch.Tensor, eps_pre: float, out, out_normed: torch.Tensor,
+                                stream=None) -> torch.Tensor:
+    """Stage 2 that also writes the sublayer pre-norm of the merged row into
+    out_normed; out (the merged row itself) may be None."""
+    T, d = _rows(O_j)
+    _check("attnres_block_merge_prenorm", lib().attnres_block_merge_prenorm(
+        _ptr(O_j), _ptr(lse_j), _ptr(P), _ptr(f_prev), int(bool(p_is_empty)), _ptr(w),
+        _ptr(gamma), eps, _ptr(gamma_pre), eps_pre, T, d, _dtype(O_j), _ptr(out), _ptr(out_normed),
+        _stream(stream)))
+    return out_normed
 
 
 def attnres_block_summary_accumulate(P, f: torch.Tensor, p_is_empty: bool, summary_out=None,

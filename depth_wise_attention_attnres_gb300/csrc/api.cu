@@ -144,6 +144,7 @@ int run_full(const FullArgs& a, cudaStream_t s) {
   m.eps = a.eps;
   m.out[0] = a.out;
   m.lse = nullptr;
+  m.pre = a.pre;
   return status_of(launch_multi_generic(m, s));
 }
 
@@ -280,6 +281,84 @@ int attnres_full_pass(const void* V, int64_t src_stride, int32_t R, int64_t T, i
   return ATTNRES_OK;
 }
 
+// Adds the sublayer pre-norm to a Full read's arguments: out_normed gets
+// gamma_pre * z / rms(z); out (z itself) may then be null. Checked like out.
+int add_prenorm(const void* V, int64_t src_stride, int32_t n_src, int64_t T, int32_t d, int32_t v_dtype,
+                const float* gamma_pre, float eps_pre, void* out, void* out_normed, int32_t out_dtype,
+                FullArgs* a) {
+  if (!gamma_pre || !out_normed || !valid_eps(eps_pre)) return ATTNRES_ERR_INVALID_ARG;
+  const int64_t E = T * d;
+  const Range rv = range_of(V, ((n_src - 1) * (n_src > 1 ? src_stride : 0) + E) * elem_size(v_dtype));
+  const Range rn = range_of(out_normed, E * elem_size(out_dtype));
+  const Range ro = out ? range_of(out, E * elem_size(out_dtype)) : Range{};
+  if (overlap(rn, rv) || overlap(rn, ro)) return ATTNRES_ERR_INVALID_ARG;
+  a->pre = PreNorm{gamma_pre, eps_pre, out_normed};
+  a->out = out;
+  return ATTNRES_OK;
+}
+
+int attnres_full_fwd_prenorm(const void* V, int64_t src_stride, int32_t n_src, int64_t T, int32_t d,
+                             int32_t v_dtype, const float* w, const float* gamma, float eps,
+                             const float* gamma_pre, float eps_pre, void* out, void* out_normed,
+                             int32_t out_dtype, void* stream) {
+  FullArgs a{};
+  // make_full checks the read against whichever output is given.
+  int st = make_full(V, src_stride, n_src, T, d, v_dtype, w, gamma, eps, out ? out : out_normed, out_dtype, &a);
+  if (st != ATTNRES_OK || T == 0) return st;
+  st = add_prenorm(V, src_stride, n_src, T, d, v_dtype, gamma_pre, eps_pre, out, out_normed, out_dtype, &a);
+  if (st != ATTNRES_OK) return st;
+  return run_full(a, as_stream(stream));
+}
+
+int attnres_full_pass_prenorm(const void* V, int64_t src_stride, int32_t R, int64_t T, int32_t d,
+                              int32_t v_dtype, const float* W, const float* Gamma, float eps,
+                              const float* Gamma_pre, float eps_pre, void* out, void* out_normed,
+                              int64_t out_stride, int32_t out_dtype, void* stream) {
+  if (R < 1 || d < 1 || T < 0 || !valid_dtype(v_dtype) || !valid_dtype(out_dtype) || !valid_eps(eps) ||
+      !valid_eps(eps_pre))
+    return ATTNRES_ERR_INVALID_ARG;
+  if (T == 0) return ATTNRES_OK;
+  if (!V || !W || !Gamma || !Gamma_pre || !out_normed) return ATTNRES_ERR_INVALID_ARG;
+  const int64_t E = T * d;
+  if (src_stride < E || out_stride < E) return ATTNRES_ERR_INVALID_ARG;
+  const int oes = elem_size(out_dtype);
+  const Range rv = range_of(V, ((R - 1) * src_stride + E) * elem_size(v_dtype));
+  const Range rn = range_of(out_normed, ((R - 1) * out_stride + E) * oes);
+  const Range ro = out ? range_of(out, ((R - 1) * out_stride + E) * oes) : Range{};
+  if (overlap(rv, rn) || overlap(rv, ro) || overlap(rn, ro)) return ATTNRES_ERR_INVALID_ARG;
+  const Range rw = range_of(W, static_cast<int64_t>(R) * d * 4);
+  const Range rg = range_of(Gamma, static_cast<int64_t>(R) * d * 4);
+  const Range rq = range_of(Gamma_pre, static_cast<int64_t>(R) * d * 4);
+  const bool independent = !overlap(rw, ro) && !overlap(rg, ro) && !overlap(rq, ro) && !overlap(rw, rn) &&
+                           !overlap(rg, rn) && !overlap(rq, rn);
+  for (int32_t r = 0; r < R; ++r) {
+    void* o = out ? static_cast<char*>(out) + r * out_stride * oes : nullptr;
+    void* on = static_cast<char*>(out_normed) + r * out_stride * oes;
+    FullArgs a{};
+    int st = make_full(V, src_stride, r + 1, T, d, v_dtype, W + static_cast<int64_t>(r) * d,
+                       Gamma + static_cast<int64_t>(r) * d, eps, o ? o : on, out_dtype, &a);
+    if (st != ATTNRES_OK) return st;
+    st = add_prenorm(V, src_stride, r + 1, T, d, v_dtype, Gamma_pre + static_cast<int64_t>(r) * d, eps_pre, o, on,
+                     out_dtype, &a);
+    if (st != ATTNRES_OK) return st;
+    a.late_wait = independent && r > 0;
+    st = run_full(a, as_stream(stream));
+    if (st != ATTNRES_OK) return st;
+  }
+  return ATTNRES_OK;
+}
+
+int attnres_rmsnorm(const void* x, int64_t T, int32_t d, int32_t dtype, const float* gamma, float eps, void* out,
+                    void* stream) {
+  if (d < 1 || T < 0 || !valid_dtype(dtype) || !valid_eps(eps)) return ATTNRES_ERR_INVALID_ARG;
+  if (T == 0) return ATTNRES_OK;
+  if (!x || !gamma || !out) return ATTNRES_ERR_INVALID_ARG;
+  const int64_t bytes = T * d * elem_size(dtype);
+  // In place (out == x) is allowed; a partial overlap is not.
+  if (out != x && overlap(range_of(x, bytes), range_of(out, bytes))) return ATTNRES_ERR_INVALID_ARG;
+  return status_of(launch_rmsnorm(x, T, d, dtype == ATTNRES_BF16, gamma, eps, out, as_stream(stream)));
+}
+
 int attnres_block_stage1(const void* Src, int64_t src_stride, int32_t n_src, int64_t T, int32_t d,
                          int32_t dtype, const float* W, const float* Gamma, int32_t S, float eps,
                          void* const* O, float* lse, void* stream) {
@@ -295,6 +374,29 @@ int attnres_block_merge(const void* O_j, const float* lse_j, float* P, const voi
   MergeArgs a{};
   const int st = make_merge(O_j, lse_j, P, f_prev, p_is_empty, w, gamma, eps, T, d, dtype, out, &a);
   if (st != ATTNRES_OK || T == 0) return st;
+  return status_of(launch_merge(a, as_stream(stream), merge_fast_ok(a)));
+}
+
+int attnres_block_merge_prenorm(const void* O_j, const float* lse_j, float* P, const void* f_prev,
+                                int32_t p_is_empty, const float* w, const float* gamma, float eps,
+                                const float* gamma_pre, float eps_pre, int64_t T, int32_t d, int32_t dtype,
+                                void* out, void* out_normed, void* stream) {
+  if (!gamma_pre || !out_normed || !valid_eps(eps_pre)) return ATTNRES_ERR_INVALID_ARG;
+  MergeArgs a{};
+  // make_merge checks the merge against whichever output is given.
+  int st = make_merge(O_j, lse_j, P, f_prev, p_is_empty, w, gamma, eps, T, d, dtype, out ? out : out_normed, &a);
+  if (st != ATTNRES_OK || T == 0) return st;
+  if (out) {
+    const int64_t E = T * d;
+    const int es = elem_size(dtype);
+    const Range rn = range_of(out_normed, E * es);
+    if (overlap(rn, range_of(out, E * es)) || overlap(rn, range_of(O_j, E * es)) ||
+        overlap(rn, range_of(P, E * 4)) || overlap(rn, range_of(lse_j, T * 4)) ||
+        (f_prev && overlap(rn, range_of(f_prev, E * es))))
+      return ATTNRES_ERR_INVALID_ARG;
+  }
+  a.out = out;
+  a.pre = PreNorm{gamma_pre, eps_pre, out_normed};
   return status_of(launch_merge(a, as_stream(stream), merge_fast_ok(a)));
 }
 

@@ -45,7 +45,9 @@ struct FullTraits {
   static constexpr bool kKeepX = CH <= 4 || (CH >= 6 && CH <= 8);
 };
 
-template <typename Tin, int CH>
+// kPre: the epilogue also writes the sublayer pre-norm of the row (a separate
+// instance, so the plain read keeps its own code and schedule).
+template <typename Tin, int CH, bool kPre>
 __global__ void __launch_bounds__((FullTraits<CH>::kNW + 1) * kWarp, FullTraits<CH>::kMinBlocks)
     full_fwd_bulk_kernel(FullArgs a, int nstage) {
   constexpr int kNW = FullTraits<CH>::kNW;  // consumer warps = rows per tile
@@ -58,7 +60,8 @@ __global__ void __launch_bounds__((FullTraits<CH>::kNW + 1) * kWarp, FullTraits<
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty_bar = full_bar + kMaxStages;
   float* wq = reinterpret_cast<float*>(smem + kBarBytes);  // w * gamma, [D]
-  Tin* stages = reinterpret_cast<Tin*>(smem + kBarBytes + D * sizeof(float));
+  float* gq = wq + D;                                       // kPre: gamma_pre, [D]
+  Tin* stages = reinterpret_cast<Tin*>(smem + kBarBytes + (kPre ? 2 : 1) * D * sizeof(float));
   constexpr int kStageElems = kTM * D;
 
   const int warp = threadIdx.x >> 5;
@@ -138,6 +141,7 @@ __global__ void __launch_bounds__((FullTraits<CH>::kNW + 1) * kWarp, FullTraits<
     const float4 w4 = reinterpret_cast<const float4*>(a.w)[i];
     const float4 g4 = reinterpret_cast<const float4*>(a.gamma)[i];
     reinterpret_cast<float4*>(wq)[i] = make_float4(w4.x * g4.x, w4.y * g4.y, w4.z * g4.z, w4.w * g4.w);
+    if constexpr (kPre) reinterpret_cast<float4*>(gq)[i] = reinterpret_cast<const float4*>(a.pre.gamma)[i];
   }
   named_sync(1, kNW * kWarp);
   const float inv_d = 1.0f / static_cast<float>(D);
@@ -215,7 +219,7 @@ __global__ void __launch_bounds__((FullTraits<CH>::kNW + 1) * kWarp, FullTraits<
       }
     }
 
-    if (ok && valid) {
+    if (!kPre && ok && valid) {
       const float inv = 1.0f / l;
 #pragma unroll
       for (int c = 0; c < CH; ++c) {
@@ -227,31 +231,69 @@ __global__ void __launch_bounds__((FullTraits<CH>::kNW + 1) * kWarp, FullTraits<
         else
           st4(static_cast<float*>(a.out) + row * D + k, o);
       }
+    } else if (kPre && ok && valid) {
+      // With the sublayer's pre-norm: z (if it is wanted), then
+      // gamma_pre * z / rms(z) from z in fp32.
+      const float inv = 1.0f / l;
+      const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+      for (int e = 0; e < NE / 2; ++e) acc[e] = fmul2(acc[e], inv2);
+      float2 q2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int k = (c * kWarp + lane) * 4;
+        q2 = ffma2(acc[c * 2], acc[c * 2], q2);
+        q2 = ffma2(acc[c * 2 + 1], acc[c * 2 + 1], q2);
+        if (a.out) {
+          const float o[4] = {acc[c * 2].x, acc[c * 2].y, acc[c * 2 + 1].x, acc[c * 2 + 1].y};
+          if (a.out_bf16)
+            st4(static_cast<bf16*>(a.out) + row * D + k, o);
+          else
+            st4(static_cast<float*>(a.out) + row * D + k, o);
+        }
+      }
+      const float rr = rsqrtf(warp_sum(q2.x + q2.y) * inv_d + a.pre.eps);
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int k = (c * kWarp + lane) * 4;
+        const float4 g4 = *reinterpret_cast<const float4*>(gq + k);
+        const float o[4] = {g4.x * (acc[c * 2].x * rr), g4.y * (acc[c * 2].y * rr), g4.z * (acc[c * 2 + 1].x * rr),
+                            g4.w * (acc[c * 2 + 1].y * rr)};
+        if (a.out_bf16)
+          st4(static_cast<bf16*>(a.pre.out) + row * D + k, o);
+        else
+          st4(static_cast<float*>(a.pre.out) + row * D + k, o);
+      }
     }
   }
   if (!ok) atomicOr(&g_full_timeout, 1u);
   if (a.late_wait) pdl_wait();
 }
 
-template <typename Tin, int CH>
-cudaError_t launch_ch(const FullArgs& a, cudaStream_t s) {
+template <typename Tin, int CH, bool kPre>
+cudaError_t launch_chp(const FullArgs& a, cudaStream_t s) {
   constexpr int D = CH * 128;
   constexpr int kTM = FullTraits<CH>::kNW;
   constexpr int kThreads = (kTM + 1) * kWarp;
   const int stage_bytes = kTM * D * static_cast<int>(sizeof(Tin));
-  const int fixed = kBarBytes + D * static_cast<int>(sizeof(float));
+  const int fixed = kBarBytes + (kPre ? 2 : 1) * D * static_cast<int>(sizeof(float));
   int nstage = (kSmemPerSM / FullTraits<CH>::kMinBlocks - 1024 - fixed) / stage_bytes;
   nstage = nstage < 2 ? 2 : (nstage > kMaxStages ? kMaxStages : nstage);
   const int smem = fixed + nstage * stage_bytes;
-  const void* fn = reinterpret_cast<const void*>(&full_fwd_bulk_kernel<Tin, CH>);
+  const void* fn = reinterpret_cast<const void*>(&full_fwd_bulk_kernel<Tin, CH, kPre>);
   cudaError_t e = allow_dynamic_smem(fn, smem);
   if (e != cudaSuccess) return e;
   const int per_sm = blocks_per_sm(fn, kThreads, smem);
   const int64_t tiles = (a.T + kTM - 1) / kTM;
   int64_t grid = static_cast<int64_t>(sm_count()) * (per_sm > 0 ? per_sm : 1);
   if (grid > tiles) grid = tiles;
-  return launch_pdl(full_fwd_bulk_kernel<Tin, CH>, static_cast<unsigned>(grid), kThreads, smem, s, a,
+  return launch_pdl(full_fwd_bulk_kernel<Tin, CH, kPre>, static_cast<unsigned>(grid), kThreads, smem, s, a,
                     nstage);
+}
+
+template <typename Tin, int CH>
+cudaError_t launch_ch(const FullArgs& a, cudaStream_t s) {
+  return a.pre.gamma ? launch_chp<Tin, CH, true>(a, s) : launch_chp<Tin, CH, false>(a, s);
 }
 
 template <typename Tin>
@@ -296,7 +338,7 @@ bool full_fast_ok(const FullArgs& a) {
   const int ch = a.d / 128;
   const bool ch_ok = (a.d % 128 == 0) && ((ch >= 1 && ch <= 8) || ch == 10 || ch == 12 || ch == 16);
   return ch_ok && aligned16(a.V) && aligned16(a.out) && aligned16(a.w) && aligned16(a.gamma) &&
-         ((a.src_stride * es) % 16 == 0);
+         ((a.src_stride * es) % 16 == 0) && (!a.pre.gamma || (aligned16(a.pre.gamma) && aligned16(a.pre.out)));
 }
 
 cudaError_t launch_full_fast(const FullArgs& a, cudaStream_t s) {

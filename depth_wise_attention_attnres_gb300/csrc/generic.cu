@@ -73,10 +73,22 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) multi_generic_kernel(Mult
     // Pass 2: weighted sum of the raw values.
     for (int j = 0; j < S; ++j) {
       const float* p = my + j * n;
+      float q = 0.f;
       for (int k = lane; k < d; k += 32) {
         float acc = 0.f;
         for (int i = 0; i < n; ++i) acc += p[i] * ld<T>(a.V, i * a.src_stride + row * d + k);
-        static_cast<T*>(a.out[j])[row * d + k] = from_f32<T>(acc);
+        if (a.out[j]) static_cast<T*>(a.out[j])[row * d + k] = from_f32<T>(acc);
+        q = fmaf(acc, acc, q);
+      }
+      if (j == 0 && a.pre.gamma) {
+        // Pass 3 (a Full read with the sublayer's pre-norm): the row again,
+        // scaled by 1 / rms of its fp32 values.
+        const float rr = rsqrtf(warp_sum(q) * inv_d + a.pre.eps);
+        for (int k = lane; k < d; k += 32) {
+          float acc = 0.f;
+          for (int i = 0; i < n; ++i) acc += p[i] * ld<T>(a.V, i * a.src_stride + row * d + k);
+          static_cast<T*>(a.pre.out)[row * d + k] = from_f32<T>(a.pre.gamma[k] * (acc * rr));
+        }
       }
     }
     __syncwarp();

@@ -11,6 +11,15 @@
 namespace attnres {
 
 // One Full AttnRes read (one query) over n_src sources.
+// The consuming sublayer's pre-norm, emitted next to an aggregated row z:
+// out = gamma * z / sqrt(mean(z^2) + eps), from z in fp32 before rounding
+// (DepthBench reading notes section 2.3: f_l = F_l(RMSNorm_pre,l(z_l))).
+struct PreNorm {
+  const float* gamma;   // [d]; nullptr: no pre-norm output
+  float eps;
+  void* out;            // [T, d] in the output dtype
+};
+
 struct FullArgs {
   const void* V;
   int64_t src_stride;  // elements
@@ -28,6 +37,7 @@ struct FullArgs {
   // instead of their start, which keeps the reads completing in order while a
   // read's loads overlap the tail of the previous one.
   int late_wait;
+  PreNorm pre;          // out may be nullptr when pre.gamma is set
 };
 
 // S queries over the same n_src sources (stage 1; the general kernel also
@@ -45,6 +55,7 @@ struct MultiArgs {
   float eps;
   void* out[ATTNRES_MAX_QUERIES];
   float* lse;           // [S, T] or nullptr
+  PreNorm pre;          // S == 1 only (a Full read); out[0] may then be nullptr
 };
 
 struct MergeArgs {
@@ -59,7 +70,8 @@ struct MergeArgs {
   int64_t T;
   int d;
   int bf16;
-  void* out;
+  void* out;            // may be nullptr when pre.gamma is set
+  PreNorm pre;
 };
 
 struct AccumArgs {
@@ -86,6 +98,9 @@ cudaError_t launch_stage1_fast(const MultiArgs& a, cudaStream_t s);
 cudaError_t launch_stage1_tc(const MultiArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s, bool fast);
 cudaError_t launch_accum(const AccumArgs& a, cudaStream_t s, bool fast);
+// RMSNorm of each row of x [T, d] (storage dtype in and out; out may be x).
+cudaError_t launch_rmsnorm(const void* x, int64_t T, int d, int is_bf16, const float* gamma, float eps, void* out,
+                           cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(cudaStream_t s);
 
 // Device-side timeout records of each kernel file: read and clear (blocking).

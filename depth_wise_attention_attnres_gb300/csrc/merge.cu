@@ -62,7 +62,8 @@ struct MergeGeom {
   int wq_off, red_off, stage_off, total;
 };
 
-inline MergeGeom merge_geom(int d, int es) {
+// pre: room for gamma_pre next to w * gamma (the pre-norm merge).
+inline MergeGeom merge_geom(int d, int es, bool pre) {
   MergeGeom g{};
   const int row_bytes = d * (2 * es + 4);
   g.TM = 8;
@@ -70,20 +71,24 @@ inline MergeGeom merge_geom(int d, int es) {
   g.wpr = kMNW / g.TM;
   g.stage_bytes = g.TM * row_bytes;
   g.wq_off = kMBar;
-  g.red_off = g.wq_off + d * 4;
-  g.stage_off = (g.red_off + kMNW * 3 * 4 + 127) / 128 * 128;
+  g.red_off = g.wq_off + (pre ? 2 : 1) * d * 4;
+  g.stage_off = (g.red_off + kMNW * 4 * 4 + 127) / 128 * 128;  // [kMNW][3] sums + [kMNW] pre-norm sums
   g.total = g.stage_off + kMStages * g.stage_bytes;
   return g;
 }
 
 // Q = 4-feature chunks per lane (a warp covers at most 128 * Q features).
-template <typename T, int Q>
+// kPre: also write the sublayer pre-norm of the merged row (a separate
+// instance, so the plain merge keeps its own code).
+template <typename T, int Q, bool kPre>
 __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, MergeGeom g) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty_bar = full_bar + kMStages;
   float* wq = reinterpret_cast<float*>(smem + g.wq_off);
+  float* gq = wq + a.d;                                      // kPre: gamma_pre
   float* red = reinterpret_cast<float*>(smem + g.red_off);  // [kMNW][3]
+  float* red2 = red + kMNW * 3;                              // [kMNW] pre-norm partial sums
   unsigned char* stages = smem + g.stage_off;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = a.d, TM = g.TM;
@@ -144,7 +149,10 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
   }
 
   // -------------------------------------------------------------- consumers
-  for (int i = threadIdx.x; i < d; i += kMNW * 32) wq[i] = a.w[i] * a.gamma[i];
+  for (int i = threadIdx.x; i < d; i += kMNW * 32) {
+    wq[i] = a.w[i] * a.gamma[i];
+    if constexpr (kPre) gq[i] = a.pre.gamma[i];
+  }
   named_sync(1, kMNW * 32);
   const int wpr = g.wpr;
   const int rslot = warp / wpr;                     // row of the tile
@@ -214,6 +222,7 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
         rok = rok && red[(rslot * wpr + w) * 3 + 2] != 0.f;
       }
     }
+    float zq = 0.f;  // this lane's share of sum(out^2), for the pre-norm
     if (rok && live) {
       const float sP = dot * rsqrtf(ss * inv_d + a.eps);
       const float M = fmaxf(lse, sP);
@@ -226,13 +235,42 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
         if (k < kend) {
           float x[4];
           lds4(so + k, x);
-          const float r[4] = {fmaf(ca, x[0], cb * p[q][0]), fmaf(ca, x[1], cb * p[q][1]),
-                              fmaf(ca, x[2], cb * p[q][2]), fmaf(ca, x[3], cb * p[q][3])};
-          st4(static_cast<T*>(a.out) + row * d + k, r);
+          // The merged row overwrites p (no longer needed).
+          p[q][0] = fmaf(ca, x[0], cb * p[q][0]);
+          p[q][1] = fmaf(ca, x[1], cb * p[q][1]);
+          p[q][2] = fmaf(ca, x[2], cb * p[q][2]);
+          p[q][3] = fmaf(ca, x[3], cb * p[q][3]);
+          if (!kPre || a.out) st4(static_cast<T*>(a.out) + row * d + k, p[q]);
+          zq = fmaf(p[q][0], p[q][0], zq); zq = fmaf(p[q][1], p[q][1], zq);
+          zq = fmaf(p[q][2], p[q][2], zq); zq = fmaf(p[q][3], p[q][3], zq);
         }
       }
     }
-    if (wpr > 1) named_sync(2 + rslot, wpr * 32);  // partners are done reading red[]
+    if constexpr (kPre) {
+      // The sublayer's pre-norm of the merged row (its parts meet like the
+      // score sums; red2 is rewritten only after the barrier below).
+      zq = warp_sum(zq);
+      if (wpr > 1) {
+        if (lane == 0) red2[warp] = zq;
+        named_sync(2 + rslot, wpr * 32);
+        zq = 0.f;
+        for (int w = 0; w < wpr; ++w) zq += red2[rslot * wpr + w];
+      }
+      if (rok && live) {
+        const float rr = rsqrtf(zq * inv_d + a.pre.eps);
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+          const int k = kbeg + (q * 32 + lane) * 4;
+          if (k < kend) {
+            const float4 g4 = *reinterpret_cast<const float4*>(gq + k);
+            const float y[4] = {g4.x * (p[q][0] * rr), g4.y * (p[q][1] * rr), g4.z * (p[q][2] * rr),
+                                g4.w * (p[q][3] * rr)};
+            st4(static_cast<T*>(a.pre.out) + row * d + k, y);
+          }
+        }
+      }
+    }
+    if (wpr > 1) named_sync(2 + rslot, wpr * 32);  // partners are done reading red[] and red2[]
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
     if (++s == kMStages) {
@@ -277,11 +315,49 @@ __global__ void __launch_bounds__(kBlock) merge_generic_kernel(MergeArgs a) {
     const float M = fmaxf(lse, s);
     const float ea = __expf(lse - M), eb = __expf(s - M);
     const float inv = 1.0f / (ea + eb);
+    float zq = 0.f;
     for (int k = lane; k < d; k += 32) {
       const int64_t off = row * d + k;
       const float o = to_f32(static_cast<const T*>(a.O)[off]);
-      static_cast<T*>(a.out)[off] = from_f32<T>(fmaf(ea * inv, o, eb * inv * a.P[off]));
+      const float z = fmaf(ea * inv, o, eb * inv * a.P[off]);
+      if (a.out) static_cast<T*>(a.out)[off] = from_f32<T>(z);
+      zq = fmaf(z, z, zq);
     }
+    if (a.pre.gamma) {
+      // The sublayer's pre-norm: the merged row again, scaled by 1 / its rms.
+      const float rr = rsqrtf(warp_sum(zq) * inv_d + a.pre.eps);
+      for (int k = lane; k < d; k += 32) {
+        const int64_t off = row * d + k;
+        const float o = to_f32(static_cast<const T*>(a.O)[off]);
+        const float z = fmaf(ea * inv, o, eb * inv * a.P[off]);
+        static_cast<T*>(a.pre.out)[off] = from_f32<T>(a.pre.gamma[k] * (z * rr));
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------- RMSNorm ------
+// out = gamma * x / sqrt(mean(x^2) + eps) per row, one warp per row, fp32
+// arithmetic; the sublayer pre-norm of a row that needs no merge (the first
+// sublayer of a block, whose output stage 1 writes).
+template <typename T>
+__global__ void __launch_bounds__(kBlock) rmsnorm_kernel(const T* x, int64_t ntok, int d, const float* gamma,
+                                                        float eps, T* out) {
+  pdl_trigger();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float inv_d = 1.0f / static_cast<float>(d);
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + warp; row < ntok;
+       row += static_cast<int64_t>(gridDim.x) * kWarps) {
+    const T* xr = x + row * d;
+    float q = 0.f;
+    for (int k = lane; k < d; k += 32) {
+      const float v = to_f32(xr[k]);
+      q = fmaf(v, v, q);
+    }
+    const float rr = rsqrtf(warp_sum(q) * inv_d + eps);
+    // Each lane rewrites only the elements it read, so out may be x.
+    for (int k = lane; k < d; k += 32) out[row * d + k] = from_f32<T>(gamma[k] * (to_f32(xr[k]) * rr));
   }
 }
 
@@ -336,10 +412,12 @@ unsigned grid_for(int64_t work_items, int per_block, const void* kernel) {
 bool merge_fast_ok(const MergeArgs& a) {
   const int es = a.bf16 ? 2 : 4;
   if (a.d % 4 != 0 || (a.d * es) % 16 != 0) return false;
-  const MergeGeom g = merge_geom(a.d, es);
+  const MergeGeom g = merge_geom(a.d, es, a.pre.gamma != nullptr);
   const int per_warp = (a.d + g.wpr - 1) / g.wpr;
-  if (per_warp > 8 * 128 || g.total > 227 * 1024) return false;
-  return aligned16(a.O) && aligned16(a.P) && aligned16(a.out) && (a.f == nullptr || aligned16(a.f));
+  // Every part of a row starts on a 4-feature chunk (aligned vector loads).
+  if (per_warp % 4 != 0 || per_warp > 8 * 128 || g.total > 227 * 1024) return false;
+  return aligned16(a.O) && aligned16(a.P) && aligned16(a.out) && (a.f == nullptr || aligned16(a.f)) &&
+         (!a.pre.gamma || (aligned16(a.pre.gamma) && aligned16(a.pre.out)));
 }
 
 bool accum_fast_ok(const AccumArgs& a) {
@@ -350,7 +428,7 @@ bool accum_fast_ok(const AccumArgs& a) {
 namespace {
 template <typename T, int Q>
 cudaError_t launch_merge_tiles(const MergeArgs& a, const MergeGeom& g, cudaStream_t s) {
-  auto k = merge_tile_kernel<T, Q>;
+  auto k = a.pre.gamma ? merge_tile_kernel<T, Q, true> : merge_tile_kernel<T, Q, false>;
   cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(k), g.total);
   if (e != cudaSuccess) return e;
   int64_t grid = (a.T + g.TM - 1) / g.TM;
@@ -361,7 +439,7 @@ cudaError_t launch_merge_tiles(const MergeArgs& a, const MergeGeom& g, cudaStrea
 
 template <typename T>
 cudaError_t launch_merge_dtype(const MergeArgs& a, cudaStream_t s) {
-  const MergeGeom g = merge_geom(a.d, sizeof(T));
+  const MergeGeom g = merge_geom(a.d, sizeof(T), a.pre.gamma != nullptr);
   const int per_warp = (a.d + g.wpr - 1) / g.wpr;
   int q = 1;
   while (q * 128 < per_warp) q <<= 1;
@@ -392,6 +470,19 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s, bool fast) {
     k<<<grid_for(a.T, kWarps, reinterpret_cast<const void*>(k)), kBlock, 0, s>>>(a);
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const void* x, int64_t T, int d, int is_bf16, const float* gamma, float eps, void* out,
+                           cudaStream_t s) {
+  const int64_t blocks = (T + kWarps - 1) / kWarps;
+  if (is_bf16) {
+    auto k = rmsnorm_kernel<bf16>;
+    return launch_pdl(k, grid_for(blocks * kBlock, kBlock, reinterpret_cast<const void*>(k)), kBlock, 0, s,
+                      static_cast<const bf16*>(x), T, d, gamma, eps, static_cast<bf16*>(out));
+  }
+  auto k = rmsnorm_kernel<float>;
+  return launch_pdl(k, grid_for(blocks * kBlock, kBlock, reinterpret_cast<const void*>(k)), kBlock, 0, s,
+                    static_cast<const float*>(x), T, d, gamma, eps, static_cast<float*>(out));
 }
 
 cudaError_t launch_accum(const AccumArgs& a, cudaStream_t s, bool fast) {

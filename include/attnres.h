@@ -108,6 +108,48 @@ int attnres_full_pass(const void* V, int64_t src_stride, int32_t R, int64_t T,
                       void* stream);
 
 /*
+ * attnres_full_fwd_prenorm / attnres_full_pass_prenorm - the same reads,
+ * each also emitting the consuming sublayer's pre-norm of its result
+ * (DepthBench reading notes section 2.3: the sublayer computes
+ * f_l = F_l(RMSNorm_pre,l(z_l)) from the aggregated z_l). The row is
+ * normalised while it is still in registers, which saves the sublayer a read
+ * of z:
+ *
+ *   out_normed[t, k] = gamma_pre[k] * z[t, k] / sqrt(mean_k z[t, k]^2 + eps_pre)
+ *
+ * from z in fp32 before it is rounded to out_dtype.
+ *
+ *   gamma_pre   device, fp32 [d] (pass: [R, d], row r for read r).
+ *   eps_pre     >= 0.
+ *   out         as for the plain read, or NULL: z itself is then not stored.
+ *   out_normed  device, [T, d] of out_dtype (pass: R of them, out_stride
+ *               elements apart, like out); must not overlap V, out, W,
+ *               Gamma or gamma_pre. Not NULL.
+ */
+int attnres_full_fwd_prenorm(const void* V, int64_t src_stride, int32_t n_src, int64_t T,
+                             int32_t d, int32_t v_dtype, const float* w, const float* gamma,
+                             float eps, const float* gamma_pre, float eps_pre, void* out,
+                             void* out_normed, int32_t out_dtype, void* stream);
+int attnres_full_pass_prenorm(const void* V, int64_t src_stride, int32_t R, int64_t T,
+                              int32_t d, int32_t v_dtype, const float* W, const float* Gamma,
+                              float eps, const float* Gamma_pre, float eps_pre, void* out,
+                              void* out_normed, int64_t out_stride, int32_t out_dtype,
+                              void* stream);
+
+/*
+ * attnres_rmsnorm - RMSNorm of each row, out = gamma * x / sqrt(mean(x^2) + eps)
+ * in fp32, stored in dtype: the sublayer pre-norm for a row no aggregation
+ * call produces with it (the first sublayer of a block, whose output is
+ * stage 1's O[0]).
+ *
+ *   x, out   device, [T, d] of dtype; out may be x (in place) but must not
+ *            otherwise overlap it.
+ *   gamma    device, fp32 [d].  eps >= 0.
+ */
+int attnres_rmsnorm(const void* x, int64_t T, int32_t d, int32_t dtype, const float* gamma,
+                    float eps, void* out, void* stream);
+
+/*
  * attnres_block_stage1 - stage 1 of the two-stage Block AttnRes computation
  * (datacamp explainer, "two-stage computation"): the S pseudo-queries of one
  * block against the cross-block sources, each source row read once for all S.
@@ -146,6 +188,19 @@ int attnres_block_stage1(const void* Src, int64_t src_stride, int32_t n_src, int
 int attnres_block_merge(const void* O_j, const float* lse_j, float* P, const void* f_prev,
                         int32_t p_is_empty, const float* w, const float* gamma, float eps,
                         int64_t T, int32_t d, int32_t dtype, void* out, void* stream);
+
+/*
+ * attnres_block_merge_prenorm - the same merge, also emitting the sublayer's
+ * pre-norm of the merged row (see attnres_full_fwd_prenorm):
+ * out_normed = gamma_pre * z / sqrt(mean(z^2) + eps_pre) from z in fp32.
+ * out may be NULL (z not stored); out_normed ([T, d] dtype, not NULL) must not
+ * overlap out, O_j, lse_j, P or f_prev.
+ */
+int attnres_block_merge_prenorm(const void* O_j, const float* lse_j, float* P,
+                                const void* f_prev, int32_t p_is_empty, const float* w,
+                                const float* gamma, float eps, const float* gamma_pre,
+                                float eps_pre, int64_t T, int32_t d, int32_t dtype, void* out,
+                                void* out_normed, void* stream);
 
 /*
  * attnres_block_summary_accumulate - running sum of a block and the block

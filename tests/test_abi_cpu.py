@@ -70,6 +70,33 @@ def test_other_entry_validation(lib):
                                   5 * P, 6 * P, 64, None) == INVALID
 
 
+def test_prenorm_entry_validation(lib):
+    # (V, stride, n, T, d, dtype, w, gamma, eps, gamma_pre, eps_pre, out, out_normed, dtype)
+    ok = (P, 64, 2, 4, 16, 1, P, P, 1e-6, P, 1e-6, 8 * P, 9 * P, 1)
+    bad = [
+        ok[:9] + (None,) + ok[10:],                      # no gamma_pre
+        ok[:12] + (None,) + ok[13:],                     # no out_normed
+        ok[:10] + (-1.0,) + ok[11:],                     # eps_pre < 0
+        ok[:12] + (P + 64,) + ok[13:],                   # out_normed overlaps V
+        ok[:12] + (8 * P + 16,) + ok[13:],               # out_normed overlaps out
+    ]
+    for args in bad:
+        assert lib.attnres_full_fwd_prenorm(*args, None) == INVALID, args
+    none_out = ok[:11] + (None,) + ok[12:]
+    assert lib.attnres_full_fwd_prenorm(*(none_out[:3] + (0,) + none_out[4:]), None) == 0  # T = 0
+    # pass: normed outputs overlapping the history
+    assert lib.attnres_full_pass_prenorm(P, 64, 2, 4, 16, 1, P, P, 1e-6, P, 1e-6, None, P + 64, 64, 1,
+                                         None) == INVALID
+    # merge: no out_normed, out_normed aliasing P
+    assert lib.attnres_block_merge_prenorm(P, 2 * P, 3 * P, 4 * P, 0, P, P, 1e-6, P, 1e-6, 4, 16, 1,
+                                           5 * P, None, None) == INVALID
+    assert lib.attnres_block_merge_prenorm(P, 2 * P, 3 * P, 4 * P, 0, P, P, 1e-6, P, 1e-6, 4, 16, 1,
+                                           5 * P, 3 * P, None) == INVALID
+    # rmsnorm: partial overlap (in place is fine, validated only)
+    assert lib.attnres_rmsnorm(P, 4, 16, 1, P, 1e-6, P + 32, None) == INVALID
+    assert lib.attnres_rmsnorm(P, 0, 16, 1, P, 1e-6, P, None) == 0
+
+
 def test_kernel_selection(lib):
     A = 1 << 20
     # Full read: d multiple of 128 and 16-byte alignment -> fast kernel.

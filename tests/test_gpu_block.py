@@ -59,7 +59,7 @@ def test_stage1_general_kernel(dt, n, S, T, d):
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
-@pytest.mark.parametrize("T,d", [(100, 1024), (33, 2048), (64, 896), (10, 100), (7, 3)])
+@pytest.mark.parametrize("T,d", [(100, 1024), (33, 2048), (64, 896), (10, 100), (7, 3), (41, 1096)])
 @pytest.mark.parametrize("mode", ["extend", "start", "as_is"])
 def test_merge_vs_oracle(dt, T, d, mode):
     """Stage-1 result from the oracle, merged on the GPU with the running sum."""
