@@ -20,6 +20,11 @@ This module adds the sequencing the pages describe on top of it:
   the plain sum of block m's member outputs and P_k the sum of the outputs of
   the earlier sublayers of the current block. An empty running sum (j = 0) is
   not a source. Sums are exact fp64 additions of the stored outputs.
+* ``read_bwd`` / ``full_read_bwd``: the gradients of one read with respect to
+  its sources, its query w and its key-norm gain gamma, given the gradient of
+  the result, by the chain rule through the read's definition (the
+  backward the pages point to when they note that stored sublayer outputs
+  are reused for it; DepthBench reading notes section 2.3 for the read).
 * ``prenorm``: the consuming sublayer's pre-norm of an aggregated row,
   RMSNorm_pre(z) (DepthBench reading notes section 2.3: f_l =
   F_l(RMSNorm_pre,l(z_l))), which the library can emit next to z.
@@ -181,6 +186,40 @@ def read(sources, w, gamma, eps, rows=None):
     if rc != 0:
         raise ValueError(f"attnres_oracle_read failed with code {rc}")
     return out, lse
+
+
+def read_bwd(sources, w, gamma, eps, dz):
+    """Gradients of one read: (dV fp64 [n, T, d], dw fp64 [d], dgamma fp64 [d]).
+
+    dz is dL/dz for the read's result z ([T, d], stored or fp64). The read is
+    e_i = w . (gamma * v_i) * r_i with r_i = 1 / sqrt(mean_k v_ik^2 + eps),
+    a = softmax_i(e), z = sum_i a_i v_i. With u = w * gamma, per token:
+      dL/da_i = dz . v_i;  dL/de_i = a_i (dL/da_i - sum_j a_j dL/da_j)
+      dL/dv_i = a_i dz + dL/de_i (r_i u - e_i r_i^2 v_i / d)
+      dL/du = sum_i dL/de_i r_i v_i  (summed over tokens);
+      dL/dw = dL/du * gamma, dL/dgamma = dL/du * w.
+    """
+    V = np.stack([widen(s) if not isinstance(s, np.ndarray) else np.asarray(s, np.float64)
+                  for s in sources])                      # [n, T, d]
+    g = np.asarray(dz, dtype=np.float64) if isinstance(dz, np.ndarray) else widen(dz)
+    d = V.shape[-1]
+    w64 = np.asarray(w, dtype=np.float64).reshape(d)
+    g64 = np.asarray(gamma, dtype=np.float64).reshape(d)
+    u = w64 * g64
+    r = 1.0 / np.sqrt(np.mean(V * V, axis=-1) + eps)      # [n, T]
+    e = r * np.einsum("ntk,k->nt", V, u)
+    a = np.exp(e - e.max(axis=0, keepdims=True))
+    a /= a.sum(axis=0, keepdims=True)
+    da = np.einsum("ntk,tk->nt", V, g)
+    de = a * (da - np.sum(a * da, axis=0, keepdims=True))
+    dV = a[..., None] * g[None] + de[..., None] * (r[..., None] * u - (e * r * r / d)[..., None] * V)
+    du = np.einsum("nt,ntk->k", de * r, V)
+    return dV, du * g64, du * w64
+
+
+def full_read_bwd(V, n_src, w, gamma, eps, dz):
+    """Gradients of the Full read over V[0 .. n_src) (see ``read_bwd``)."""
+    return read_bwd(_slices(V, n_src), w, gamma, eps, dz)
 
 
 def _slices(V, n):

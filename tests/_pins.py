@@ -304,11 +304,80 @@ def pin_prenorm_of_zero_query_read(orc):
     _close(out[0], np.array([0.25, 2.0]), 1e-9, "pre-norm of the mean")
 
 
+# ----------------------------------------------------------------- backward ----
+
+def _fd_case(seed, n, T, d, eps):
+    rng = _rng(seed)
+    V = rng.normal(size=(n, T, d)) * np.arange(1, n + 1).reshape(n, 1, 1) ** 0.5
+    w = rng.normal(size=d)
+    gamma = 1 + 0.3 * rng.normal(size=d)
+    dz = rng.normal(size=(T, d))
+    return V, w, gamma, dz, eps
+
+
+def pin_bwd_finite_differences(orc):
+    """Gradients against central differences of the forward read (which is the
+    C oracle, a separate implementation): L = sum(dz * z), step 1e-6, fp64."""
+    V, w, gamma, dz, eps = _fd_case(51, 3, 2, 5, 0.1)
+    dV, dw, dg = orc.read_bwd(list(V), w, gamma, eps, dz)
+    h = 1e-6
+
+    def loss(V_, w_, g_):
+        z, _ = orc.read(list(V_), w_, g_, eps)
+        return float(np.sum(z * dz))
+
+    fd = np.zeros_like(V)
+    for idx in np.ndindex(V.shape):
+        vp, vm = V.copy(), V.copy()
+        vp[idx] += h
+        vm[idx] -= h
+        fd[idx] = (loss(vp, w, gamma) - loss(vm, w, gamma)) / (2 * h)
+    _close(dV, fd, 1e-7, "dV vs finite differences")
+    eye = np.eye(V.shape[-1])
+    fw = np.array([(loss(V, w + h * e, gamma) - loss(V, w - h * e, gamma)) / (2 * h) for e in eye])
+    fg = np.array([(loss(V, w, gamma + h * e) - loss(V, w, gamma - h * e)) / (2 * h) for e in eye])
+    _close(dw, fw, 1e-7, "dw vs finite differences")
+    _close(dg, fg, 1e-7, "dgamma vs finite differences")
+
+
+def pin_bwd_single_source(orc):
+    """One source: z = v_0 whatever the score, so dv_0 = dz and dw = dgamma = 0."""
+    V, w, gamma, dz, eps = _fd_case(52, 1, 3, 6, 1e-6)
+    dV, dw, dg = orc.read_bwd(list(V), w, gamma, eps, dz)
+    _close(dV[0], dz, 1e-14, "single-source dV")
+    _close(dw, np.zeros(6), 1e-14, "single-source dw")
+    _close(dg, np.zeros(6), 1e-14, "single-source dgamma")
+
+
+def pin_bwd_equal_sources(orc):
+    """n equal sources: the weights are 1/n and every dL/da_i is the same, so the
+    score gradients vanish: dv_i = dz / n and dw = dgamma = 0."""
+    V, w, gamma, dz, eps = _fd_case(53, 1, 2, 5, 1e-6)
+    n = 4
+    dV, dw, dg = orc.read_bwd([V[0]] * n, w, gamma, eps, dz)
+    for i in range(n):
+        _close(dV[i], dz / n, 1e-14, f"equal sources dV[{i}]")
+    _close(dw, np.zeros(5), 1e-13, "equal sources dw")
+    _close(dg, np.zeros(5), 1e-13, "equal sources dgamma")
+
+
+def pin_bwd_permutation(orc):
+    """Permuting the sources permutes dV and leaves dw and dgamma unchanged."""
+    V, w, gamma, dz, eps = _fd_case(54, 4, 3, 5, 1e-3)
+    dV, dw, dg = orc.read_bwd(list(V), w, gamma, eps, dz)
+    perm = [2, 0, 3, 1]
+    pV, pw, pg = orc.read_bwd([V[i] for i in perm], w, gamma, eps, dz)
+    _close(pV, dV[perm], 1e-12, "permuted dV")
+    _close(pw, dw, 1e-12, "permuted dw")
+    _close(pg, dg, 1e-12, "permuted dgamma")
+
+
 ALL_PINS = [
     pin_golden, pin_bf16_widening, pin_zero_query_is_mean, pin_single_source_identity,
     pin_two_sources_logistic, pin_equal_sources, pin_hardmax_limit,
     pin_permutation_invariance, pin_key_scale_invariance, pin_split_merge,
     pin_block_s1_equals_full, pin_block_zero_query_means, pin_stage1_and_merge_reference,
     pin_bruteforce, pin_prenorm_constant_row, pin_prenorm_unit_rms,
-    pin_prenorm_scale_invariance, pin_prenorm_of_zero_query_read,
+    pin_prenorm_scale_invariance, pin_prenorm_of_zero_query_read, pin_bwd_finite_differences,
+    pin_bwd_single_source, pin_bwd_equal_sources, pin_bwd_permutation,
 ]

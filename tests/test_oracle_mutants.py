@@ -112,3 +112,50 @@ def _prenorm_mutant(kind):
 def test_prenorm_mutant_is_caught(kind, monkeypatch, oracle_mod):
     monkeypatch.setattr(oracle, "prenorm", _prenorm_mutant(kind))
     assert _run_pins(oracle), f"pre-norm mutant {kind} passed every pin"
+
+
+def _bwd_mutant(kind):
+    real = oracle.read_bwd
+
+    def read_bwd(sources, w, gamma, eps, dz):
+        V = np.stack([np.asarray(s, np.float64) if isinstance(s, np.ndarray) else oracle.widen(s)
+                      for s in sources])
+        g = np.asarray(dz, np.float64) if isinstance(dz, np.ndarray) else oracle.widen(dz)
+        d = V.shape[-1]
+        w64 = np.asarray(w, np.float64).reshape(d)
+        g64 = np.asarray(gamma, np.float64).reshape(d)
+        u = w64 * g64
+        r = 1.0 / np.sqrt(np.mean(V * V, axis=-1) + eps)
+        e = r * np.einsum("ntk,k->nt", V, u)
+        a = np.exp(e - e.max(axis=0, keepdims=True))
+        a /= a.sum(axis=0, keepdims=True)
+        da = np.einsum("ntk,tk->nt", V, g)
+        de = a * (da - np.sum(a * da, axis=0, keepdims=True))
+        if kind == "score_grad_sign":
+            de = -de
+        rms_term = (e * r * r / d)[..., None] * V
+        if kind == "no_rms_derivative":
+            rms_term = 0.0 * V
+        if kind == "rms_derivative_r_cubed":
+            rms_term = (e * r * r * r / d)[..., None] * V
+        value_term = a[..., None] * g[None]
+        if kind == "no_value_path":
+            value_term = 0.0 * V
+        dV = value_term + de[..., None] * (r[..., None] * u - rms_term)
+        du = np.einsum("nt,ntk->k", de * r, V)
+        if kind == "du_from_weights":
+            du = np.einsum("nt,ntk->k", a * r, V)
+        if kind == "dw_without_gain":
+            return dV, du, du * w64
+        if kind == "gains_swapped":
+            return dV, du * w64, du * g64
+        raise ValueError(kind)
+    del real
+    return read_bwd
+
+
+@pytest.mark.parametrize("kind", ["score_grad_sign", "no_rms_derivative", "rms_derivative_r_cubed",
+                                  "no_value_path", "du_from_weights", "dw_without_gain", "gains_swapped"])
+def test_bwd_mutant_is_caught(kind, monkeypatch, oracle_mod):
+    monkeypatch.setattr(oracle, "read_bwd", _bwd_mutant(kind))
+    assert _run_pins(oracle), f"backward mutant {kind} passed every pin"
