@@ -211,17 +211,31 @@ class FullPassStep:
         self.out = torch.empty(wl.R, wl.T, wl.d, device=dev, dtype=dt)
         es = 2 if wl.dtype == "bf16" else 4
         self.bytes = full_pass_bytes(wl.R, wl.T, wl.d, es)
-        if op != "read":
+        if op in ("prenorm", "prenorm_both"):
             g = inputs.generator(wl.seed + 1, dev)
             self.Gpre = 1 + 0.1 * inputs.queries(wl.R, wl.d, 1.0, g, dev)
             self.normed = torch.empty(wl.R, wl.T, wl.d, device=dev, dtype=dt)
             if op == "prenorm_both":
                 self.bytes += wl.R * wl.T * wl.d * es
+        if op == "bwd":
+            # The pass backward: reads in reverse order, each adding its share
+            # into fp32 dV (read-modify-write), dW and dGamma.
+            g = inputs.generator(wl.seed + 2, dev)
+            self.dZ = inputs.randn((wl.R, wl.T, wl.d), wl.dtype, g, dev)
+            self.dV = torch.zeros(wl.R, wl.T, wl.d, device=dev)
+            self.dW = torch.zeros(wl.R, wl.d, device=dev)
+            self.dG = torch.zeros(wl.R, wl.d, device=dev)
+            E = wl.T * wl.d
+            self.bytes = sum((r + 1) * E * (es + 8) + E * es for r in range(wl.R))
         self.launches = wl.R
 
     def __call__(self):
         if self.op == "read":
             self.ar.attnres_full_pass(self.V, self.W, self.G, self.wl.eps, self.out)
+        elif self.op == "bwd":
+            for r in reversed(range(self.wl.R)):
+                self.ar.attnres_full_bwd(self.V, r + 1, self.W[r], self.G[r], self.wl.eps, self.dZ[r], self.dV,
+                                         self.dW[r], self.dG[r])
         else:
             self.ar.attnres_full_pass_prenorm(self.V, self.W, self.G, self.wl.eps, self.Gpre, self.wl.eps,
                                               self.out if self.op == "prenorm_both" else None, self.normed)
@@ -495,10 +509,12 @@ def ours(args):
     torch.cuda.synchronize()
 
     if wl.kind == "full_pass":
-        digest = kernel_digest("full_fwd.cu")
-        traffic = NCU_TRAFFIC.get(("full_fwd_bulk_kernel", digest))
+        kname, kfile = (("full_bwd_bulk_kernel", "full_bwd.cu") if args.op == "bwd"
+                        else ("full_fwd_bulk_kernel", "full_fwd.cu"))
+        digest = kernel_digest(kfile)
+        traffic = NCU_TRAFFIC.get((kname, digest))
         line["roofline"] = {
-            "kernel": "full_fwd_bulk_kernel", "bound": "hbm", "achieved": gbs,
+            "kernel": kname, "bound": "hbm", "achieved": gbs,
             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
             "frac_of_nominal_8000": gbs / NOMINAL_HBM_GBS,
             "peak_source": peaks["source"],
@@ -587,9 +603,9 @@ def main():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(
         n for n, w in inputs.WORKLOADS.items() if w.kind != "full_read"))
-    p.add_argument("--op", choices=["read", "prenorm", "prenorm_both"], default="read",
+    p.add_argument("--op", choices=["read", "prenorm", "prenorm_both", "bwd"], default="read",
                    help="Full pass only: plain reads, reads emitting the sublayer pre-norm instead of "
-                        "their result, or both")
+                        "their result, or both, or the pass backward (dV, dW, dGamma)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-block", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")

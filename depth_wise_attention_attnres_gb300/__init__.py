@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     attnres_block_stage1,
     attnres_block_summary_accumulate,
     attnres_device_status,
+    attnres_full_bwd,
     attnres_full_fwd,
     attnres_full_fwd_prenorm,
     attnres_full_pass,

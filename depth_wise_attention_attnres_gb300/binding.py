@@ -33,6 +33,8 @@ _SIGNATURES = {
     "attnres_full_pass_prenorm": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _F, _VP,
                                   _VP, _I64, _I32, _VP],
     "attnres_rmsnorm": [_VP, _I64, _I32, _I32, _VP, _F, _VP, _VP],
+    "attnres_full_bwd": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _I32, _VP, _I64, _VP, _VP,
+                         _VP],
     "attnres_block_stage1": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _I32, _F,
                              ctypes.POINTER(_VP), _VP, _VP],
     "attnres_block_merge": [_VP, _VP, _VP, _VP, _I32, _VP, _VP, _F, _I64, _I32, _I32, _VP, _VP],
@@ -199,6 +201,26 @@ def attnres_full_pass_prenorm(V: torch.Tensor, W: torch.Tensor, Gamma: torch.Ten
         _ptr(V), stride, R, T, d, _dtype(V), _ptr(W), _ptr(Gamma), eps, _ptr(Gamma_pre), eps_pre,
         _ptr(out), _ptr(out_normed), ostride, _dtype(out_normed), _stream(stream)))
     return out_normed
+
+
+def attnres_full_bwd(V: torch.Tensor, n_src: int, w: torch.Tensor, gamma: torch.Tensor, eps: float,
+                     dz: torch.Tensor, dV: torch.Tensor, dw: torch.Tensor | None = None,
+                     dgamma: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Backward of the read over V[0 .. n_src): ADD dL/dV (fp32 [n, T, d]) into dV
+    and dL/dw, dL/dgamma (fp32 [d]) into dw, dgamma, given dz = dL/dz [T, d]."""
+    _, T, d, stride = _slices(V)
+    dn, dT, dd, dstride = _slices(dV)
+    if (dT, dd) != (T, d) or dn < n_src or dV.dtype != torch.float32:
+        raise ValueError("dV must be fp32 [n_src, T, d]")
+    if _rows(dz) != (T, d):
+        raise ValueError("dz must be [T, d]")
+    for t in (dw, dgamma):
+        if t is not None and (t.dtype != torch.float32 or t.numel() != d):
+            raise ValueError("dw and dgamma must be fp32 [d]")
+    _check("attnres_full_bwd", lib().attnres_full_bwd(
+        _ptr(V), stride, n_src, T, d, _dtype(V), _ptr(w), _ptr(gamma), eps, _ptr(dz), _dtype(dz),
+        _ptr(dV), dstride, _ptr(dw), _ptr(dgamma), _stream(stream)))
+    return dV
 
 
 def attnres_rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float, out: torch.Tensor,

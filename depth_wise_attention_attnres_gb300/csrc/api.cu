@@ -359,6 +359,34 @@ int attnres_rmsnorm(const void* x, int64_t T, int32_t d, int32_t dtype, const fl
   return status_of(launch_rmsnorm(x, T, d, dtype == ATTNRES_BF16, gamma, eps, out, as_stream(stream)));
 }
 
+int attnres_full_bwd(const void* V, int64_t src_stride, int32_t n_src, int64_t T, int32_t d,
+                     int32_t v_dtype, const float* w, const float* gamma, float eps, const void* dz,
+                     int32_t dz_dtype, float* dV, int64_t dv_stride, float* dw, float* dgamma,
+                     void* stream) {
+  if (n_src < 1 || d < 1 || T < 0 || !valid_dtype(v_dtype) || !valid_dtype(dz_dtype) || !valid_eps(eps))
+    return ATTNRES_ERR_INVALID_ARG;
+  if (T == 0) return ATTNRES_OK;
+  if (!V || !w || !gamma || !dz || !dV) return ATTNRES_ERR_INVALID_ARG;
+  const int64_t E = T * d;
+  if (n_src > 1 && (src_stride < E || dv_stride < E)) return ATTNRES_ERR_INVALID_ARG;
+  const int64_t sstr = n_src > 1 ? src_stride : 0, dstr = n_src > 1 ? dv_stride : 0;
+  const Range rv = range_of(V, ((n_src - 1) * sstr + E) * elem_size(v_dtype));
+  const Range rz = range_of(dz, E * elem_size(dz_dtype));
+  const Range rd = range_of(dV, ((n_src - 1) * dstr + E) * 4);
+  const Range rw = dw ? range_of(dw, static_cast<int64_t>(d) * 4) : Range{};
+  const Range rg = dgamma ? range_of(dgamma, static_cast<int64_t>(d) * 4) : Range{};
+  const Range rq = range_of(w, static_cast<int64_t>(d) * 4), rk = range_of(gamma, static_cast<int64_t>(d) * 4);
+  if (overlap(rd, rv) || overlap(rd, rz) || overlap(rd, rw) || overlap(rd, rg) || overlap(rd, rq) ||
+      overlap(rd, rk) || overlap(rw, rg) || overlap(rw, rv) || overlap(rg, rv) || overlap(rw, rz) ||
+      overlap(rg, rz) || overlap(rw, rq) || overlap(rw, rk) || overlap(rg, rq) || overlap(rg, rk))
+    return ATTNRES_ERR_INVALID_ARG;
+  const BwdArgs a{V, sstr, n_src, T, d, v_dtype == ATTNRES_BF16, w, gamma, eps, dz, dz_dtype == ATTNRES_BF16,
+                  dV, dstr, dw, dgamma};
+  const bool fast = full_bwd_fast_ok(a);
+  if (!fast && d > kMaxBwdGenericD) return ATTNRES_ERR_UNSUPPORTED;
+  return status_of(launch_full_bwd(a, as_stream(stream), fast));
+}
+
 int attnres_block_stage1(const void* Src, int64_t src_stride, int32_t n_src, int64_t T, int32_t d,
                          int32_t dtype, const float* W, const float* Gamma, int32_t S, float eps,
                          void* const* O, float* lse, void* stream) {
@@ -470,13 +498,14 @@ int attnres_device_status(void* stream) {
     cudaGetLastError();
     return ATTNRES_ERR_CUDA;
   }
-  unsigned int f1 = 0, f2 = 0, f3 = 0, f4 = 0;
+  unsigned int f1 = 0, f2 = 0, f3 = 0, f4 = 0, f5 = 0;
   if (take_timeout_full(&f1) != cudaSuccess || take_timeout_stage1(&f2) != cudaSuccess ||
-      take_timeout_merge(&f3) != cudaSuccess || take_timeout_stage1tc(&f4) != cudaSuccess) {
+      take_timeout_merge(&f3) != cudaSuccess || take_timeout_stage1tc(&f4) != cudaSuccess ||
+      take_timeout_bwd(&f5) != cudaSuccess) {
     cudaGetLastError();
     return ATTNRES_ERR_CUDA;
   }
-  if (f1 || f2 || f3 || f4) return ATTNRES_ERR_TIMEOUT;
+  if (f1 || f2 || f3 || f4 || f5) return ATTNRES_ERR_TIMEOUT;
   e = cudaGetLastError();
   return e == cudaSuccess ? ATTNRES_OK : ATTNRES_ERR_CUDA;
 }

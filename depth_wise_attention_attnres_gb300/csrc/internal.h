@@ -74,6 +74,27 @@ struct MergeArgs {
   PreNorm pre;
 };
 
+// Backward of one read (full_bwd.cu): dV, dw, dgamma accumulated in fp32.
+struct BwdArgs {
+  const void* V;
+  int64_t src_stride;   // elements
+  int n_src;
+  int64_t T;
+  int d;
+  int v_bf16;
+  const float* w;
+  const float* gamma;
+  float eps;
+  const void* dz;       // dL/dz [T, d]
+  int dz_bf16;
+  float* dV;            // [n_src, T, d] fp32, += ; sources dv_stride elements apart
+  int64_t dv_stride;
+  float* dw;            // [d] fp32, += ; may be nullptr
+  float* dgamma;        // [d] fp32, += ; may be nullptr
+};
+constexpr int kMaxBwdFastSources = 256;   // per-(row, source) scalars live in shared memory
+constexpr int kMaxBwdGenericD = 16384;    // du of a CTA lives in shared memory
+
 struct AccumArgs {
   float* P;
   const void* f;
@@ -102,6 +123,9 @@ cudaError_t launch_accum(const AccumArgs& a, cudaStream_t s, bool fast);
 cudaError_t launch_rmsnorm(const void* x, int64_t T, int d, int is_bf16, const float* gamma, float eps, void* out,
                            cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(cudaStream_t s);
+bool full_bwd_fast_ok(const BwdArgs& a);
+cudaError_t launch_full_bwd(const BwdArgs& a, cudaStream_t s, bool fast);
+cudaError_t take_timeout_bwd(unsigned int* flag);
 
 // Device-side timeout records of each kernel file: read and clear (blocking).
 cudaError_t take_timeout_full(unsigned int* flag);

@@ -150,6 +150,35 @@ int attnres_rmsnorm(const void* x, int64_t T, int32_t d, int32_t dtype, const fl
                     float eps, void* out, void* stream);
 
 /*
+ * attnres_full_bwd - backward of one read over V[0 .. n_src): given
+ * dz = dL/dz of its result, ADD the gradients with respect to the sources,
+ * the query and the key-norm gain into dV, dw and dgamma. The read is
+ * e_i = r_i (u . v_i), u = w * gamma, r_i = 1 / sqrt(mean_k v_ik^2 + eps),
+ * a = softmax_i(e), z = sum_i a_i v_i (DepthBench reading notes section 2.3);
+ * by the chain rule, per token:
+ *   dL/da_i = dz . v_i,  dL/de_i = a_i (dL/da_i - sum_j a_j dL/da_j),
+ *   dL/dv_i = a_i dz + dL/de_i (r_i u - e_i r_i^2 v_i / d),
+ *   dL/du = sum over tokens and i of dL/de_i r_i v_i, dw = dL/du * gamma,
+ *   dgamma = dL/du * w.
+ * Accumulation (+=) lets a model's backward add every later read's share to
+ * a source's gradient; zero the buffers before the first call.
+ *
+ *   V, src_stride, n_src, T, d, v_dtype, w, gamma, eps   as attnres_full_fwd.
+ *   dz         device, [T, d] of dz_dtype.
+ *   dV         device, fp32, n_src slices [T, d] dv_stride elements apart
+ *              (>= T*d when n_src > 1); added to with atomic adds.
+ *   dw, dgamma device, fp32 [d], added to; either may be NULL (skipped).
+ * None of dV, dw, dgamma may overlap each other or an input. Returns
+ * ATTNRES_ERR_UNSUPPORTED for shapes no kernel covers (d > 16384 off the
+ * fast path). Results depend on the order of atomic additions only within
+ * fp32 rounding.
+ */
+int attnres_full_bwd(const void* V, int64_t src_stride, int32_t n_src, int64_t T, int32_t d,
+                     int32_t v_dtype, const float* w, const float* gamma, float eps,
+                     const void* dz, int32_t dz_dtype, float* dV, int64_t dv_stride, float* dw,
+                     float* dgamma, void* stream);
+
+/*
  * attnres_block_stage1 - stage 1 of the two-stage Block AttnRes computation
  * (datacamp explainer, "two-stage computation"): the S pseudo-queries of one
  * block against the cross-block sources, each source row read once for all S.

@@ -97,6 +97,24 @@ def test_prenorm_entry_validation(lib):
     assert lib.attnres_rmsnorm(P, 0, 16, 1, P, 1e-6, P, None) == 0
 
 
+def test_full_bwd_validation(lib):
+    # (V, stride, n, T, d, dtype, w, gamma, eps, dz, dz_dtype, dV, dv_stride, dw, dgamma)
+    ok = (P, 64, 2, 4, 16, 1, P, P, 1e-6, 2 * P, 1, 8 * P, 64, 16 * P, 17 * P)
+    bad = [
+        ok[:2] + (0,) + ok[3:],                          # n_src = 0
+        ok[:11] + (None,) + ok[12:],                     # no dV
+        ok[:11] + (P + 64,) + ok[12:],                   # dV overlaps V
+        ok[:11] + (2 * P,) + ok[12:],                    # dV overlaps dz
+        ok[:13] + (8 * P + 64,) + ok[14:],               # dw overlaps dV
+        ok[:14] + (16 * P + 32,),                        # dgamma overlaps dw
+        ok[:10] + (9,) + ok[11:],                        # bad dz dtype
+        ok[:12] + (63,) + ok[13:],                       # dv_stride < T*d
+    ]
+    for args in bad:
+        assert lib.attnres_full_bwd(*args, None) == INVALID, args
+    assert lib.attnres_full_bwd(*(ok[:3] + (0,) + ok[4:]), None) == 0  # T = 0
+
+
 def test_kernel_selection(lib):
     A = 1 << 20
     # Full read: d multiple of 128 and 16-byte alignment -> fast kernel.
