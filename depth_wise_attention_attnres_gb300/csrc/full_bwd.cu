@@ -13,8 +13,8 @@
 // full_bwd_bulk_kernel: the Full-read pipeline run twice per tile of 8 token
 // rows (one consumer warp per row). A producer warp streams every (tile,
 // source) block with one bulk copy, first for pass A and again for pass B (the
-// second copy of a block mostly hits L2: a CTA's 8 rows of all sources are a
-// few hundred KB). Pass A forms Sigma v^2, u . v and dz . v per source with
+// second pass takes the sources in reverse order, so its first blocks are
+// the ones still in L2). Pass A forms Sigma v^2, u . v and dz . v per source with
 // packed FMAs and warp sums and keeps e_i, dz . v_i and r_i in shared memory
 // while an online softmax gathers the max, the mass and sum_i a_i dL/da_i.
 // The per-source coefficients then turn dv_i into A_i dz + B_i u + C_i v_i
@@ -133,7 +133,10 @@ __global__ void __launch_bounds__(kBThreads, BwdTraits<CH>::kMinBlocks)
         break;
       }
       const int tile = static_cast<int>(it / (2 * n));
-      const int src = static_cast<int>((it - static_cast<int64_t>(tile) * 2 * n) % n);
+      // Pass A in source order, pass B in reverse (its first blocks are the
+      // ones pass A brought in last, the likeliest still in L2).
+      const int j = static_cast<int>(it - static_cast<int64_t>(tile) * 2 * n);
+      const int src = j < n ? j : 2 * n - 1 - j;
       const int64_t row0 = r0 + static_cast<int64_t>(tile) * R / ntiles;
       const int rows = static_cast<int>(r0 + static_cast<int64_t>(tile + 1) * R / ntiles - row0);
       const uint32_t bytes = static_cast<uint32_t>(rows) * D * sizeof(Tin);
@@ -260,8 +263,8 @@ __global__ void __launch_bounds__(kBThreads, BwdTraits<CH>::kMinBlocks)
       __syncwarp();
     }
 
-    // Pass B: dv_i into dV, du into registers.
-    for (int src = 0; src < n && ok; ++src) {
+    // Pass B (sources in reverse): dv_i into dV, du into registers.
+    for (int src = n - 1; src >= 0 && ok; --src) {
       if (!mbar_wait(smem_u32(&full_bar[stage]), phase)) {
         ok = false;
         break;
