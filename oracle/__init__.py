@@ -25,6 +25,11 @@ This module adds the sequencing the pages describe on top of it:
   the result, by the chain rule through the read's definition (the
   backward the pages point to when they note that stored sublayer outputs
   are reused for it; DepthBench reading notes section 2.3 for the read).
+* ``query_projection`` / ``read_dynamic_query``: the input-dependent query
+  the pages report as an ablation (LLMRes blog, on the paper's ablation: a
+  query projected from the current hidden state by a per-layer d x d matrix
+  instead of the fixed learned pseudo-query): q(t) = W_q h(t) per token, and
+  the read scored with that per-token query.
 * ``prenorm``: the consuming sublayer's pre-norm of an aggregated row,
   RMSNorm_pre(z) (DepthBench reading notes section 2.3: f_l =
   F_l(RMSNorm_pre,l(z_l))), which the library can emit next to z.
@@ -186,6 +191,31 @@ def read(sources, w, gamma, eps, rows=None):
     if rc != 0:
         raise ValueError(f"attnres_oracle_read failed with code {rc}")
     return out, lse
+
+
+def query_projection(H, Wq):
+    """Per-token query q(t) = Wq h(t): fp64 [T, d_out] from H [T, d_in] and Wq
+    [d_out, d_in] (stored or fp64)."""
+    h = np.asarray(H, np.float64) if isinstance(H, np.ndarray) else widen(H)
+    w = np.asarray(Wq, np.float64) if isinstance(Wq, np.ndarray) else widen(Wq)
+    return h @ w.T
+
+
+def read_dynamic_query(sources, Q, gamma, eps):
+    """A read whose query differs per token: e_i(t) = Q(t) . (gamma * v_i(t)) *
+    r_i(t), a(t) = softmax_i(e(t)), z(t) = sum_i a_i(t) v_i(t). Q is [T, d].
+    Returns (z fp64 [T, d], lse fp64 [T])."""
+    V = np.stack([widen(s) if not isinstance(s, np.ndarray) else np.asarray(s, np.float64)
+                  for s in sources])                      # [n, T, d]
+    q = np.asarray(Q, np.float64) if isinstance(Q, np.ndarray) else widen(Q)
+    g = np.asarray(gamma, np.float64).reshape(-1)
+    r = 1.0 / np.sqrt(np.mean(V * V, axis=-1) + eps)      # [n, T]
+    e = r * np.einsum("ntk,tk->nt", V, q * g)
+    m = e.max(axis=0)
+    p = np.exp(e - m)
+    z = p.sum(axis=0)
+    out = np.einsum("nt,ntk->tk", p / z, V)
+    return out, m + np.log(z)
 
 
 def read_bwd(sources, w, gamma, eps, dz):

@@ -304,6 +304,50 @@ def pin_prenorm_of_zero_query_read(orc):
     _close(out[0], np.array([0.25, 2.0]), 1e-9, "pre-norm of the mean")
 
 
+# ------------------------------------------------------ input-dependent query ----
+
+def pin_dynamic_query_constant_rows(orc):
+    """Every token's query equal to one w: the read equals the fixed-query read
+    of the C oracle (a separate implementation), outputs and lse."""
+    rng = _rng(61)
+    n, T, d = 4, 5, 6
+    V = rng.normal(size=(n, T, d)) * np.arange(1, n + 1).reshape(n, 1, 1)
+    w = rng.normal(size=d)
+    gamma = 1 + 0.3 * rng.normal(size=d)
+    z, lse = orc.read_dynamic_query(list(V), np.tile(w, (T, 1)), gamma, 1e-3)
+    rz, rl = orc.read(list(V), w, gamma, 1e-3)
+    _close(z, rz, 1e-12, "constant-row query vs fixed query")
+    _close(lse, rl, 1e-12, "constant-row query lse")
+
+
+def pin_dynamic_query_per_token(orc):
+    """Each token's result equals the fixed-query read with that token's query
+    (token by token through the C oracle), and a zero query gives the mean."""
+    rng = _rng(62)
+    n, T, d = 3, 4, 5
+    V = rng.normal(size=(n, T, d))
+    Q = rng.normal(size=(T, d)) * 2.0
+    gamma = 1 + 0.3 * rng.normal(size=d)
+    z, _ = orc.read_dynamic_query(list(V), Q, gamma, 1e-6)
+    for t in range(T):
+        rz, _ = orc.read([V[i, t:t + 1] for i in range(n)], Q[t], gamma, 1e-6)
+        _close(z[t], rz[0], 1e-12, f"token {t} with its own query")
+    z0, _ = orc.read_dynamic_query(list(V), np.zeros((T, d)), gamma, 1e-6)
+    _close(z0, V.mean(axis=0), 1e-14, "zero query is the mean")
+
+
+def pin_query_projection(orc):
+    """q = Wq h: the identity returns h, a permutation permutes its features,
+    and a hand case: h = (1, 2), Wq = [[1, 1], [3, -1]] gives (3, 1)."""
+    rng = _rng(63)
+    H = rng.normal(size=(3, 4))
+    _close(orc.query_projection(H, np.eye(4)), H, 0.0, "identity projection")
+    P = np.eye(4)[[2, 0, 3, 1]]
+    _close(orc.query_projection(H, P), H[:, [2, 0, 3, 1]], 0.0, "permutation projection")
+    _close(orc.query_projection(np.array([[1.0, 2.0]]), np.array([[1.0, 1.0], [3.0, -1.0]])),
+           np.array([[3.0, 1.0]]), 0.0, "hand-worked projection")
+
+
 # ----------------------------------------------------------------- backward ----
 
 def _fd_case(seed, n, T, d, eps):
@@ -380,4 +424,5 @@ ALL_PINS = [
     pin_bruteforce, pin_prenorm_constant_row, pin_prenorm_unit_rms,
     pin_prenorm_scale_invariance, pin_prenorm_of_zero_query_read, pin_bwd_finite_differences,
     pin_bwd_single_source, pin_bwd_equal_sources, pin_bwd_permutation,
+    pin_dynamic_query_constant_rows, pin_dynamic_query_per_token, pin_query_projection,
 ]

@@ -159,3 +159,44 @@ def _bwd_mutant(kind):
 def test_bwd_mutant_is_caught(kind, monkeypatch, oracle_mod):
     monkeypatch.setattr(oracle, "read_bwd", _bwd_mutant(kind))
     assert _run_pins(oracle), f"backward mutant {kind} passed every pin"
+
+
+def _dynq_mutant(kind):
+    def read_dynamic_query(sources, Q, gamma, eps):
+        V = np.stack([np.asarray(s, np.float64) if isinstance(s, np.ndarray) else oracle.widen(s)
+                      for s in sources])
+        q = np.asarray(Q, np.float64)
+        g = np.asarray(gamma, np.float64).reshape(-1)
+        r = 1.0 / np.sqrt(np.mean(V * V, axis=-1) + eps)
+        if kind == "query_of_token_0":
+            q = np.repeat(q[:1], q.shape[0], axis=0)
+        if kind == "no_gain":
+            g = np.ones_like(g)
+        if kind == "query_transposed_tokens":
+            q = q[::-1]
+        e = r * np.einsum("ntk,tk->nt", V, q * g)
+        m = e.max(axis=0)
+        p = np.exp(e - m)
+        z = p.sum(axis=0)
+        return np.einsum("nt,ntk->tk", p / z, V), m + np.log(z)
+    return read_dynamic_query
+
+
+def _proj_mutant(kind):
+    def query_projection(H, Wq):
+        h = np.asarray(H, np.float64)
+        w = np.asarray(Wq, np.float64)
+        return h @ w if kind == "not_transposed" else (h @ w.T) * (0.5 if kind == "half" else 1.0)
+    return query_projection
+
+
+@pytest.mark.parametrize("kind", ["query_of_token_0", "no_gain", "query_transposed_tokens"])
+def test_dynamic_query_mutant_is_caught(kind, monkeypatch, oracle_mod):
+    monkeypatch.setattr(oracle, "read_dynamic_query", _dynq_mutant(kind))
+    assert _run_pins(oracle), f"dynamic-query mutant {kind} passed every pin"
+
+
+@pytest.mark.parametrize("kind", ["not_transposed", "half"])
+def test_projection_mutant_is_caught(kind, monkeypatch, oracle_mod):
+    monkeypatch.setattr(oracle, "query_projection", _proj_mutant(kind))
+    assert _run_pins(oracle), f"projection mutant {kind} passed every pin"
