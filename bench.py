@@ -217,6 +217,16 @@ class FullPassStep:
             self.normed = torch.empty(wl.R, wl.T, wl.d, device=dev, dtype=dt)
             if op == "prenorm_both":
                 self.bytes += wl.R * wl.T * wl.d * es
+        if op == "dynq":
+            # Input-dependent query: read r's query projected from its newest
+            # source V[r] by its own Wq[r] (tensor-core GEMM), then the read.
+            g = inputs.generator(wl.seed + 3, dev)
+            self.Wq = (inputs.randn((wl.R, wl.d, wl.d), "f32", g, dev) / wl.d ** 0.5).to(torch.bfloat16)
+            self.Q = torch.empty(wl.T, wl.d, device=dev)
+            E = wl.T * wl.d
+            # per read: the GEMM reads V[r] and Wq[r] and writes Q; the read adds Q
+            self.bytes += sum(E * es + wl.d * wl.d * 2 + E * 4 + E * 4 for _ in range(wl.R))
+            self.flops = 2 * wl.T * wl.d * wl.d * wl.R
         if op == "bwd":
             # The pass backward: reads in reverse order, each adding its share
             # into fp32 dV (read-modify-write), dW and dGamma.
@@ -227,11 +237,15 @@ class FullPassStep:
             self.dG = torch.zeros(wl.R, wl.d, device=dev)
             E = wl.T * wl.d
             self.bytes = sum((r + 1) * E * (es + 8) + E * es for r in range(wl.R))
-        self.launches = wl.R
+        self.launches = wl.R * (2 if op == "dynq" else 1)
 
     def __call__(self):
         if self.op == "read":
             self.ar.attnres_full_pass(self.V, self.W, self.G, self.wl.eps, self.out)
+        elif self.op == "dynq":
+            for r in range(self.wl.R):
+                self.ar.attnres_query_projection(self.V[r], self.Wq[r], self.Q)
+                self.ar.attnres_full_fwd_dynq(self.V, r + 1, self.Q, self.G[r], self.wl.eps, self.out[r])
         elif self.op == "bwd":
             for r in reversed(range(self.wl.R)):
                 self.ar.attnres_full_bwd(self.V, r + 1, self.W[r], self.G[r], self.wl.eps, self.dZ[r], self.dV,
@@ -603,9 +617,10 @@ def main():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(
         n for n, w in inputs.WORKLOADS.items() if w.kind != "full_read"))
-    p.add_argument("--op", choices=["read", "prenorm", "prenorm_both", "bwd"], default="read",
+    p.add_argument("--op", choices=["read", "prenorm", "prenorm_both", "bwd", "dynq"], default="read",
                    help="Full pass only: plain reads, reads emitting the sublayer pre-norm instead of "
-                        "their result, or both, or the pass backward (dV, dW, dGamma)")
+                        "their result, or both, the pass backward (dV, dW, dGamma), or reads with "
+                        "input-dependent queries (projection + read)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-block", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")

@@ -15,10 +15,12 @@ from .binding import (  # noqa: F401
     attnres_device_status,
     attnres_full_bwd,
     attnres_full_fwd,
+    attnres_full_fwd_dynq,
     attnres_full_fwd_prenorm,
     attnres_full_pass,
     attnres_full_pass_prenorm,
     attnres_kernel_path,
+    attnres_query_projection,
     attnres_rmsnorm,
     attnres_status_string,
     lib,

@@ -33,6 +33,8 @@ _SIGNATURES = {
     "attnres_full_pass_prenorm": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _F, _VP,
                                   _VP, _I64, _I32, _VP],
     "attnres_rmsnorm": [_VP, _I64, _I32, _I32, _VP, _F, _VP, _VP],
+    "attnres_query_projection": [_VP, _I64, _I32, _I32, _VP, _VP, _VP],
+    "attnres_full_fwd_dynq": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _I32, _VP],
     "attnres_full_bwd": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _I32, _VP, _I64, _VP, _VP,
                          _VP],
     "attnres_block_stage1": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _I32, _F,
@@ -221,6 +223,30 @@ def attnres_full_bwd(V: torch.Tensor, n_src: int, w: torch.Tensor, gamma: torch.
         _ptr(V), stride, n_src, T, d, _dtype(V), _ptr(w), _ptr(gamma), eps, _ptr(dz), _dtype(dz),
         _ptr(dV), dstride, _ptr(dw), _ptr(dgamma), _stream(stream)))
     return dV
+
+
+def attnres_query_projection(H: torch.Tensor, Wq: torch.Tensor, Q: torch.Tensor, stream=None) -> torch.Tensor:
+    """Q = H Wq^T (H bf16 [T, d], Wq bf16 [d, d], Q fp32 [T, d]): the input-dependent query."""
+    T, d = _rows(H)
+    if tuple(Wq.shape) != (d, d) or Wq.dtype != torch.bfloat16 or not Wq.is_contiguous():
+        raise ValueError("Wq must be contiguous bf16 [d, d]")
+    if _rows(Q) != (T, d) or Q.dtype != torch.float32:
+        raise ValueError("Q must be fp32 [T, d]")
+    _check("attnres_query_projection", lib().attnres_query_projection(
+        _ptr(H), T, d, _dtype(H), _ptr(Wq), _ptr(Q), _stream(stream)))
+    return Q
+
+
+def attnres_full_fwd_dynq(V: torch.Tensor, n_src: int, Q: torch.Tensor, gamma: torch.Tensor, eps: float,
+                          out: torch.Tensor, stream=None) -> torch.Tensor:
+    """The Full read over V[0 .. n_src) with token t scored by its own query Q[t] (fp32 [T, d])."""
+    _, T, d, stride = _slices(V)
+    if _rows(out) != (T, d) or _rows(Q) != (T, d) or Q.dtype != torch.float32:
+        raise ValueError("out must be [T, d] and Q fp32 [T, d]")
+    _check("attnres_full_fwd_dynq", lib().attnres_full_fwd_dynq(
+        _ptr(V), stride, n_src, T, d, _dtype(V), _ptr(Q), _ptr(gamma), eps, _ptr(out), _dtype(out),
+        _stream(stream)))
+    return out
 
 
 def attnres_rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float, out: torch.Tensor,

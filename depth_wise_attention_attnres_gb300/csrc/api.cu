@@ -145,6 +145,7 @@ int run_full(const FullArgs& a, cudaStream_t s) {
   m.out[0] = a.out;
   m.lse = nullptr;
   m.pre = a.pre;
+  m.Q = a.Q;
   return status_of(launch_multi_generic(m, s));
 }
 
@@ -346,6 +347,33 @@ int attnres_full_pass_prenorm(const void* V, int64_t src_stride, int32_t R, int6
     if (st != ATTNRES_OK) return st;
   }
   return ATTNRES_OK;
+}
+
+int attnres_query_projection(const void* H, int64_t T, int32_t d, int32_t h_dtype, const void* Wq, float* Q,
+                             void* stream) {
+  if (d < 1 || T < 0 || !valid_dtype(h_dtype)) return ATTNRES_ERR_INVALID_ARG;
+  if (h_dtype != ATTNRES_BF16) return ATTNRES_ERR_UNSUPPORTED;
+  if (T == 0) return ATTNRES_OK;
+  if (!H || !Wq || !Q) return ATTNRES_ERR_INVALID_ARG;
+  const Range rq = range_of(Q, T * d * 4);
+  if (overlap(rq, range_of(H, T * d * 2)) || overlap(rq, range_of(Wq, static_cast<int64_t>(d) * d * 2)))
+    return ATTNRES_ERR_INVALID_ARG;
+  cudaStream_t s = as_stream(stream);
+  return status_of(proj_ok(H, Wq, Q, d) ? launch_proj(H, Wq, Q, T, d, s) : launch_proj_generic(H, Wq, Q, T, d, s));
+}
+
+int attnres_full_fwd_dynq(const void* V, int64_t src_stride, int32_t n_src, int64_t T, int32_t d, int32_t v_dtype,
+                          const float* Q, const float* gamma, float eps, void* out, int32_t out_dtype,
+                          void* stream) {
+  FullArgs a{};
+  // make_full checks the read; the shared query argument is unused here.
+  int st = make_full(V, src_stride, n_src, T, d, v_dtype, gamma, gamma, eps, out, out_dtype, &a);
+  if (st != ATTNRES_OK || T == 0) return st;
+  if (!Q) return ATTNRES_ERR_INVALID_ARG;
+  if (overlap(range_of(Q, T * d * 4), range_of(out, T * d * elem_size(out_dtype)))) return ATTNRES_ERR_INVALID_ARG;
+  a.w = nullptr;
+  a.Q = Q;
+  return run_full(a, as_stream(stream));
 }
 
 int attnres_rmsnorm(const void* x, int64_t T, int32_t d, int32_t dtype, const float* gamma, float eps, void* out,

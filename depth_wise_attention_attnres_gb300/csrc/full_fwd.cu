@@ -43,11 +43,16 @@ struct FullTraits {
   // Keeping the converted row in registers saves a second shared read when
   // the registers allow it.
   static constexpr bool kKeepX = CH <= 4 || (CH >= 6 && CH <= 8);
+  // fp32 values in shared memory before the stages: w * gamma, plus gamma_pre
+  // (mode 1) or one query row per consumer warp (mode 2).
+  static constexpr int fixed_floats(int mode) { return CH * 128 * (mode == 1 ? 2 : (mode == 2 ? 1 + kNW : 1)); }
 };
 
-// kPre: the epilogue also writes the sublayer pre-norm of the row (a separate
-// instance, so the plain read keeps its own code and schedule).
-template <typename Tin, int CH, bool kPre>
+// kMode 0: the read; 1: the epilogue also writes the sublayer pre-norm of the
+// row; 2: every token has its own query (a.Q, the input-dependent query),
+// staged per row in shared memory. Separate instances, so the plain read
+// keeps its own code and schedule.
+template <typename Tin, int CH, int kMode>
 __global__ void __launch_bounds__((FullTraits<CH>::kNW + 1) * kWarp, FullTraits<CH>::kMinBlocks)
     full_fwd_bulk_kernel(FullArgs a, int nstage) {
   constexpr int kNW = FullTraits<CH>::kNW;  // consumer warps = rows per tile
@@ -60,8 +65,9 @@ __global__ void __launch_bounds__((FullTraits<CH>::kNW + 1) * kWarp, FullTraits<
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty_bar = full_bar + kMaxStages;
   float* wq = reinterpret_cast<float*>(smem + kBarBytes);  // w * gamma, [D]
-  float* gq = wq + D;                                       // kPre: gamma_pre, [D]
-  Tin* stages = reinterpret_cast<Tin*>(smem + kBarBytes + (kPre ? 2 : 1) * D * sizeof(float));
+  constexpr bool kPre = kMode == 1, kDynQ = kMode == 2;
+  float* gq = wq + D;                                       // kPre: gamma_pre, [D]; kDynQ: q * gamma rows [kNW][D]
+  Tin* stages = reinterpret_cast<Tin*>(smem + kBarBytes + FullTraits<CH>::fixed_floats(kMode) * sizeof(float));
   constexpr int kStageElems = kTM * D;
 
   const int warp = threadIdx.x >> 5;
@@ -138,9 +144,11 @@ __global__ void __launch_bounds__((FullTraits<CH>::kNW + 1) * kWarp, FullTraits<
   // -------------------------------------------------------------- consumers
   // w * gamma into shared memory; the producer is already streaming meanwhile.
   for (int i = threadIdx.x; i < D / 4; i += kNW * kWarp) {
-    const float4 w4 = reinterpret_cast<const float4*>(a.w)[i];
-    const float4 g4 = reinterpret_cast<const float4*>(a.gamma)[i];
-    reinterpret_cast<float4*>(wq)[i] = make_float4(w4.x * g4.x, w4.y * g4.y, w4.z * g4.z, w4.w * g4.w);
+    if constexpr (!kDynQ) {  // with per-token queries there is no shared w
+      const float4 w4 = reinterpret_cast<const float4*>(a.w)[i];
+      const float4 g4 = reinterpret_cast<const float4*>(a.gamma)[i];
+      reinterpret_cast<float4*>(wq)[i] = make_float4(w4.x * g4.x, w4.y * g4.y, w4.z * g4.z, w4.w * g4.w);
+    }
     if constexpr (kPre) reinterpret_cast<float4*>(gq)[i] = reinterpret_cast<const float4*>(a.pre.gamma)[i];
   }
   named_sync(1, kNW * kWarp);
@@ -158,6 +166,21 @@ __global__ void __launch_bounds__((FullTraits<CH>::kNW + 1) * kWarp, FullTraits<
 #pragma unroll
     for (int e = 0; e < NE / 2; ++e) acc[e] = make_float2(0.f, 0.f);
     float m = -INFINITY, l = 0.f;
+    const float* qrow = wq;  // the query (times gamma) this row is scored with
+    if constexpr (kDynQ) {
+      float* qr = gq + warp * D;
+      if (valid) {
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const int k = (c * kWarp + lane) * 4;
+          const float4 q4 = *reinterpret_cast<const float4*>(a.Q + row * D + k);
+          const float4 g4 = *reinterpret_cast<const float4*>(a.gamma + k);
+          *reinterpret_cast<float4*>(qr + k) = make_float4(q4.x * g4.x, q4.y * g4.y, q4.z * g4.z, q4.w * g4.w);
+        }
+      }
+      __syncwarp();
+      qrow = qr;
+    }
 
     for (int src = 0; src < n; ++src) {
       if (!mbar_wait(smem_u32(&full_bar[stage]), phase)) {
@@ -179,7 +202,7 @@ __global__ void __launch_bounds__((FullTraits<CH>::kNW + 1) * kWarp, FullTraits<
           const float2 xb = make_float2(t4[2], t4[3]);
           ss2a = ffma2(xa, xa, ss2a);
           ss2b = ffma2(xb, xb, ss2b);
-          const float4 w4 = *reinterpret_cast<const float4*>(wq + (c * kWarp + lane) * 4);
+          const float4 w4 = *reinterpret_cast<const float4*>(qrow + (c * kWarp + lane) * 4);
           dt2a = ffma2(make_float2(w4.x, w4.y), xa, dt2a);
           dt2b = ffma2(make_float2(w4.z, w4.w), xb, dt2b);
         }
@@ -270,30 +293,31 @@ __global__ void __launch_bounds__((FullTraits<CH>::kNW + 1) * kWarp, FullTraits<
   if (a.late_wait) pdl_wait();
 }
 
-template <typename Tin, int CH, bool kPre>
+template <typename Tin, int CH, int kMode>
 cudaError_t launch_chp(const FullArgs& a, cudaStream_t s) {
   constexpr int D = CH * 128;
   constexpr int kTM = FullTraits<CH>::kNW;
   constexpr int kThreads = (kTM + 1) * kWarp;
   const int stage_bytes = kTM * D * static_cast<int>(sizeof(Tin));
-  const int fixed = kBarBytes + (kPre ? 2 : 1) * D * static_cast<int>(sizeof(float));
+  const int fixed = kBarBytes + FullTraits<CH>::fixed_floats(kMode) * static_cast<int>(sizeof(float));
   int nstage = (kSmemPerSM / FullTraits<CH>::kMinBlocks - 1024 - fixed) / stage_bytes;
   nstage = nstage < 2 ? 2 : (nstage > kMaxStages ? kMaxStages : nstage);
   const int smem = fixed + nstage * stage_bytes;
-  const void* fn = reinterpret_cast<const void*>(&full_fwd_bulk_kernel<Tin, CH, kPre>);
+  const void* fn = reinterpret_cast<const void*>(&full_fwd_bulk_kernel<Tin, CH, kMode>);
   cudaError_t e = allow_dynamic_smem(fn, smem);
   if (e != cudaSuccess) return e;
   const int per_sm = blocks_per_sm(fn, kThreads, smem);
   const int64_t tiles = (a.T + kTM - 1) / kTM;
   int64_t grid = static_cast<int64_t>(sm_count()) * (per_sm > 0 ? per_sm : 1);
   if (grid > tiles) grid = tiles;
-  return launch_pdl(full_fwd_bulk_kernel<Tin, CH, kPre>, static_cast<unsigned>(grid), kThreads, smem, s, a,
+  return launch_pdl(full_fwd_bulk_kernel<Tin, CH, kMode>, static_cast<unsigned>(grid), kThreads, smem, s, a,
                     nstage);
 }
 
 template <typename Tin, int CH>
 cudaError_t launch_ch(const FullArgs& a, cudaStream_t s) {
-  return a.pre.gamma ? launch_chp<Tin, CH, true>(a, s) : launch_chp<Tin, CH, false>(a, s);
+  if (a.Q) return launch_chp<Tin, CH, 2>(a, s);
+  return a.pre.gamma ? launch_chp<Tin, CH, 1>(a, s) : launch_chp<Tin, CH, 0>(a, s);
 }
 
 template <typename Tin>
@@ -338,7 +362,8 @@ bool full_fast_ok(const FullArgs& a) {
   const int ch = a.d / 128;
   const bool ch_ok = (a.d % 128 == 0) && ((ch >= 1 && ch <= 8) || ch == 10 || ch == 12 || ch == 16);
   return ch_ok && aligned16(a.V) && aligned16(a.out) && aligned16(a.w) && aligned16(a.gamma) &&
-         ((a.src_stride * es) % 16 == 0) && (!a.pre.gamma || (aligned16(a.pre.gamma) && aligned16(a.pre.out)));
+         ((a.src_stride * es) % 16 == 0) && (!a.pre.gamma || (aligned16(a.pre.gamma) && aligned16(a.pre.out))) &&
+         aligned16(a.Q) && !(a.Q && a.pre.gamma);
 }
 
 cudaError_t launch_full_fast(const FullArgs& a, cudaStream_t s) {

@@ -46,7 +46,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) multi_generic_kernel(Mult
         ss += x * x;
 #pragma unroll
         for (int j = 0; j < ATTNRES_MAX_QUERIES; ++j)
-          if (j < S) dot[j] += a.W[j * static_cast<int64_t>(d) + k] * a.Gamma[j * static_cast<int64_t>(d) + k] * x;
+          if (j < S) {
+            const float q = a.Q ? a.Q[row * d + k] : a.W[j * static_cast<int64_t>(d) + k];
+            dot[j] += q * a.Gamma[j * static_cast<int64_t>(d) + k] * x;
+          }
       }
       ss = warp_sum(ss);
       const float r = rsqrtf(ss * inv_d + a.eps);

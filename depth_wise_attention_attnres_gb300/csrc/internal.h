@@ -38,6 +38,7 @@ struct FullArgs {
   // read's loads overlap the tail of the previous one.
   int late_wait;
   PreNorm pre;          // out may be nullptr when pre.gamma is set
+  const float* Q;       // [T, d] fp32 per-token query (input-dependent); w then unused
 };
 
 // S queries over the same n_src sources (stage 1; the general kernel also
@@ -56,6 +57,7 @@ struct MultiArgs {
   void* out[ATTNRES_MAX_QUERIES];
   float* lse;           // [S, T] or nullptr
   PreNorm pre;          // S == 1 only (a Full read); out[0] may then be nullptr
+  const float* Q;       // S == 1 only: [T, d] fp32 per-token query instead of W
 };
 
 struct MergeArgs {
@@ -124,6 +126,10 @@ cudaError_t launch_rmsnorm(const void* x, int64_t T, int d, int is_bf16, const f
                            cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(cudaStream_t s);
 bool full_bwd_fast_ok(const BwdArgs& a);
+// Q = H Wq^T (bf16 H [T, d], Wq [d, d]; fp32 Q): the input-dependent query.
+bool proj_ok(const void* H, const void* Wq, const float* Q, int d);
+cudaError_t launch_proj(const void* H, const void* Wq, float* Q, int64_t T, int d, cudaStream_t s);
+cudaError_t launch_proj_generic(const void* H, const void* Wq, float* Q, int64_t T, int d, cudaStream_t s);
 cudaError_t launch_full_bwd(const BwdArgs& a, cudaStream_t s, bool fast);
 cudaError_t take_timeout_bwd(unsigned int* flag);
 

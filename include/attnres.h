@@ -137,6 +137,29 @@ int attnres_full_pass_prenorm(const void* V, int64_t src_stride, int32_t R, int6
                               void* stream);
 
 /*
+ * attnres_query_projection / attnres_full_fwd_dynq - the input-dependent
+ * query (the ablation the pages report: LLMRes blog, on the paper's ablation:
+ * a query projected from the current hidden state by a per-layer d x d matrix
+ * instead of the fixed learned pseudo-query).
+ *
+ * attnres_query_projection: Q[t, j] = sum_k Wq[j, k] H[t, k], i.e. Q = H Wq^T,
+ * on the tensor cores (bf16 inputs, fp32 sums).
+ *   H    device, [T, d] of h_dtype (ATTNRES_BF16 only; else UNSUPPORTED).
+ *   Wq   device, bf16 [d, d], row j the weights of query feature j.
+ *   Q    device, fp32 [T, d]; must not overlap H or Wq.
+ *
+ * attnres_full_fwd_dynq: the Full read with token t scored by its own query:
+ * e_i(t) = Q[t] . (gamma * v_i(t)) / rms(v_i(t)); otherwise as
+ * attnres_full_fwd (there is no shared w).
+ *   Q    device, fp32 [T, d]; must not overlap out.
+ */
+int attnres_query_projection(const void* H, int64_t T, int32_t d, int32_t h_dtype, const void* Wq,
+                             float* Q, void* stream);
+int attnres_full_fwd_dynq(const void* V, int64_t src_stride, int32_t n_src, int64_t T, int32_t d,
+                          int32_t v_dtype, const float* Q, const float* gamma, float eps, void* out,
+                          int32_t out_dtype, void* stream);
+
+/*
  * attnres_rmsnorm - RMSNorm of each row, out = gamma * x / sqrt(mean(x^2) + eps)
  * in fp32, stored in dtype: the sublayer pre-norm for a row no aggregation
  * call produces with it (the first sublayer of a block, whose output is

@@ -115,6 +115,17 @@ def test_full_bwd_validation(lib):
     assert lib.attnres_full_bwd(*(ok[:3] + (0,) + ok[4:]), None) == 0  # T = 0
 
 
+def test_dynamic_query_validation(lib):
+    # projection: fp32 H unsupported, Q overlapping H, null Wq, T = 0
+    assert lib.attnres_query_projection(P, 4, 16, 0, 2 * P, 3 * P, None) == UNSUPPORTED
+    assert lib.attnres_query_projection(P, 4, 16, 1, 2 * P, P + 32, None) == INVALID
+    assert lib.attnres_query_projection(P, 4, 16, 1, None, 3 * P, None) == INVALID
+    assert lib.attnres_query_projection(P, 0, 16, 1, 2 * P, 3 * P, None) == 0
+    # read with per-token queries: no Q, Q overlapping out
+    assert lib.attnres_full_fwd_dynq(P, 64, 2, 4, 16, 1, None, P, 1e-6, 8 * P, 1, None) == INVALID
+    assert lib.attnres_full_fwd_dynq(P, 64, 2, 4, 16, 1, 8 * P + 16, P, 1e-6, 8 * P, 1, None) == INVALID
+
+
 def test_kernel_selection(lib):
     A = 1 << 20
     # Full read: d multiple of 128 and 16-byte alignment -> fast kernel.
