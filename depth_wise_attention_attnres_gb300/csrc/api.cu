@@ -359,6 +359,7 @@ int attnres_query_projection(const void* H, int64_t T, int32_t d, int32_t h_dtyp
   if (overlap(rq, range_of(H, T * d * 2)) || overlap(rq, range_of(Wq, static_cast<int64_t>(d) * d * 2)))
     return ATTNRES_ERR_INVALID_ARG;
   cudaStream_t s = as_stream(stream);
+  if (proj_tc_ok(H, Wq, Q, T, d)) return status_of(launch_proj_tensor(H, Wq, Q, T, d, s));
   return status_of(proj_ok(H, Wq, Q, d) ? launch_proj(H, Wq, Q, T, d, s) : launch_proj_generic(H, Wq, Q, T, d, s));
 }
 
@@ -526,14 +527,14 @@ int attnres_device_status(void* stream) {
     cudaGetLastError();
     return ATTNRES_ERR_CUDA;
   }
-  unsigned int f1 = 0, f2 = 0, f3 = 0, f4 = 0, f5 = 0;
+  unsigned int f1 = 0, f2 = 0, f3 = 0, f4 = 0, f5 = 0, f6 = 0;
   if (take_timeout_full(&f1) != cudaSuccess || take_timeout_stage1(&f2) != cudaSuccess ||
       take_timeout_merge(&f3) != cudaSuccess || take_timeout_stage1tc(&f4) != cudaSuccess ||
-      take_timeout_bwd(&f5) != cudaSuccess) {
+      take_timeout_bwd(&f5) != cudaSuccess || take_timeout_proj(&f6) != cudaSuccess) {
     cudaGetLastError();
     return ATTNRES_ERR_CUDA;
   }
-  if (f1 || f2 || f3 || f4 || f5) return ATTNRES_ERR_TIMEOUT;
+  if (f1 || f2 || f3 || f4 || f5 || f6) return ATTNRES_ERR_TIMEOUT;
   e = cudaGetLastError();
   return e == cudaSuccess ? ATTNRES_OK : ATTNRES_ERR_CUDA;
 }

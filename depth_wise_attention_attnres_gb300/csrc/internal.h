@@ -130,6 +130,9 @@ bool full_bwd_fast_ok(const BwdArgs& a);
 bool proj_ok(const void* H, const void* Wq, const float* Q, int d);
 cudaError_t launch_proj(const void* H, const void* Wq, float* Q, int64_t T, int d, cudaStream_t s);
 cudaError_t launch_proj_generic(const void* H, const void* Wq, float* Q, int64_t T, int d, cudaStream_t s);
+bool proj_tc_ok(const void* H, const void* Wq, const float* Q, int64_t T, int d);
+cudaError_t launch_proj_tensor(const void* H, const void* Wq, float* Q, int64_t T, int d, cudaStream_t s);
+cudaError_t take_timeout_proj(unsigned int* flag);
 cudaError_t launch_full_bwd(const BwdArgs& a, cudaStream_t s, bool fast);
 cudaError_t take_timeout_bwd(unsigned int* flag);
 

@@ -9,6 +9,9 @@
 // pipeline into shared rows padded to 80 bytes (ldmatrix without bank
 // conflicts), m16n8k16 bf16 MMAs with fp32 accumulation. bf16 products are
 // exact in fp32, so Q carries only the fp32 rounding of the sums.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -152,6 +155,251 @@ cudaError_t launch_proj_generic(const void* H, const void* Wq, float* Q, int64_t
   if (blocks > cap) blocks = cap;
   return launch_pdl(proj_generic_kernel, static_cast<unsigned>(blocks), 256, 0, s, static_cast<const bf16*>(H),
                     static_cast<const bf16*>(Wq), Q, T, d);
+}
+
+
+// ------------------------------------------------------------ tcgen05 path --
+// The same GEMM on the 5th-generation tensor cores: one 128 x 128 output tile
+// per CTA, the fp32 accumulator in tensor memory (128 lanes x 128 columns).
+// Operand tiles of 128 rows x 64 K (one 128-byte swizzle atom per row) arrive
+// by 2-d TMA copies with the 128-byte swizzle into 4 stages; one thread issues
+// tcgen05.mma (M = 128, N = 128, K = 16, bf16 x bf16 -> fp32), and
+// tcgen05.commit frees a stage once the MMAs that read it are done. The four
+// warps then read their 32-lane quarter of the accumulator with tcgen05.ld and
+// store their rows. Every wait is bounded; whatever happens, the CTA waits for
+// the MMAs it issued and the copies in flight and frees its tensor memory.
+namespace {
+
+__device__ unsigned int g_proj_timeout = 0;
+
+constexpr int kTBM = 128, kTBN = 128, kTBK = 64, kTStages = 4;
+constexpr int kTTileBytes = kTBM * kTBK * 2;           // one operand tile, 16 KB
+constexpr int kTStageBytes = 2 * kTTileBytes;          // A and B
+constexpr int kTSmem = 1024 + kTStages * kTStageBytes + 128;
+constexpr int kTThreads = 128;
+constexpr uint32_t kTmemCols = 128;
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits 4-5),
+// bf16 A (7-9) and B (10-12), both K-major (15, 16), N / 8 (17-22), M / 16 (24-28).
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(kTBN >> 3) << 17) |
+                            (static_cast<uint32_t>(kTBM >> 4) << 24);
+
+// Shared-memory descriptor of a K-major operand tile in the 128-byte swizzle
+// (8-row atoms of 128-byte rows, 1024 bytes apart): start address / 16 (bits
+// 0-13), leading offset (ignored for this layout, 1), stride offset 1024 / 16
+// (32-45), descriptor version 1 (46-47), layout SWIZZLE_128B = 2 (61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+      ::"r"(tmem), "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__global__ void __launch_bounds__(kTThreads, 1)
+    proj_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, float* Q,
+                   int64_t T, int d) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kTStages * kTStageBytes);
+  uint64_t* empty_bar = full_bar + kTStages;
+  uint64_t* done_bar = empty_bar + kTStages;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done_bar + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * kTBM, n0 = blockIdx.y * kTBN;
+  const int nk = d / kTBK;
+
+  pdl_trigger();
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < kTStages; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    mbar_init(smem_u32(done_bar), 1);
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_holder;
+  pdl_wait();
+
+  bool ok = true;
+  if (warp == 0 && lane == 0) {
+    // Producer: A rows m0.., B rows n0.., 64 K per stage.
+    int s = 0;
+    uint32_t phase = 0;
+    int issued = 0;
+    for (int kt = 0; kt < nk; ++kt) {
+      if (!mbar_wait(smem_u32(&empty_bar[s]), phase ^ 1u)) {
+        ok = false;
+        break;
+      }
+      const uint32_t fb = smem_u32(&full_bar[s]);
+      mbar_arrive_expect_tx(fb, kTStageBytes);
+      const uint32_t st = smem_u32(smem + s * kTStageBytes);
+      tma_load_2d(st, &tmA, kt * kTBK, m0, fb);
+      tma_load_2d(st + kTTileBytes, &tmB, kt * kTBK, n0, fb);
+      ++issued;
+      if (++s == kTStages) {
+        s = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) {
+      atomicOr(&g_proj_timeout, 1u);
+      for (int it = issued > kTStages ? issued - kTStages : 0; it < issued; ++it)
+        (void)mbar_wait(smem_u32(&full_bar[it % kTStages]), static_cast<uint32_t>((it / kTStages) & 1));
+    }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer: 4 MMAs of K = 16 per stage (the descriptor start moves 32 B).
+    int s = 0;
+    uint32_t phase = 0;
+    for (int kt = 0; kt < nk; ++kt) {
+      if (!mbar_wait(smem_u32(&full_bar[s]), phase)) {
+        ok = false;
+        break;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t st = smem_u32(smem + s * kTStageBytes);
+      const uint64_t da = sw128_desc(st), db = sw128_desc(st + kTTileBytes);
+#pragma unroll
+      for (int k = 0; k < kTBK / 16; ++k)
+        umma_bf16(tmem, da + static_cast<uint64_t>(k * 2), db + static_cast<uint64_t>(k * 2), (kt | k) != 0);
+      umma_commit(smem_u32(&empty_bar[s]));
+      if (++s == kTStages) {
+        s = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) atomicOr(&g_proj_timeout, 1u);
+    // Signals once every MMA issued above is done (also after a timeout).
+    umma_commit(smem_u32(done_bar));
+  }
+  __syncwarp();
+
+  // Epilogue: warp w holds rows m0 + 32 w .. of the tile in its TMEM lanes.
+  const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(done_bar), 0));
+  if (got) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const int64_t row = static_cast<int64_t>(m0) + warp * 32 + lane;
+#pragma unroll 1
+    for (int c = 0; c < kTBN / 32; ++c) {
+      float v[32];
+      tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(c * 32), v);
+      if (row < T) {
+        float4* dst = reinterpret_cast<float4*>(Q + row * d + n0 + c * 32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      }
+    }
+  } else if (lane == 0) {
+    atomicOr(&g_proj_timeout, 1u);
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 proj_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// A [rows, d] bf16 operand as a 2-d tensor, box {64, 128}, 128-byte swizzle.
+bool encode_operand(const void* base, int64_t rows, int d, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = proj_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+  const cuuint32_t box[2] = {kTBK, kTBM};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_proj_tc(const void* H, const void* Wq, float* Q, int64_t T, int d, cudaStream_t s) {
+  alignas(64) CUtensorMap ma, mb;
+  if (!encode_operand(H, T, d, &ma) || !encode_operand(Wq, d, d, &mb)) return cudaErrorInvalidValue;
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(&proj_tc_kernel), kTSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((T + kTBM - 1) / kTBM), static_cast<unsigned>(d / kTBN));
+  cfg.blockDim = dim3(kTThreads);
+  cfg.dynamicSmemBytes = kTSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, proj_tc_kernel, ma, mb, Q, T, d);
+}
+
+}  // namespace
+
+bool proj_tc_ok(const void* H, const void* Wq, const float* Q, int64_t T, int d) {
+  return d % kTBN == 0 && aligned16(H) && aligned16(Wq) && aligned16(Q) && T < (int64_t(1) << 31) &&
+         (T + kTBM - 1) / kTBM <= 0x7fffffff && proj_encode_fn() != nullptr;
+}
+
+cudaError_t take_timeout_proj(unsigned int* flag) {
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(flag, g_proj_timeout, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_proj_timeout, &zero, sizeof(unsigned int));
+}
+
+cudaError_t launch_proj_tensor(const void* H, const void* Wq, float* Q, int64_t T, int d, cudaStream_t s) {
+  return launch_proj_tc(H, Wq, Q, T, d, s);
 }
 
 bool proj_ok(const void* H, const void* Wq, const float* Q, int d) {
