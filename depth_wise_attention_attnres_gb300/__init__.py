@@ -22,6 +22,8 @@ from .binding import (  # noqa: F401
     attnres_kernel_path,
     attnres_query_projection,
     attnres_rmsnorm,
+    attnres_stage1_dsplit_finish,
+    attnres_stage1_dsplit_partials,
     attnres_status_string,
     lib,
 )

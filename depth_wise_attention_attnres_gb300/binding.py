@@ -33,6 +33,9 @@ _SIGNATURES = {
     "attnres_full_pass_prenorm": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _F, _VP,
                                   _VP, _I64, _I32, _VP],
     "attnres_rmsnorm": [_VP, _I64, _I32, _I32, _VP, _F, _VP, _VP],
+    "attnres_stage1_dsplit_partials": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _I32, _VP, _I32, _VP],
+    "attnres_stage1_dsplit_finish": [_VP, _I64, _I32, _I64, _I32, _I32, _I32, _VP, _I32, _F,
+                                     ctypes.POINTER(_VP), _VP, _VP],
     "attnres_query_projection": [_VP, _I64, _I32, _I32, _VP, _VP, _VP],
     "attnres_full_fwd_dynq": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _I32, _VP],
     "attnres_full_bwd": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _I32, _VP, _I64, _VP, _VP,
@@ -247,6 +250,31 @@ def attnres_full_fwd_dynq(V: torch.Tensor, n_src: int, Q: torch.Tensor, gamma: t
         _ptr(V), stride, n_src, T, d, _dtype(V), _ptr(Q), _ptr(gamma), eps, _ptr(out), _dtype(out),
         _stream(stream)))
     return out
+
+
+def attnres_stage1_dsplit_partials(Src: torch.Tensor, n_src: int, W: torch.Tensor, Gamma: torch.Tensor,
+                                   partials: torch.Tensor, accumulate: bool, stream=None) -> torch.Tensor:
+    """One feature shard's part of the stage-1 score sums: Src [n, T, d_shard], W and
+    Gamma fp32 [S, d_shard] (the shard's slices); partials fp32 [T, n_src, S + 1]."""
+    _, T, ds, stride = _slices(Src)
+    S = W.shape[0]
+    if tuple(partials.shape) != (T, n_src, S + 1) or partials.dtype != torch.float32:
+        raise ValueError("partials must be fp32 [T, n_src, S + 1]")
+    _check("attnres_stage1_dsplit_partials", lib().attnres_stage1_dsplit_partials(
+        _ptr(Src), stride, n_src, T, ds, _dtype(Src), _ptr(W), _ptr(Gamma), S, _ptr(partials),
+        int(bool(accumulate)), _stream(stream)))
+    return partials
+
+
+def attnres_stage1_dsplit_finish(Src: torch.Tensor, n_src: int, d_total: int, partials: torch.Tensor,
+                                 eps: float, O: list, lse: torch.Tensor | None, stream=None) -> None:
+    """A shard's features of the S normalised reads from the summed partials."""
+    _, T, ds, stride = _slices(Src)
+    S = len(O)
+    ptrs = (ctypes.c_void_p * max(S, 1))(*[_ptr(o) for o in O])
+    _check("attnres_stage1_dsplit_finish", lib().attnres_stage1_dsplit_finish(
+        _ptr(Src), stride, n_src, T, ds, d_total, _dtype(Src), _ptr(partials), S, eps, ptrs,
+        _ptr(lse), _stream(stream)))
 
 
 def attnres_rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float, out: torch.Tensor,

@@ -416,6 +416,75 @@ int attnres_full_bwd(const void* V, int64_t src_stride, int32_t n_src, int64_t T
   return status_of(launch_full_bwd(a, as_stream(stream), fast));
 }
 
+// Shared checks of the two d-split calls: the shard's sources and queries.
+int make_dsplit(const void* Src, int64_t src_stride, int32_t n_src, int64_t T, int32_t d_shard, int32_t d_total,
+                int32_t dtype, const float* W, const float* Gamma, int32_t S, float eps, float* partials,
+                DsplitArgs* a) {
+  if (n_src < 1 || d_shard < 1 || d_total < d_shard || T < 0 || !valid_dtype(dtype) || !valid_eps(eps) || S < 1 ||
+      S > ATTNRES_MAX_QUERIES)
+    return ATTNRES_ERR_INVALID_ARG;
+  if (T == 0) return ATTNRES_OK;
+  if (!Src || !partials) return ATTNRES_ERR_INVALID_ARG;
+  const int64_t E = T * d_shard;
+  if (n_src > 1 && src_stride < E) return ATTNRES_ERR_INVALID_ARG;
+  const Range rs = range_of(Src, ((n_src - 1) * (n_src > 1 ? src_stride : 0) + E) * elem_size(dtype));
+  const Range rp = range_of(partials, static_cast<int64_t>(n_src) * (S + 1) * T * 4);
+  if (overlap(rs, rp)) return ATTNRES_ERR_INVALID_ARG;
+  *a = DsplitArgs{};
+  a->Src = Src;
+  a->src_stride = n_src > 1 ? src_stride : 0;
+  a->n_src = n_src;
+  a->T = T;
+  a->d_shard = d_shard;
+  a->d_total = d_total;
+  a->bf16 = dtype == ATTNRES_BF16;
+  a->W = W;
+  a->Gamma = Gamma;
+  a->S = S;
+  a->eps = eps;
+  a->partials = partials;
+  return ATTNRES_OK;
+}
+
+int attnres_stage1_dsplit_partials(const void* Src, int64_t src_stride, int32_t n_src, int64_t T, int32_t d_shard,
+                                   int32_t dtype, const float* W, const float* Gamma, int32_t S, float* partials,
+                                   int32_t accumulate, void* stream) {
+  DsplitArgs a;
+  const int st = make_dsplit(Src, src_stride, n_src, T, d_shard, d_shard, dtype, W, Gamma, S, 0.f, partials, &a);
+  if (st != ATTNRES_OK || T == 0) return st;
+  if (!W || !Gamma) return ATTNRES_ERR_INVALID_ARG;
+  a.accumulate = accumulate != 0;
+  if (!dsplit_ok(a)) return ATTNRES_ERR_UNSUPPORTED;
+  return status_of(launch_dsplit_partials(a, as_stream(stream)));
+}
+
+int attnres_stage1_dsplit_finish(const void* Src, int64_t src_stride, int32_t n_src, int64_t T, int32_t d_shard,
+                                 int32_t d_total, int32_t dtype, const float* partials, int32_t S, float eps,
+                                 void* const* O, float* lse, void* stream) {
+  DsplitArgs a;
+  const int st = make_dsplit(Src, src_stride, n_src, T, d_shard, d_total, dtype, nullptr, nullptr, S, eps,
+                             const_cast<float*>(partials), &a);
+  if (st != ATTNRES_OK || T == 0) return st;
+  if (!O) return ATTNRES_ERR_INVALID_ARG;
+  const int64_t E = T * d_shard;
+  const int es = elem_size(dtype);
+  const Range rs = range_of(Src, ((n_src - 1) * a.src_stride + E) * es);
+  const Range rp = range_of(partials, static_cast<int64_t>(n_src) * (S + 1) * T * 4);
+  const Range rl = lse ? range_of(lse, static_cast<int64_t>(S) * T * 4) : Range{};
+  if (overlap(rl, rs) || overlap(rl, rp)) return ATTNRES_ERR_INVALID_ARG;
+  for (int j = 0; j < S; ++j) {
+    if (!O[j]) return ATTNRES_ERR_INVALID_ARG;
+    const Range ro = range_of(O[j], E * es);
+    if (overlap(ro, rs) || overlap(ro, rp) || overlap(ro, rl)) return ATTNRES_ERR_INVALID_ARG;
+    for (int q = 0; q < j; ++q)
+      if (overlap(ro, range_of(O[q], E * es))) return ATTNRES_ERR_INVALID_ARG;
+    a.out[j] = O[j];
+  }
+  a.lse = lse;
+  if (!dsplit_ok(a)) return ATTNRES_ERR_UNSUPPORTED;
+  return status_of(launch_dsplit_finish(a, as_stream(stream)));
+}
+
 int attnres_block_stage1(const void* Src, int64_t src_stride, int32_t n_src, int64_t T, int32_t d,
                          int32_t dtype, const float* W, const float* Gamma, int32_t S, float eps,
                          void* const* O, float* lse, void* stream) {
@@ -527,14 +596,15 @@ int attnres_device_status(void* stream) {
     cudaGetLastError();
     return ATTNRES_ERR_CUDA;
   }
-  unsigned int f1 = 0, f2 = 0, f3 = 0, f4 = 0, f5 = 0, f6 = 0;
+  unsigned int f1 = 0, f2 = 0, f3 = 0, f4 = 0, f5 = 0, f6 = 0, f7 = 0;
   if (take_timeout_full(&f1) != cudaSuccess || take_timeout_stage1(&f2) != cudaSuccess ||
       take_timeout_merge(&f3) != cudaSuccess || take_timeout_stage1tc(&f4) != cudaSuccess ||
-      take_timeout_bwd(&f5) != cudaSuccess || take_timeout_proj(&f6) != cudaSuccess) {
+      take_timeout_bwd(&f5) != cudaSuccess || take_timeout_proj(&f6) != cudaSuccess ||
+      take_timeout_dsplit(&f7) != cudaSuccess) {
     cudaGetLastError();
     return ATTNRES_ERR_CUDA;
   }
-  if (f1 || f2 || f3 || f4 || f5 || f6) return ATTNRES_ERR_TIMEOUT;
+  if (f1 || f2 || f3 || f4 || f5 || f6 || f7) return ATTNRES_ERR_TIMEOUT;
   e = cudaGetLastError();
   return e == cudaSuccess ? ATTNRES_OK : ATTNRES_ERR_CUDA;
 }

@@ -97,6 +97,26 @@ struct BwdArgs {
 constexpr int kMaxBwdFastSources = 256;   // per-(row, source) scalars live in shared memory
 constexpr int kMaxBwdGenericD = 16384;    // du of a CTA lives in shared memory
 
+// Block stage 1 over one feature shard (dsplit.cu).
+struct DsplitArgs {
+  const void* Src;      // [n_src, T, d_shard] the shard's features of each source
+  int64_t src_stride;   // elements
+  int n_src;
+  int64_t T;
+  int d_shard;
+  int d_total;          // the full width (the mean of squares divides by it)
+  int bf16;
+  const float* W;       // [S, d_shard] the shard's slice of each query
+  const float* Gamma;   // [S, d_shard]
+  int S;
+  float eps;
+  float* partials;      // [T][n_src][S + 1] fp32: sum v^2, then the S dots
+  int accumulate;       // partials: add to the buffer instead of writing it
+  void* out[ATTNRES_MAX_QUERIES];  // finish: [T, d_shard] per query
+  float* lse;           // finish: [S, T] or nullptr
+};
+constexpr int kMaxDsplitShard = 512;
+
 struct AccumArgs {
   float* P;
   const void* f;
@@ -133,6 +153,10 @@ cudaError_t launch_proj_generic(const void* H, const void* Wq, float* Q, int64_t
 bool proj_tc_ok(const void* H, const void* Wq, const float* Q, int64_t T, int d);
 cudaError_t launch_proj_tensor(const void* H, const void* Wq, float* Q, int64_t T, int d, cudaStream_t s);
 cudaError_t take_timeout_proj(unsigned int* flag);
+bool dsplit_ok(const DsplitArgs& a);
+cudaError_t launch_dsplit_partials(const DsplitArgs& a, cudaStream_t s);
+cudaError_t launch_dsplit_finish(const DsplitArgs& a, cudaStream_t s);
+cudaError_t take_timeout_dsplit(unsigned int* flag);
 cudaError_t launch_full_bwd(const BwdArgs& a, cudaStream_t s, bool fast);
 cudaError_t take_timeout_bwd(unsigned int* flag);
 

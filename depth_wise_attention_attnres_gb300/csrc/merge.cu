@@ -37,16 +37,6 @@ constexpr int kWarps = kBlock / 32;
 
 // ------------------------------------------------------------- fast merge --
 
-// 4 consecutive features: bf16 as 8 bytes, fp32 as 16 bytes (global memory).
-__device__ __forceinline__ void ldg4(const bf16* p, float (&x)[4]) {
-  const uint2 v = *reinterpret_cast<const uint2*>(p);
-  x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
-}
-__device__ __forceinline__ void ldg4(const float* p, float (&x)[4]) {
-  const float4 v = *reinterpret_cast<const float4*>(p);
-  x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-}
-
 __device__ unsigned int g_merge_timeout = 0;
 
 constexpr int kMNW = 8;                      // consumer warps

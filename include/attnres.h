@@ -222,6 +222,44 @@ int attnres_block_stage1(const void* Src, int64_t src_stride, int32_t n_src, int
                          int32_t S, float eps, void* const* O, float* lse, void* stream);
 
 /*
+ * attnres_stage1_dsplit_partials / attnres_stage1_dsplit_finish - stage 1 with
+ * the features split into shards (datacamp explainer, system optimisations,
+ * "memory-efficient prefill": block representations sharded across
+ * tensor-parallel devices; read as a feature split, where each device keeps a
+ * slice of every source row and only score statistics cross devices). A score needs
+ * ss = sum_k v_k^2 and dot_j = sum_k w_jk gamma_jk v_k over all d features;
+ * both are sums, so each shard forms its part and the parts are added (the one
+ * exchange step: an all-reduce of (1 + S) floats per (source, token)). With the
+ * totals, each shard finishes the softmax and its own features of the outputs.
+ *
+ * partials:
+ *   Src       device, [n_src, T, d_shard] the shard's features, src_stride >= T*d_shard.
+ *   W, Gamma  device, fp32 [S, d_shard], the shard's slice of each query row.
+ *   partials  device, fp32 [T][n_src][S + 1]: for token t and source i, entry 0
+ *             holds ss, entry 1 + j dot_j. accumulate != 0 adds to it (the
+ *             shards of one GPU in turn); 0 overwrites.
+ * finish:
+ *   Src       as above; d_total the full feature count (mean of squares).
+ *   partials  the totals over all shards.
+ *   O         host array of S device pointers, [T, d_shard] each: the shard's
+ *             features of each query's normalised read.
+ *   lse       device, fp32 [S, T] or NULL.
+ * Kernels: bf16 shards whose width is a multiple of 64 stream the sources by
+ * TMA and take the dots, sum v^2 and (with at most 16 sources) the weighted
+ * sums on the tensor cores; other shapes take FMA kernels.
+ * Shards wider than 512 features, or unaligned buffers, return
+ * ATTNRES_ERR_UNSUPPORTED.
+ */
+int attnres_stage1_dsplit_partials(const void* Src, int64_t src_stride, int32_t n_src, int64_t T,
+                                   int32_t d_shard, int32_t dtype, const float* W,
+                                   const float* Gamma, int32_t S, float* partials,
+                                   int32_t accumulate, void* stream);
+int attnres_stage1_dsplit_finish(const void* Src, int64_t src_stride, int32_t n_src, int64_t T,
+                                 int32_t d_shard, int32_t d_total, int32_t dtype,
+                                 const float* partials, int32_t S, float eps, void* const* O,
+                                 float* lse, void* stream);
+
+/*
  * attnres_block_merge - stage 2 for one sublayer: extend the block's running
  * sum and merge it, as one more softmax source, with the stage-1 result
  * (datacamp explainer, "two-stage computation": online-softmax merge of the

@@ -126,6 +126,18 @@ def test_dynamic_query_validation(lib):
     assert lib.attnres_full_fwd_dynq(P, 64, 2, 4, 16, 1, 8 * P + 16, P, 1e-6, 8 * P, 1, None) == INVALID
 
 
+def test_dsplit_validation(lib):
+    ptrs = (ctypes.c_void_p * 2)(P * 8, P * 16)
+    same = (ctypes.c_void_p * 2)(P * 8, P * 8)
+    # partials: S out of range, partials overlapping Src, shard wider than 512
+    assert lib.attnres_stage1_dsplit_partials(P, 64, 2, 4, 16, 1, P, P, 0, 2 * P, 0, None) == INVALID
+    assert lib.attnres_stage1_dsplit_partials(P, 64, 2, 4, 16, 1, P, P, 2, P + 32, 0, None) == INVALID
+    assert lib.attnres_stage1_dsplit_partials(P, 4096, 2, 4, 1024, 1, P, P, 2, 8 * P, 0, None) == UNSUPPORTED
+    # finish: d_total below the shard, overlapping outputs
+    assert lib.attnres_stage1_dsplit_finish(P, 64, 2, 4, 16, 8, 1, 2 * P, 2, 1e-6, ptrs, None, None) == INVALID
+    assert lib.attnres_stage1_dsplit_finish(P, 64, 2, 4, 16, 64, 1, 2 * P, 2, 1e-6, same, None, None) == INVALID
+
+
 def test_kernel_selection(lib):
     A = 1 << 20
     # Full read: d multiple of 128 and 16-byte alignment -> fast kernel.
