@@ -64,6 +64,25 @@ def block_pass_bytes(N: int, S: int, T: int, d: int, es: int, freeze_last: bool 
     return {"stage1": st1, "merge": merge, "freeze": freeze, "total": st1 + merge + freeze}
 
 
+DSPLIT_SHARDS = 4
+
+
+def dsplit_stage1_bytes(N: int, S: int, T: int, d: int, es: int, P: int) -> dict:
+    """Algorithmic bytes of the Block pass's N stage-1 reads taken as a d-split
+    over P feature shards. Block n (n+1 sources): the partials kernels read
+    every source row once and write the fp32 sums [T, n+1, S+1] (the first
+    shard writes them, the others read and write them); the finish kernels
+    read every source row once more and the sums once per shard, and write S
+    output rows and S lse values per token."""
+    E = T * d
+    part = fin = 0
+    for n in range(N):
+        sums = (n + 1) * T * (S + 1) * 4
+        part += (n + 1) * E * es + sums * (2 * P - 1)
+        fin += (n + 1) * E * es + sums * P + S * E * es + S * T * 4
+    return {"partials": part, "finish": fin, "total": part + fin}
+
+
 # ---------------------------------------------------------------- clocks ----
 
 class ClockSampler:
@@ -279,12 +298,83 @@ class BlockPassStep:
                                    self.Src, self.O, self.lse, self.P, self.out)
 
 
+class DsplitStep:
+    """The Block pass's N stage-1 reads (block n: the embedding and n block
+    summaries as sources, the block's S queries) with the features split over
+    P shards, as a tensor-parallel prefill lays them out: per block, every
+    shard's partial score sums (added in turn, where devices would all-reduce
+    them), then every shard's finish."""
+
+    def __init__(self, wl, dev, P=DSPLIT_SHARDS):
+        from depth_wise_attention_attnres_gb300 import binding
+        self.ar = binding
+        self.wl = wl
+        self.P = P
+        dt = inputs.DTYPES[wl.dtype]
+        ds = wl.d // P
+        g = inputs.generator(wl.seed, dev)
+        src = inputs.history(wl.N, wl.T, wl.d, wl.dtype, g, dev, wl.depth_scaled)
+        W = inputs.queries(wl.N * wl.S, wl.d, wl.w_std, g, dev)
+        G = torch.ones((wl.N * wl.S, wl.d), dtype=torch.float32, device=dev)
+        self.Src = [src[:, :, p * ds:(p + 1) * ds].contiguous() for p in range(P)]
+        self.Wp = [W[:, p * ds:(p + 1) * ds].contiguous() for p in range(P)]
+        self.Gp = [G[:, p * ds:(p + 1) * ds].contiguous() for p in range(P)]
+        del src
+        self.parts = [torch.empty(wl.T, n + 1, wl.S + 1, device=dev) for n in range(wl.N)]
+        self.outs = [[torch.empty(wl.T, ds, device=dev, dtype=dt) for _ in range(wl.S)] for _ in range(P)]
+        self.lse = torch.empty(wl.S, wl.T, device=dev)
+        self.launches = wl.N * 2 * P
+        es = 2 if wl.dtype == "bf16" else 4
+        self.byte_parts = dsplit_stage1_bytes(wl.N, wl.S, wl.T, wl.d, es, P)
+        self.bytes = self.byte_parts["total"]
+
+    def partials(self, n, stream=None):
+        S = self.wl.S
+        for p in range(self.P):
+            self.ar.attnres_stage1_dsplit_partials(self.Src[p], n + 1, self.Wp[p][n * S:(n + 1) * S],
+                                                   self.Gp[p][n * S:(n + 1) * S], self.parts[n], p > 0,
+                                                   stream=stream)
+
+    def finish(self, n, stream=None):
+        for p in range(self.P):
+            self.ar.attnres_stage1_dsplit_finish(self.Src[p], n + 1, self.wl.d, self.parts[n], self.wl.eps,
+                                                 self.outs[p], self.lse if p == 0 else None, stream=stream)
+
+    def __call__(self):
+        for n in range(self.wl.N):
+            self.partials(n)
+            self.finish(n)
+
+
+def time_dsplit_kernels(step, reps, stream):
+    """Device time of the partials and finish launches of a d-split step."""
+    acc = {"partials": 0.0, "finish": 0.0}
+    marks = []
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            for n in range(step.wl.N):
+                for kind in ("partials", "finish"):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    getattr(step, kind)(n, stream=stream)
+                    b.record(stream)
+                    marks.append((kind, a, b))
+    torch.cuda.synchronize()
+    for kind, a, b in marks:
+        acc[kind] += a.elapsed_time(b)
+    return {k: v / reps for k, v in acc.items()}
+
+
 def make_step(name, dev, op="read"):
     wl = inputs.WORKLOADS[name]
     if wl.kind == "full_pass":
+        if op == "dsplit":
+            raise ValueError("--op dsplit applies to Block-pass workloads")
         return FullPassStep(wl, dev, op)
+    if wl.kind == "block_pass" and op == "dsplit":
+        return DsplitStep(wl, dev)
     if op != "read":
-        raise ValueError("--op applies to Full-pass workloads")
+        raise ValueError("--op applies to Full-pass workloads (dsplit: Block-pass workloads)")
     if wl.kind == "block_pass":
         return BlockPassStep(wl, dev)
     raise ValueError(f"{name} is a parity case, not a benchmark workload")
@@ -536,6 +626,18 @@ def ours(args):
             "per_launch_bytes": step.bytes / step.launches,
             "note": "the step is R launches of this one kernel back to back in a CUDA graph; "
                     "average launch duration = step time / R (gaps included)"}
+    elif isinstance(step, DsplitStep):
+        times = time_dsplit_kernels(step, 3, stream)
+        parts = step.byte_parts
+        kernels = {k: {"ms": times[k], "gbs": parts[k] / (times[k] / 1e3) / 1e9} for k in times}
+        top = max(kernels, key=lambda k: kernels[k]["ms"])
+        g = kernels[top]["gbs"]
+        line["config"]["shards"] = step.P
+        line["roofline"] = {
+            "kernel": {"partials": "dsplit_partials_tc_kernel", "finish": "dsplit_finish_tc_kernel"}[top],
+            "bound": "hbm", "achieved": g, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": g / peaks["hbm_gbs"], "frac_of_nominal_8000": g / NOMINAL_HBM_GBS,
+            "peak_source": peaks["source"], "traffic": None, "per_kernel": kernels}
     else:
         times = time_block_kernels(step, 3, stream)
         parts = step.byte_parts
@@ -617,10 +719,11 @@ def main():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(
         n for n, w in inputs.WORKLOADS.items() if w.kind != "full_read"))
-    p.add_argument("--op", choices=["read", "prenorm", "prenorm_both", "bwd", "dynq"], default="read",
-                   help="Full pass only: plain reads, reads emitting the sublayer pre-norm instead of "
+    p.add_argument("--op", choices=["read", "prenorm", "prenorm_both", "bwd", "dynq", "dsplit"], default="read",
+                   help="Full pass: plain reads, reads emitting the sublayer pre-norm instead of "
                         "their result, or both, the pass backward (dV, dW, dGamma), or reads with "
-                        "input-dependent queries (projection + read)")
+                        "input-dependent queries (projection + read). Block pass: dsplit, the stage-1 "
+                        "reads with the features split over 4 shards")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-block", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
