@@ -48,15 +48,6 @@ __host__ __device__ inline int tc_pitch(int ds) { return (((ds * 2 + 127) / 128)
 
 inline int finish_smem(const DsplitArgs& a) { return kDWarps * a.n_src * ((a.S + 3) & ~3) * 4; }
 
-// c += A (16x16 bf16, row-major fragments a) * B (16x8 bf16, col-major fragments b0 b1), fp32.
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 template <typename T>
 __global__ void __launch_bounds__(kDWarps * 32) dsplit_partials_kernel(DsplitArgs a) {
   extern __shared__ float wq[];  // [S][d_s] w * gamma of the shard
@@ -212,16 +203,6 @@ __device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap* ma
       "%5}], [%6];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(tok0), "r"(0), "r"(bar)
       : "memory");
-}
-
-// d = A * B (the accumulator starts at zero).
-__device__ __forceinline__ void mma16816_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  const float z = 0.f;
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%10,%10,%10,%10};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
 }
 
 // Fire-and-forget fp32 add to global memory (one add per address and launch,
@@ -412,12 +393,6 @@ __global__ void __launch_bounds__(8 * 32, 1)
     for (int64_t jj = j; jj < j + G.nst && first + jj * tstride < ntiles; ++jj)
       (void)mbar_wait(smem_u32(&bars[jj % G.nst]), static_cast<uint32_t>((jj / G.nst) & 1));
   }
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
 }
 
 // bf16 finish on the tensor cores (n <= 16 sources, shard width a multiple of

@@ -34,20 +34,6 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ void ldsm_x4_p(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_p(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 __global__ void __launch_bounds__(kPThreads) proj_kernel(const bf16* H, const bf16* Wq, float* Q, int64_t T,
                                                          int d) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -103,13 +89,13 @@ __global__ void __launch_bounds__(kPThreads) proj_kernel(const bf16* H, const bf
     for (int kk = 0; kk < kPBK; kk += 16) {
       uint32_t af[4][4], bfr[2][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) ldsm_x4_p(smem_u32(Ab + (i * 16 + a_row) * kPPitch + kk + a_col), af[i]);
+      for (int i = 0; i < 4; ++i) ldsm_x4(smem_u32(Ab + (i * 16 + a_row) * kPPitch + kk + a_col), af[i]);
 #pragma unroll
-      for (int j = 0; j < 2; ++j) ldsm_x4_p(smem_u32(Bb + (j * 16 + b_row) * kPPitch + kk + b_col), bfr[j]);
+      for (int j = 0; j < 2; ++j) ldsm_x4(smem_u32(Bb + (j * 16 + b_row) * kPPitch + kk + b_col), bfr[j]);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) mma_p(acc[i][j], af[i], bfr[j >> 1][(j & 1) * 2], bfr[j >> 1][(j & 1) * 2 + 1]);
+        for (int j = 0; j < 4; ++j) mma16816(acc[i][j], af[i], bfr[j >> 1][(j & 1) * 2], bfr[j >> 1][(j & 1) * 2 + 1]);
     }
     __syncthreads();  // the stage is overwritten by a later load
   }
