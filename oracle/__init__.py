@@ -25,6 +25,11 @@ This module adds the sequencing the pages describe on top of it:
   the result, by the chain rule through the read's definition (the
   backward the pages point to when they note that stored sublayer outputs
   are reused for it; DepthBench reading notes section 2.3 for the read).
+* ``block_pass_bwd``: the gradients of a whole Block pass by the chain rule
+  through its definition: each read's ``read_bwd`` over its source set, the
+  gradient of a block summary b_m (a plain sum) passed unchanged to every
+  member output of block m, and that of the running sum P_k to every earlier
+  output of the current block.
 * ``query_projection`` / ``read_dynamic_query``: the input-dependent query
   the pages report as an ablation (LLMRes blog, on the paper's ablation: a
   query projected from the current hidden state by a per-layer d x d matrix
@@ -250,6 +255,41 @@ def read_bwd(sources, w, gamma, eps, dz):
 def full_read_bwd(V, n_src, w, gamma, eps, dz):
     """Gradients of the Full read over V[0 .. n_src) (see ``read_bwd``)."""
     return read_bwd(_slices(V, n_src), w, gamma, eps, dz)
+
+
+def block_pass_bwd(Src, F, N, S, W, Gamma, eps, dOut):
+    """Gradients of a Block AttnRes pass with loss sum_k <dOut[k], out_k>.
+
+    Src: the embedding (Src[0]) and the frozen block summaries b_1 .. b_{N-1}
+    as the forward stored them; the reads take them as given. F: [N*S, T, d]
+    sublayer outputs; the running sums P_k are exact fp64 sums of them. W,
+    Gamma: [N*S, d]. dOut: [N*S, T, d]. Returns fp64 (dEmb [T, d], dF [N*S, T,
+    d], dW [N*S, d], dGamma [N*S, d]). A summary b_m is the plain sum of block
+    (m-1)'s outputs, so its gradient reaches each of them unchanged; the
+    gradient of P_k reaches each output of the current block before k.
+    """
+    s64 = [widen(Src[i]) if not isinstance(Src, np.ndarray) else np.asarray(Src[i], np.float64)
+           for i in range(N)]
+    f64 = widen(F) if not isinstance(F, np.ndarray) else np.asarray(F, np.float64)
+    g = widen(dOut) if not isinstance(dOut, np.ndarray) else np.asarray(dOut, np.float64)
+    W64 = np.asarray(W, np.float64)
+    G64 = np.asarray(Gamma, np.float64)
+    dEmb = np.zeros_like(s64[0])
+    dF = np.zeros_like(f64)
+    dW = np.zeros((N * S, W64.shape[-1]))
+    dG = np.zeros_like(dW)
+    for k in range(N * S):
+        n, j = divmod(k, S)
+        srcs = [s64[m] for m in range(n + 1)]
+        if j >= 1:
+            srcs.append(np.sum(f64[n * S:k], axis=0))
+        dV, dW[k], dG[k] = read_bwd(srcs, W64[k], G64[k], eps, g[k])
+        dEmb += dV[0]
+        for m in range(1, n + 1):
+            dF[(m - 1) * S:m * S] += dV[m]
+        if j >= 1:
+            dF[n * S:k] += dV[n + 1]
+    return dEmb, dF, dW, dG
 
 
 def _slices(V, n):

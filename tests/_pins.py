@@ -416,6 +416,63 @@ def pin_bwd_permutation(orc):
     _close(pg, dg, 1e-12, "permuted dgamma")
 
 
+def _block_bwd_case(seed, N, S, T, d, eps):
+    rng = _rng(seed)
+    emb = rng.normal(size=(T, d))
+    F = rng.normal(size=(N * S, T, d))
+    W = 0.7 * rng.normal(size=(N * S, d))
+    G = 1 + 0.3 * rng.normal(size=(N * S, d))
+    dOut = rng.normal(size=(N * S, T, d))
+    Src = np.stack([emb] + [F[(m - 1) * S:m * S].sum(axis=0) for m in range(1, N)])
+    return emb, F, W, G, dOut, Src, eps
+
+
+def pin_block_bwd_finite_differences(orc):
+    """Block pass gradients against central differences of the C oracle's
+    forward Block pass (summaries and running sums as exact sums of F):
+    L = sum_k <dOut_k, out_k>, step 1e-6, fp64."""
+    N, S = 2, 3
+    emb, F, W, G, dOut, Src, eps = _block_bwd_case(55, N, S, 2, 3, 0.05)
+    dEmb, dF, dW, dG = orc.block_pass_bwd(Src, F, N, S, W, G, eps, dOut)
+    h = 1e-6
+
+    def loss(e_, F_, W_, G_):
+        return float(np.sum(orc.block_pass(e_, F_, N, S, W_, G_, eps) * dOut))
+
+    def fd(x, f):
+        out = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            out[idx] = (f(xp) - f(xm)) / (2 * h)
+        return out
+
+    _close(dEmb, fd(emb, lambda x: loss(x, F, W, G)), 1e-7, "block dEmb vs finite differences")
+    _close(dF, fd(F, lambda x: loss(emb, x, W, G)), 1e-7, "block dF vs finite differences")
+    _close(dW, fd(W, lambda x: loss(emb, F, x, G)), 1e-7, "block dW vs finite differences")
+    _close(dG, fd(G, lambda x: loss(emb, F, W, x)), 1e-7, "block dGamma vs finite differences")
+
+
+def pin_block_bwd_s1_is_full_pass_bwd(orc):
+    """With S = 1 the Block pass is the Full pass over [emb, f_0, f_1, ...]
+    (each summary is one output, no running sum), so its gradients are the
+    sums of the Full reads' gradients."""
+    L = 4
+    emb, F, W, G, dOut, Src, eps = _block_bwd_case(56, L, 1, 3, 4, 1e-6)
+    dEmb, dF, dW, dG = orc.block_pass_bwd(Src, F, L, 1, W, G, eps, dOut)
+    V = np.concatenate([emb[None], F])
+    ref = np.zeros_like(V)
+    for k in range(L):
+        dV, dw, dg = orc.read_bwd(list(V[:k + 1]), W[k], G[k], eps, dOut[k])
+        ref[:k + 1] += dV
+        _close(dW[k], dw, 1e-13, f"S=1 dW[{k}]")
+        _close(dG[k], dg, 1e-13, f"S=1 dGamma[{k}]")
+    _close(dEmb, ref[0], 1e-13, "S=1 dEmb")
+    _close(dF[:L - 1], ref[1:L], 1e-13, "S=1 dF")
+    _close(dF[L - 1], np.zeros_like(dF[L - 1]), 0.0, "S=1 dF of the last output (read by none)")
+
+
 ALL_PINS = [
     pin_golden, pin_bf16_widening, pin_zero_query_is_mean, pin_single_source_identity,
     pin_two_sources_logistic, pin_equal_sources, pin_hardmax_limit,
@@ -425,4 +482,5 @@ ALL_PINS = [
     pin_prenorm_scale_invariance, pin_prenorm_of_zero_query_read, pin_bwd_finite_differences,
     pin_bwd_single_source, pin_bwd_equal_sources, pin_bwd_permutation,
     pin_dynamic_query_constant_rows, pin_dynamic_query_per_token, pin_query_projection,
+    pin_block_bwd_finite_differences, pin_block_bwd_s1_is_full_pass_bwd,
 ]

@@ -161,6 +161,45 @@ def test_bwd_mutant_is_caught(kind, monkeypatch, oracle_mod):
     assert _run_pins(oracle), f"backward mutant {kind} passed every pin"
 
 
+def _block_bwd_mutant(kind):
+    def block_pass_bwd(Src, F, N, S, W, Gamma, eps, dOut):
+        s64 = [np.asarray(Src[i], np.float64) for i in range(N)]
+        f64 = np.asarray(F, np.float64)
+        g = np.asarray(dOut, np.float64)
+        dEmb = np.zeros_like(s64[0])
+        dF = np.zeros_like(f64)
+        dW = np.zeros((N * S, np.asarray(W).shape[-1]))
+        dG = np.zeros_like(dW)
+        for k in range(N * S):
+            n, j = divmod(k, S)
+            srcs = [s64[m] for m in range(n + 1)]
+            if j >= 1:
+                srcs.append(np.sum(f64[n * S:k], axis=0))
+            dV, dW[k], dG[k] = oracle.read_bwd(srcs, np.asarray(W[k], np.float64), np.asarray(Gamma[k], np.float64),
+                                               eps, g[k])
+            if kind != "embedding_grad_dropped":
+                dEmb += dV[0]
+            for m in range(1, n + 1):
+                if kind == "summary_to_first_member":
+                    dF[(m - 1) * S] += dV[m]
+                elif kind == "summary_to_next_block":
+                    dF[m * S:(m + 1) * S] += dV[m]
+                else:
+                    dF[(m - 1) * S:m * S] += dV[m]
+            if j >= 1 and kind != "running_sum_grad_dropped":
+                hi = k + 1 if kind == "running_sum_includes_current" else k
+                dF[n * S:hi] += dV[n + 1]
+        return dEmb, dF, dW, dG
+    return block_pass_bwd
+
+
+@pytest.mark.parametrize("kind", ["embedding_grad_dropped", "summary_to_first_member", "summary_to_next_block",
+                                  "running_sum_grad_dropped", "running_sum_includes_current"])
+def test_block_bwd_mutant_is_caught(kind, monkeypatch, oracle_mod):
+    monkeypatch.setattr(oracle, "block_pass_bwd", _block_bwd_mutant(kind))
+    assert _run_pins(oracle), f"Block backward mutant {kind} passed every pin"
+
+
 def _dynq_mutant(kind):
     def read_dynamic_query(sources, Q, gamma, eps):
         V = np.stack([np.asarray(s, np.float64) if isinstance(s, np.ndarray) else oracle.widen(s)
