@@ -7,6 +7,8 @@ Python under the same names.
 from .binding import (  # noqa: F401
     AttnResError,
     attnres_abi_version,
+    attnres_block_bwd,
+    attnres_block_bwd_scratch_floats,
     attnres_block_merge,
     attnres_block_merge_prenorm,
     attnres_block_pass,

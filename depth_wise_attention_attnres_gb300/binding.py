@@ -40,6 +40,9 @@ _SIGNATURES = {
     "attnres_full_fwd_dynq": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _I32, _VP],
     "attnres_full_bwd": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _I32, _VP, _I64, _VP, _VP,
                          _VP],
+    "attnres_block_bwd": [_VP, _I64, _VP, _I64, _I32, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _I64, _I32,
+                          _VP, _VP, _I64, _VP, _VP, _VP, _I64, _VP],
+    "attnres_block_bwd_scratch_floats": [_I32, _I32, _I64, _I32],
     "attnres_block_stage1": [_VP, _I64, _I32, _I64, _I32, _I32, _VP, _VP, _I32, _F,
                              ctypes.POINTER(_VP), _VP, _VP],
     "attnres_block_merge": [_VP, _VP, _VP, _VP, _I32, _VP, _VP, _F, _I64, _I32, _I32, _VP, _VP],
@@ -83,7 +86,8 @@ def lib() -> ctypes.CDLL:
             for name, args in _SIGNATURES.items():
                 fn = getattr(handle, name)
                 fn.argtypes = args
-                fn.restype = ctypes.c_char_p if name == "attnres_status_string" else ctypes.c_int
+                fn.restype = (ctypes.c_char_p if name == "attnres_status_string" else
+                              ctypes.c_int64 if name == "attnres_block_bwd_scratch_floats" else ctypes.c_int)
             _lib = handle
     return _lib
 
@@ -226,6 +230,42 @@ def attnres_full_bwd(V: torch.Tensor, n_src: int, w: torch.Tensor, gamma: torch.
         _ptr(V), stride, n_src, T, d, _dtype(V), _ptr(w), _ptr(gamma), eps, _ptr(dz), _dtype(dz),
         _ptr(dV), dstride, _ptr(dw), _ptr(dgamma), _stream(stream)))
     return dV
+
+
+def attnres_block_bwd_scratch_floats(N: int, S: int, T: int, d: int) -> int:
+    """fp32 scratch elements attnres_block_bwd needs."""
+    return int(lib().attnres_block_bwd_scratch_floats(N, S, T, d))
+
+
+def attnres_block_bwd(Src: torch.Tensor, F: torch.Tensor, N: int, S: int, W: torch.Tensor, Gamma: torch.Tensor,
+                      eps: float, dOut: torch.Tensor, dEmb: torch.Tensor, dF: torch.Tensor,
+                      dW: torch.Tensor | None = None, dGamma: torch.Tensor | None = None,
+                      scratch: torch.Tensor | None = None, stream=None) -> None:
+    """Backward of a Block pass: ADD dL/d(embedding) into dEmb (fp32 [T, d]), dL/dF
+    into dF (fp32 [N*S, T, d]) and dL/dW, dL/dGamma into dW, dGamma (fp32 [N*S, d]),
+    given dOut = dL/dout [N*S, T, d]. Src holds the embedding and the frozen block
+    summaries the forward left (Src[0 .. N-1]). scratch: fp32, at least
+    attnres_block_bwd_scratch_floats(N, S, T, d) elements (allocated here if None)."""
+    _, T, d, fstride = _slices(F)
+    _, _, _, sstride = _slices(Src)
+    _, _, _, zstride = _slices(dOut)
+    dn, dT, dd, dfstride = _slices(dF)
+    if (dT, dd) != (T, d) or dn < N * S or dF.dtype != torch.float32:
+        raise ValueError("dF must be fp32 [N*S, T, d]")
+    if _rows(dEmb) != (T, d) or dEmb.dtype != torch.float32:
+        raise ValueError("dEmb must be fp32 [T, d]")
+    for t in (dW, dGamma):
+        if t is not None and (t.dtype != torch.float32 or t.numel() != N * S * d or not t.is_contiguous()):
+            raise ValueError("dW and dGamma must be contiguous fp32 [N*S, d]")
+    need = attnres_block_bwd_scratch_floats(N, S, T, d)
+    if scratch is None:
+        scratch = torch.empty(need, device=F.device, dtype=torch.float32)
+    if scratch.dtype != torch.float32 or scratch.numel() < need:
+        raise ValueError(f"scratch must be fp32 with at least {need} elements")
+    _check("attnres_block_bwd", lib().attnres_block_bwd(
+        _ptr(Src), sstride, _ptr(F), fstride, N, S, T, d, _dtype(F), _ptr(W), _ptr(Gamma), eps, _ptr(dOut),
+        zstride, _dtype(dOut), _ptr(dEmb), _ptr(dF), dfstride, _ptr(dW), _ptr(dGamma), _ptr(scratch),
+        scratch.numel(), _stream(stream)))
 
 
 def attnres_query_projection(H: torch.Tensor, Wq: torch.Tensor, Q: torch.Tensor, stream=None) -> torch.Tensor:

@@ -22,7 +22,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libattnres.so")
 
 SOURCES = ["api.cu", "full_fwd.cu", "stage1.cu", "merge.cu", "generic.cu", "noalloc.cu",
-           "stage1_tc.cu", "full_bwd.cu", "proj.cu", "dsplit.cu"]
+           "stage1_tc.cu", "full_bwd.cu", "proj.cu", "dsplit.cu", "block_bwd.cu"]
 HEADERS = ["common.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

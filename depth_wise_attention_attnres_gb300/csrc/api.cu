@@ -416,6 +416,92 @@ int attnres_full_bwd(const void* V, int64_t src_stride, int32_t n_src, int64_t T
   return status_of(launch_full_bwd(a, as_stream(stream), fast));
 }
 
+int64_t attnres_block_bwd_scratch_floats(int32_t N, int32_t S, int64_t T, int32_t d) {
+  if (N < 1 || S < 1 || T < 0 || d < 1) return -1;
+  return (2 * static_cast<int64_t>(N + 1) + S + 1) * T * d;
+}
+
+int attnres_block_bwd(const void* Src, int64_t src_stride, const void* F, int64_t f_stride, int32_t N, int32_t S,
+                      int64_t T, int32_t d, int32_t dtype, const float* W, const float* Gamma, float eps,
+                      const void* dOut, int64_t dout_stride, int32_t dout_dtype, float* dEmb, float* dF,
+                      int64_t df_stride, float* dW, float* dGamma, float* scratch, int64_t scratch_floats,
+                      void* stream) {
+  if (N < 1 || S < 1 || d < 1 || T < 0 || !valid_dtype(dtype) || !valid_dtype(dout_dtype) || !valid_eps(eps))
+    return ATTNRES_ERR_INVALID_ARG;
+  if (T == 0) return ATTNRES_OK;
+  if (!Src || !F || !W || !Gamma || !dOut || !dEmb || !dF || !scratch) return ATTNRES_ERR_INVALID_ARG;
+  const int64_t E = T * d;
+  const int64_t L = static_cast<int64_t>(N) * S;
+  if ((N > 1 && src_stride < E) || (L > 1 && (f_stride < E || dout_stride < E || df_stride < E)))
+    return ATTNRES_ERR_INVALID_ARG;
+  if (scratch_floats < attnres_block_bwd_scratch_floats(N, S, T, d)) return ATTNRES_ERR_INVALID_ARG;
+  const int es = elem_size(dtype);
+  const Range rS = range_of(Src, ((N - 1) * (N > 1 ? src_stride : 0) + E) * es);
+  const Range rF = range_of(F, ((L - 1) * (L > 1 ? f_stride : 0) + E) * es);
+  const Range rZ = range_of(dOut, ((L - 1) * (L > 1 ? dout_stride : 0) + E) * elem_size(dout_dtype));
+  const Range rE = range_of(dEmb, E * 4);
+  const Range rD = range_of(dF, ((L - 1) * (L > 1 ? df_stride : 0) + E) * 4);
+  const Range rW = dW ? range_of(dW, L * d * 4) : Range{};
+  const Range rG = dGamma ? range_of(dGamma, L * d * 4) : Range{};
+  const Range rX = range_of(scratch, attnres_block_bwd_scratch_floats(N, S, T, d) * 4);
+  const Range rq = range_of(W, L * d * 4), rk = range_of(Gamma, L * d * 4);
+  const Range outs[] = {rE, rD, rW, rG, rX};
+  const Range ins[] = {rS, rF, rZ, rq, rk};
+  for (int i = 0; i < 5; ++i) {
+    for (int j = 0; j < 5; ++j)
+      if (overlap(outs[i], ins[j])) return ATTNRES_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 5; ++j)
+      if (overlap(outs[i], outs[j])) return ATTNRES_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = as_stream(stream);
+  // Scratch: fp32 sources Vs [N + 1][E] (embedding, b_1 .. b_{N-1}, and the
+  // slot after block n's sources that holds its running sum), their
+  // gradients dVs [N + 1][E], the running sums Ps [S][E] (Ps[j] = P of the
+  // block's sublayer j), and G [E], the running sum's gradient over the later
+  // reads of the block.
+  float* Vs = scratch;
+  float* dVs = Vs + (N + 1) * E;
+  float* Ps = dVs + (N + 1) * E;
+  float* G = Ps + static_cast<int64_t>(S) * E;
+  const char* Fb = static_cast<const char*>(F);
+  const char* Zb = static_cast<const char*>(dOut);
+  const int is_bf16 = dtype == ATTNRES_BF16;
+  if (cudaMemsetAsync(dVs, 0, (N + 1) * E * 4, s) != cudaSuccess) return ATTNRES_ERR_CUDA;
+  int st = status_of(launch_widen_rows(Src, N > 1 ? src_stride : 0, is_bf16, Vs, N, E, s));
+  if (st != ATTNRES_OK) return st;
+  for (int32_t n = N - 1; n >= 0; --n) {
+    const int64_t k0 = static_cast<int64_t>(n) * S;
+    // The gradient of b_{n+1}, complete now that every later block is done,
+    // goes to each member of block n; its slot then holds block n's running sum.
+    if (n + 1 < N) {
+      st = status_of(launch_spread(dF + k0 * df_stride, df_stride, S, dVs + (n + 1) * E, E, s));
+      if (st != ATTNRES_OK) return st;
+      if (cudaMemsetAsync(dVs + (n + 1) * E, 0, E * 4, s) != cudaSuccess) return ATTNRES_ERR_CUDA;
+    }
+    // Running sums as the forward formed them: P_1 = f_{k0}, P_j = P_{j-1} + f_{k0+j-1}.
+    for (int32_t j = 1; j < S; ++j) {
+      st = status_of(launch_psum(Ps + j * E, j == 1 ? nullptr : Ps + (j - 1) * E, Fb + (k0 + j - 1) * f_stride * es,
+                                 is_bf16, E, s));
+      if (st != ATTNRES_OK) return st;
+    }
+    if (cudaMemsetAsync(G, 0, E * 4, s) != cudaSuccess) return ATTNRES_ERR_CUDA;
+    for (int32_t j = S - 1; j >= 0; --j) {
+      const int64_t k = k0 + j;
+      if (j >= 1 && cudaMemcpyAsync(Vs + (n + 1) * E, Ps + j * E, E * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return ATTNRES_ERR_CUDA;
+      st = attnres_full_bwd(Vs, E, n + 1 + (j >= 1 ? 1 : 0), T, d, ATTNRES_F32, W + k * d, Gamma + k * d, eps,
+                            Zb + k * dout_stride * elem_size(dout_dtype), dout_dtype, dVs, E,
+                            dW ? dW + k * d : nullptr, dGamma ? dGamma + k * d : nullptr, stream);
+      if (st != ATTNRES_OK) return st;
+      if (j >= 1) {
+        st = status_of(launch_gupdate(G, dVs + (n + 1) * E, dF + (k - 1) * df_stride, E, s));
+        if (st != ATTNRES_OK) return st;
+      }
+    }
+  }
+  return status_of(launch_spread(dEmb, 0, 1, dVs, E, s));
+}
+
 // Shared checks of the two d-split calls: the shard's sources and queries.
 int make_dsplit(const void* Src, int64_t src_stride, int32_t n_src, int64_t T, int32_t d_shard, int32_t d_total,
                 int32_t dtype, const float* W, const float* Gamma, int32_t S, float eps, float* partials,

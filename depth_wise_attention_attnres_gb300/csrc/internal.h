@@ -158,6 +158,12 @@ cudaError_t launch_dsplit_partials(const DsplitArgs& a, cudaStream_t s);
 cudaError_t launch_dsplit_finish(const DsplitArgs& a, cudaStream_t s);
 cudaError_t take_timeout_dsplit(unsigned int* flag);
 cudaError_t launch_full_bwd(const BwdArgs& a, cudaStream_t s, bool fast);
+// Block pass backward helpers (block_bwd.cu); E elements per row, fp32 rows E apart.
+cudaError_t launch_widen_rows(const void* src, int64_t src_stride, int is_bf16, float* dst, int R, int64_t E,
+                              cudaStream_t s);
+cudaError_t launch_psum(float* dst, const float* prev, const void* f, int is_bf16, int64_t E, cudaStream_t s);
+cudaError_t launch_gupdate(float* G, float* ds, float* dfp, int64_t E, cudaStream_t s);
+cudaError_t launch_spread(float* dst, int64_t dst_stride, int R, const float* g, int64_t E, cudaStream_t s);
 cudaError_t take_timeout_bwd(unsigned int* flag);
 
 // Device-side timeout records of each kernel file: read and clear (blocking).

@@ -202,6 +202,41 @@ int attnres_full_bwd(const void* V, int64_t src_stride, int32_t n_src, int64_t T
                      float* dgamma, void* stream);
 
 /*
+ * attnres_block_bwd - gradients of a whole Block pass (the pass of
+ * attnres_block_pass) with respect to the embedding, every sublayer output,
+ * and every read's query and key gain, given dL/dout_k for every sublayer k.
+ * Block AttnRes (DepthBench reading notes section 2.5; LLMRes blog, "Block
+ * Attention Residuals"): sublayer k = n * S + j reads {embedding, b_1 .. b_n,
+ * P_k if j >= 1}, with b_m the plain sum of block (m-1)'s outputs and P_k the
+ * sum of block n's outputs before k. By the chain rule the gradient of b_m
+ * reaches every member of block m-1 unchanged and that of P_k every output of
+ * block n before k. The reads run in reverse order through the Full read's
+ * backward (attnres_full_bwd) over fp32 copies of their sources, with the
+ * running sums rebuilt by the same fp32 additions the forward made.
+ *
+ *   Src       device, [N][T][d] dtype, rows src_stride apart: Src[0] the
+ *             embedding, Src[m] the frozen summary b_m (as the forward pass
+ *             left them); row N (if any) is not read.
+ *   F         device, [N*S][T][d] dtype: the sublayer outputs, f_stride apart.
+ *   W, Gamma  device, fp32 [N*S][d]: each read's query and key gain.
+ *   dOut      device, [N*S][T][d] dout_dtype: dL/dout_k, dout_stride apart.
+ *   dEmb      device, fp32 [T][d], +=.
+ *   dF        device, fp32 [N*S][T][d], +=, df_stride apart.
+ *   dW, dGamma device, fp32 [N*S][d], +=; may be NULL.
+ *   scratch   device, fp32, at least attnres_block_bwd_scratch_floats(N, S,
+ *             T, d) floats (the caller's; contents on return unspecified).
+ * Returns ATTNRES_ERR_INVALID_ARG for bad sizes, strides, a short scratch or
+ * outputs overlapping inputs or each other; launch errors as ATTNRES_ERR_CUDA.
+ */
+int attnres_block_bwd(const void* Src, int64_t src_stride, const void* F, int64_t f_stride, int32_t N,
+                      int32_t S, int64_t T, int32_t d, int32_t dtype, const float* W, const float* Gamma,
+                      float eps, const void* dOut, int64_t dout_stride, int32_t dout_dtype, float* dEmb,
+                      float* dF, int64_t df_stride, float* dW, float* dGamma, float* scratch,
+                      int64_t scratch_floats, void* stream);
+/* Scratch attnres_block_bwd needs: (2 (N + 1) + S + 1) * T * d floats; -1 for bad sizes. */
+int64_t attnres_block_bwd_scratch_floats(int32_t N, int32_t S, int64_t T, int32_t d);
+
+/*
  * attnres_block_stage1 - stage 1 of the two-stage Block AttnRes computation
  * (datacamp explainer, "two-stage computation"): the S pseudo-queries of one
  * block against the cross-block sources, each source row read once for all S.

@@ -115,6 +115,28 @@ def test_full_bwd_validation(lib):
     assert lib.attnres_full_bwd(*(ok[:3] + (0,) + ok[4:]), None) == 0  # T = 0
 
 
+def test_block_bwd_validation(lib):
+    need = (2 * 3 + 2 + 1) * 64
+    assert lib.attnres_block_bwd_scratch_floats(2, 2, 4, 16) == need
+    assert lib.attnres_block_bwd_scratch_floats(0, 2, 4, 16) == -1
+    # (Src, src_stride, F, f_stride, N, S, T, d, dtype, W, Gamma, eps, dOut, dout_stride, dout_dtype,
+    #  dEmb, dF, df_stride, dW, dGamma, scratch, scratch_floats)
+    ok = (P, 64, 2 * P, 64, 2, 2, 4, 16, 1, 3 * P, 4 * P, 1e-6, 5 * P, 64, 1, 6 * P, 7 * P, 64, 8 * P, 9 * P,
+          10 * P, need)
+    bad = [
+        ok[:4] + (0,) + ok[5:],                          # N = 0
+        ok[:21] + (need - 1,),                           # scratch too short
+        ok[:16] + (2 * P + 8,) + ok[17:],                # dF overlaps F
+        ok[:20] + (6 * P + 16,) + ok[21:],               # scratch overlaps dEmb
+        ok[:14] + (9,) + ok[15:],                        # bad dOut dtype
+        ok[:17] + (63,) + ok[18:],                       # df_stride < T*d
+        ok[:15] + (None,) + ok[16:],                     # no dEmb
+    ]
+    for args in bad:
+        assert lib.attnres_block_bwd(*args, None) == INVALID, args
+    assert lib.attnres_block_bwd(*(ok[:6] + (0,) + ok[7:]), None) == 0  # T = 0
+
+
 def test_dynamic_query_validation(lib):
     # projection: fp32 H unsupported, Q overlapping H, null Wq, T = 0
     assert lib.attnres_query_projection(P, 4, 16, 0, 2 * P, 3 * P, None) == UNSUPPORTED
