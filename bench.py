@@ -67,6 +67,33 @@ def block_pass_bytes(N: int, S: int, T: int, d: int, es: int, freeze_last: bool 
 DSPLIT_SHARDS = 4
 
 
+def block_bwd_bytes(N: int, S: int, T: int, d: int, es: int) -> dict:
+    """Algorithmic bytes of the Block pass backward as attnres_block_bwd runs it.
+
+    Per read k = nS + j over n_src = n + 1 (+ 1 for the running sum when j >= 1)
+    fp32 sources: the read backward moves n_src rows (read) and their fp32
+    gradient rows (read and written) and dL/dout_k ("read"); with j >= 1 the
+    running sum is copied into its source slot and its gradient routed (G,
+    the slot and dF_{k-1} read and written: "route"). Per block: the running
+    sums rebuilt, and the gradient of the block's summary added to its S
+    members ("route"). Once: the sources widened to fp32 and their gradients
+    zeroed; the embedding's gradient added at the end ("route").
+    """
+    E = T * d
+    read = route = 0
+    for n in range(N):
+        for j in range(S):
+            n_src = n + 1 + (1 if j >= 1 else 0)
+            read += n_src * E * (4 + 8) + E * es
+            if j >= 1:
+                route += 8 * E + 24 * E
+        route += E * (es + 4) + max(S - 2, 0) * E * (4 + es + 4) + 4 * E  # running sums, G zeroed
+        if n + 1 < N:
+            route += 4 * E + S * 8 * E + 4 * E
+    route += (N + 1) * 4 * E + N * E * (es + 4) + 12 * E
+    return {"read": read, "route": route, "total": read + route}
+
+
 def dsplit_stage1_bytes(N: int, S: int, T: int, d: int, es: int, P: int) -> dict:
     """Algorithmic bytes of the Block pass's N stage-1 reads taken as a d-split
     over P feature shards. Block n (n+1 sources): the partials kernels read
@@ -346,6 +373,38 @@ class DsplitStep:
             self.finish(n)
 
 
+class BlockBwdStep:
+    """The Block pass backward: the forward pass runs once at set-up (its
+    frozen summaries are what the backward reads); a step is one
+    attnres_block_bwd over all N*S reads with seeded dL/dout."""
+
+    def __init__(self, wl, dev):
+        from depth_wise_attention_attnres_gb300 import binding
+        self.ar = binding
+        self.wl = wl
+        fwd = BlockPassStep(wl, dev)
+        fwd()
+        self.Src, self.F, self.W, self.G = fwd.Src, fwd.F, fwd.W, fwd.G
+        del fwd
+        torch.cuda.empty_cache()
+        g = inputs.generator(wl.seed + 4, dev)
+        self.dOut = inputs.randn((wl.N * wl.S, wl.T, wl.d), wl.dtype, g, dev)
+        self.dEmb = torch.zeros(wl.T, wl.d, device=dev)
+        self.dF = torch.zeros(wl.N * wl.S, wl.T, wl.d, device=dev)
+        self.dW = torch.zeros(wl.N * wl.S, wl.d, device=dev)
+        self.dGamma = torch.zeros(wl.N * wl.S, wl.d, device=dev)
+        self.scratch = torch.empty(binding.attnres_block_bwd_scratch_floats(wl.N, wl.S, wl.T, wl.d), device=dev)
+        L = wl.N * wl.S
+        self.launches = L + (L - wl.N) + wl.N * max(wl.S - 1, 0) + (wl.N - 1) + 2
+        es = 2 if wl.dtype == "bf16" else 4
+        self.byte_parts = block_bwd_bytes(wl.N, wl.S, wl.T, wl.d, es)
+        self.bytes = self.byte_parts["total"]
+
+    def __call__(self):
+        self.ar.attnres_block_bwd(self.Src, self.F, self.wl.N, self.wl.S, self.W, self.G, self.wl.eps, self.dOut,
+                                  self.dEmb, self.dF, self.dW, self.dGamma, self.scratch)
+
+
 def time_dsplit_kernels(step, reps, stream):
     """Device time of the partials and finish launches of a d-split step."""
     acc = {"partials": 0.0, "finish": 0.0}
@@ -373,6 +432,8 @@ def make_step(name, dev, op="read"):
         return FullPassStep(wl, dev, op)
     if wl.kind == "block_pass" and op == "dsplit":
         return DsplitStep(wl, dev)
+    if wl.kind == "block_pass" and op == "bwd":
+        return BlockBwdStep(wl, dev)
     if op != "read":
         raise ValueError("--op applies to Full-pass workloads (dsplit: Block-pass workloads)")
     if wl.kind == "block_pass":
@@ -626,6 +687,15 @@ def ours(args):
             "per_launch_bytes": step.bytes / step.launches,
             "note": "the step is R launches of this one kernel back to back in a CUDA graph; "
                     "average launch duration = step time / R (gaps included)"}
+    elif isinstance(step, BlockBwdStep):
+        g = step.byte_parts["total"] / (ms / 1e3) / 1e9
+        line["roofline"] = {
+            "kernel": "full_bwd_bulk_kernel", "bound": "hbm", "achieved": g, "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": g / peaks["hbm_gbs"], "frac_of_nominal_8000": g / NOMINAL_HBM_GBS,
+            "peak_source": peaks["source"], "traffic": None,
+            "byte_parts": step.byte_parts,
+            "note": "whole step: the per-read backward launches carry "
+                    f"{step.byte_parts['read'] / step.byte_parts['total']:.0%} of the algorithmic bytes"}
     elif isinstance(step, DsplitStep):
         times = time_dsplit_kernels(step, 3, stream)
         parts = step.byte_parts
@@ -723,7 +793,7 @@ def main():
                    help="Full pass: plain reads, reads emitting the sublayer pre-norm instead of "
                         "their result, or both, the pass backward (dV, dW, dGamma), or reads with "
                         "input-dependent queries (projection + read). Block pass: dsplit, the stage-1 "
-                        "reads with the features split over 4 shards")
+                        "reads with the features split over 4 shards; bwd, the pass backward")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-block", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")

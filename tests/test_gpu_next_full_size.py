@@ -95,3 +95,17 @@ def test_dsplit_stage1_full_size_sampled():
         got = torch.cat([step.outs[p][j][rows] for p in range(step.P)], dim=1)
         assert rel_err(got, refO[j]) <= TOL["bf16"], f"O[{j}]"
     assert float(np.max(np.abs(step.lse[:, rows].cpu().double().numpy() - refL))) <= 1e-4
+
+
+def test_block_pass_backward_full_size_sampled():
+    """The Block pass backward (`--op bwd` on the Block workload): dEmb and dF on
+    sampled token rows (the forward's frozen summaries as the sources)."""
+    step = bench.make_step(BLOCK, dev(), "bwd")
+    _run(step)
+    wl = step.wl
+    rows = inputs.sample_rows(wl.T, 24).to(dev())
+    rE, rF, _, _ = oracle.block_pass_bwd(step.Src[:, rows, :].cpu(), step.F[:, rows, :].cpu(), wl.N, wl.S,
+                                         step.W.cpu().double().numpy(), step.G.cpu().double().numpy(), wl.eps,
+                                         step.dOut[:, rows, :].cpu())
+    assert rel_err(step.dEmb[rows], rE) <= TOL["f32"]
+    assert rel_err(step.dF[:, rows, :], rF) <= TOL["f32"]
