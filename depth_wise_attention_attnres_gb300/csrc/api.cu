@@ -661,9 +661,15 @@ int attnres_block_pass(const void* F, int64_t f_stride, int32_t N, int32_t S, in
     if (st != ATTNRES_OK) return st;
     // Stage 2: fold the running sum in, one sublayer at a time.
     for (int j = 1; j < S; ++j) {
-      st = attnres_block_merge(O[j], lse_scratch + j * T, P_scratch, Fb + (k0 + j - 1) * f_stride * es,
-                               j == 1, W + (k0 + j) * d, Gamma + (k0 + j) * d, eps, T, d, dtype,
-                               outb + (k0 + j) * out_stride * es, stream);
+      MergeArgs m{};
+      st = make_merge(O[j], lse_scratch + j * T, P_scratch, Fb + (k0 + j - 1) * f_stride * es, j == 1,
+                      W + (k0 + j) * d, Gamma + (k0 + j) * d, eps, T, d, dtype, outb + (k0 + j) * out_stride * es,
+                      &m);
+      if (st != ATTNRES_OK) return st;
+      // The merge before this one writes neither O[j] nor f; stage 1 (before
+      // merge 1) writes O[j].
+      m.early = j >= 2;
+      st = status_of(launch_merge(m, as_stream(stream), merge_fast_ok(m)));
       if (st != ATTNRES_OK) return st;
     }
     // Freeze the block summary b_{n+1} = P + f_last into Src[n + 1].

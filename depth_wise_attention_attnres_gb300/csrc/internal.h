@@ -74,6 +74,10 @@ struct MergeArgs {
   int bf16;
   void* out;            // may be nullptr when pre.gamma is set
   PreNorm pre;
+  // Fetch the first tiles of O_j and f before waiting for the previous
+  // kernel: only when that kernel writes neither (in a Block pass, the merge
+  // before, never stage 1, which writes O_j).
+  int early;
 };
 
 // Backward of one read (full_bwd.cu): dV, dw, dgamma accumulated in fp32.

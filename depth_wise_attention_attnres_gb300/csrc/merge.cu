@@ -92,7 +92,6 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
   const int R = static_cast<int>(r1 - r0);
   const int ntiles = (R + TM - 1) / TM;
 
-  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMStages; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
@@ -101,7 +100,6 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
     mbar_fence_init();
   }
   __syncthreads();
-  pdl_wait();
 
   if (warp == kMNW) {
     // ------------------------------------------------------------ producer
@@ -110,7 +108,32 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
     uint32_t phase = 0;
     int issued = 0;
     bool ok = true;
-    for (int t = 0; t < ntiles; ++t) {
+    // With a.early the first stages' O_j and f rows (which no kernel still
+    // running writes) are fetched before the previous kernel has finished;
+    // their P rows, which it writes, after.
+    const int t_pre = a.early ? min(kMStages, ntiles) : 0;
+    for (int t = 0; t < t_pre; ++t) {
+      const int64_t row0 = r0 + static_cast<int64_t>(t) * R / ntiles;
+      const uint32_t rows = static_cast<uint32_t>(r0 + static_cast<int64_t>(t + 1) * R / ntiles - row0);
+      unsigned char* st = stages + static_cast<size_t>(t) * g.stage_bytes;
+      const uint32_t fb = smem_u32(&full_bar[t]);
+      mbar_arrive_expect_tx(fb, rows * (row_t + (with_f ? row_t : 0u) + (with_p ? row_p : 0u)));
+      bulk_g2s(smem_u32(st), static_cast<const T*>(a.O) + row0 * d, rows * row_t, fb);
+      if (with_f)
+        bulk_g2s(smem_u32(st + TM * row_t), static_cast<const T*>(a.f) + row0 * d, rows * row_t, fb);
+    }
+    pdl_wait();
+    pdl_trigger();
+    for (int t = 0; t < t_pre; ++t) {
+      const int64_t row0 = r0 + static_cast<int64_t>(t) * R / ntiles;
+      const uint32_t rows = static_cast<uint32_t>(r0 + static_cast<int64_t>(t + 1) * R / ntiles - row0);
+      unsigned char* st = stages + static_cast<size_t>(t) * g.stage_bytes;
+      if (with_p) bulk_g2s(smem_u32(st + 2 * TM * row_t), a.P + row0 * d, rows * row_p, smem_u32(&full_bar[t]));
+    }
+    issued = t_pre;
+    s = t_pre % kMStages;
+    phase = t_pre == kMStages ? 1u : 0u;
+    for (int t = t_pre; t < ntiles; ++t) {
       if (!mbar_wait(smem_u32(&empty_bar[s]), phase ^ 1u)) {
         ok = false;
         break;
@@ -139,6 +162,10 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
   }
 
   // -------------------------------------------------------------- consumers
+  // Everything below may read what the previous kernel wrote, and the next
+  // kernel may start once every CTA is past this point.
+  pdl_wait();
+  pdl_trigger();
   for (int i = threadIdx.x; i < d; i += kMNW * 32) {
     wq[i] = a.w[i] * a.gamma[i];
     if constexpr (kPre) gq[i] = a.pre.gamma[i];
