@@ -160,10 +160,10 @@ inline PtGeom ring_geom(int n, int ds, int tab_fixed, int tab_warp) {
 
 inline PtGeom pt_geom(int n, int ds, int NT) { return ring_geom(n, ds, 2 * NT * 8 * tc_pitch(ds) * 2, 0); }
 
-// Per-warp area of the tensor-core finish: bf16 weights [hi, lo][16 queries]
-// [8 NK sources], then the box's partials (at most 16 pairs x 17 floats).
+// Per-warp area of the tensor-core finish: bf16 weights [2 tokens][hi, lo][16
+// queries][8 NK sources], then the box's partials (at most 16 pairs x 17 floats).
 constexpr int kFinPartFloats = 16 * (ATTNRES_MAX_QUERIES + 1);
-__host__ __device__ inline int fin_warp_bytes(int NK) { return 2 * 16 * 8 * NK * 2 + kFinPartFloats * 4; }
+__host__ __device__ inline int fin_warp_bytes(int NK) { return 2 * 2 * 16 * 8 * NK * 2 + kFinPartFloats * 4; }
 inline PtGeom fin_geom(int n, int ds) { return ring_geom(n, ds, 0, fin_warp_bytes((n + 7) / 8)); }
 
 PFN_cuTensorMapEncodeTiled_v12000 dsplit_encode_fn() {
@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(8 * 32, 1)
 // parts, then their lo parts), B = the sources' 8 features (k: the 8 sources,
 // twice), read with ldmatrix.trans from the swizzled box (the 8 source lines
 // of a token are 8 consecutive lines, so their units fall in 8 banks).
-template <int NK, int R>
+template <int NK, int R, int kTT>
 __global__ void __launch_bounds__(8 * 32, 1)
     dsplit_finish_tc_kernel(DsplitArgs a, PtGeom G, const __grid_constant__ CUtensorMap tmap) {
   extern __shared__ __align__(16) unsigned char dsm_raw[];
@@ -413,9 +413,8 @@ __global__ void __launch_bounds__(8 * 32, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
   unsigned char* area = dsm + G.tab_off + warp * fin_warp_bytes(NK);
-  bf16* whi = reinterpret_cast<bf16*>(area);  // [16][np]
-  bf16* wlo = whi + 16 * np;
-  float* part = reinterpret_cast<float*>(area + 2 * 16 * np * 2);
+  bf16* wts = reinterpret_cast<bf16*>(area);  // per token of a pair: hi [16][np], then lo [16][np]
+  float* part = reinterpret_cast<float*>(area + 2 * 2 * 16 * np * 2);
   uint64_t* bars = reinterpret_cast<uint64_t*>(dsm + G.bar_off) + warp * G.nst;
   const uint32_t ring = smem_u32(dsm + static_cast<size_t>(warp) * G.nst * G.stage_bytes);
   const int64_t ntiles = (a.T + G.TM - 1) / G.TM;
@@ -436,7 +435,7 @@ __global__ void __launch_bounds__(8 * 32, 1)
     }
   }
   // Weights of absent queries and sources stay zero.
-  for (int e = lane; e < 2 * 16 * np; e += 32) whi[e] = __float2bfloat16_rn(0.f);
+  for (int e = lane; e < 2 * 2 * 16 * np; e += 32) wts[e] = __float2bfloat16_rn(0.f);
   // The first box's partials (later boxes' are loaded one box ahead).
   constexpr int kPL = (kFinPartFloats + 31) / 32;
   float pv[kPL];
@@ -480,84 +479,116 @@ __global__ void __launch_bounds__(8 * 32, 1)
     }
     __syncwarp();
     const uint32_t box = ring + slot * G.stage_bytes;
-    for (int tm = 0; tm < G.TM; ++tm) {
-      const int64_t t = tile * G.TM + tm;
-      if (t >= a.T) break;
-      // Softmax weights of the token: lane (group, j) takes query j over
+    // kTT tokens of the box at a time (independent work to interleave; with
+    // two, the second repeats the first when the box or T has no second).
+    for (int tm0 = 0; tm0 < G.TM; tm0 += kTT) {
+      const int64_t t0 = tile * G.TM + tm0;
+      if (t0 >= a.T) break;
+      const bool has1 = kTT == 2 && tm0 + 1 < G.TM && t0 + 1 < a.T;
+      const int tmv[2] = {tm0, has1 ? tm0 + 1 : tm0};
+      // Softmax weights of each token: lane (group, j) takes query j over
       // sources group, group + G2, ...; butterflies combine the groups.
-      const float* pt = part + tm * n * (S + 1);
-      float m = -INFINITY, ev[R];
+      float m[2] = {-INFINITY, -INFINITY}, ev[2][R];
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int i = grp + r * G2;
-        ev[r] = -INFINITY;
-        if (jq < S && i < n) {
-          ev[r] = pt[i * (S + 1) + 1 + jq] * rsqrtf(pt[i * (S + 1)] * inv_d + a.eps);
-          m = fmaxf(m, ev[r]);
-        }
-      }
-      for (int o = Q2; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      float z = 0.f;
+      for (int tt = 0; tt < kTT; ++tt) {
+        const float* pt = part + tmv[tt] * n * (S + 1);
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        ev[r] = (jq < S && grp + r * G2 < n) ? __expf(ev[r] - m) : 0.f;
-        z += ev[r];
-      }
-      for (int o = Q2; o < 32; o <<= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-      const float inv = 1.0f / z;
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int i = grp + r * G2;
-        if (jq < S && i < n) {
-          const float w = ev[r] * inv;
-          const bf16 h = __float2bfloat16_rn(w);
-          whi[jq * np + i] = h;
-          wlo[jq * np + i] = __float2bfloat16_rn(w - __bfloat162float(h));
-        }
-      }
-      if (a.lse && grp == 0 && jq < S) a.lse[jq * a.T + t] = m + __logf(z);
-      __syncwarp();
-      uint32_t af[NK][4];
-#pragma unroll
-      for (int kb = 0; kb < NK; ++kb) {
-        af[kb][0] = *reinterpret_cast<const uint32_t*>(whi + g * np + 8 * kb + 2 * q);
-        af[kb][1] = *reinterpret_cast<const uint32_t*>(whi + (g + 8) * np + 8 * kb + 2 * q);
-        af[kb][2] = *reinterpret_cast<const uint32_t*>(wlo + g * np + 8 * kb + 2 * q);
-        af[kb][3] = *reinterpret_cast<const uint32_t*>(wlo + (g + 8) * np + 8 * kb + 2 * q);
-      }
-      // ldmatrix rows: lane l gives source 8 kb + (l & 7) (clamped to a real
-      // one; its weight is zero) of unit 4 uq + (l >> 3).
-      bf16* o0t = o0 + t * ds;
-      bf16* o1t = o1 + t * ds;
-      int Lsrc[NK];
-#pragma unroll
-      for (int kb = 0; kb < NK; ++kb) Lsrc[kb] = tm * n + min(8 * kb + (lane & 7), n - 1);
-      for (int c = 0; c < ds / 64; ++c) {
-        float acc[8][4];
-#pragma unroll
-        for (int kb = 0; kb < NK; ++kb) {
-          const int L = c * G.P + Lsrc[kb];
-          const uint32_t lb = box + L * 128u + ((L & 7) << 4);
-#pragma unroll
-          for (int uq = 0; uq < 2; ++uq) {
-            uint32_t r[4];
-            ldsm_x4_trans(lb ^ (((uq << 2) | (lane >> 3)) << 4), r);
-#pragma unroll
-            for (int mm = 0; mm < 4; ++mm) {
-              if (kb == 0)
-                mma16816_z(acc[uq * 4 + mm], af[kb], r[mm], r[mm]);
-              else
-                mma16816(acc[uq * 4 + mm], af[kb], r[mm], r[mm]);
-            }
+        for (int r = 0; r < R; ++r) {
+          const int i = grp + r * G2;
+          ev[tt][r] = -INFINITY;
+          if (jq < S && i < n) {
+            ev[tt][r] = pt[i * (S + 1) + 1 + jq] * rsqrtf(pt[i * (S + 1)] * inv_d + a.eps);
+            m[tt] = fmaxf(m[tt], ev[tt][r]);
           }
         }
-        // D: query g (and g + 8), features c * 64 + 8u + 2q, + 1.
-        uint32_t* r0 = reinterpret_cast<uint32_t*>(o0t + c * 64 + 2 * q);
-        uint32_t* r1 = reinterpret_cast<uint32_t*>(o1t + c * 64 + 2 * q);
+      }
+      for (int o = Q2; o < 32; o <<= 1) {
+        m[0] = fmaxf(m[0], __shfl_xor_sync(0xffffffffu, m[0], o));
+        if (kTT == 2) m[1] = fmaxf(m[1], __shfl_xor_sync(0xffffffffu, m[1], o));
+      }
+      float z[2] = {0.f, 0.f};
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          if (o0) r0[4 * u] = pack_bf16x2(acc[u][0], acc[u][1]);
-          if (o1) r1[4 * u] = pack_bf16x2(acc[u][2], acc[u][3]);
+      for (int tt = 0; tt < kTT; ++tt)
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          ev[tt][r] = (jq < S && grp + r * G2 < n) ? __expf(ev[tt][r] - m[tt]) : 0.f;
+          z[tt] += ev[tt][r];
+        }
+      for (int o = Q2; o < 32; o <<= 1) {
+        z[0] += __shfl_xor_sync(0xffffffffu, z[0], o);
+        if (kTT == 2) z[1] += __shfl_xor_sync(0xffffffffu, z[1], o);
+      }
+#pragma unroll
+      for (int tt = 0; tt < kTT; ++tt) {
+        const float inv = 1.0f / z[tt];
+        bf16* whi = wts + tt * 2 * 16 * np;
+        bf16* wlo = whi + 16 * np;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const int i = grp + r * G2;
+          if (jq < S && i < n) {
+            const float w = ev[tt][r] * inv;
+            const bf16 h = __float2bfloat16_rn(w);
+            whi[jq * np + i] = h;
+            wlo[jq * np + i] = __float2bfloat16_rn(w - __bfloat162float(h));
+          }
+        }
+        if (a.lse && grp == 0 && jq < S && (tt == 0 || has1)) a.lse[jq * a.T + t0 + tt] = m[tt] + __logf(z[tt]);
+      }
+      __syncwarp();
+      uint32_t af[2][NK][4];
+      int Lsrc[2][NK];
+#pragma unroll
+      for (int tt = 0; tt < kTT; ++tt) {
+        const bf16* whi = wts + tt * 2 * 16 * np;
+        const bf16* wlo = whi + 16 * np;
+#pragma unroll
+        for (int kb = 0; kb < NK; ++kb) {
+          af[tt][kb][0] = *reinterpret_cast<const uint32_t*>(whi + g * np + 8 * kb + 2 * q);
+          af[tt][kb][1] = *reinterpret_cast<const uint32_t*>(whi + (g + 8) * np + 8 * kb + 2 * q);
+          af[tt][kb][2] = *reinterpret_cast<const uint32_t*>(wlo + g * np + 8 * kb + 2 * q);
+          af[tt][kb][3] = *reinterpret_cast<const uint32_t*>(wlo + (g + 8) * np + 8 * kb + 2 * q);
+          // ldmatrix rows: lane l gives source 8 kb + (l & 7) (clamped to a
+          // real one; its weight is zero) of unit 4 uq + (l >> 3).
+          Lsrc[tt][kb] = tmv[tt] * n + min(8 * kb + (lane & 7), n - 1);
+        }
+      }
+      for (int c = 0; c < ds / 64; ++c) {
+        float acc[2][8][4];
+#pragma unroll
+        for (int kb = 0; kb < NK; ++kb) {
+          uint32_t rr[2][2][4];
+#pragma unroll
+          for (int tt = 0; tt < kTT; ++tt) {
+            const int L = c * G.P + Lsrc[tt][kb];
+            const uint32_t lb = box + L * 128u + ((L & 7) << 4);
+#pragma unroll
+            for (int uq = 0; uq < 2; ++uq) ldsm_x4_trans(lb ^ (((uq << 2) | (lane >> 3)) << 4), rr[tt][uq]);
+          }
+#pragma unroll
+          for (int tt = 0; tt < kTT; ++tt)
+#pragma unroll
+            for (int uq = 0; uq < 2; ++uq)
+#pragma unroll
+              for (int mm = 0; mm < 4; ++mm) {
+                if (kb == 0)
+                  mma16816_z(acc[tt][uq * 4 + mm], af[tt][kb], rr[tt][uq][mm], rr[tt][uq][mm]);
+                else
+                  mma16816(acc[tt][uq * 4 + mm], af[tt][kb], rr[tt][uq][mm], rr[tt][uq][mm]);
+              }
+        }
+        // D: query g (and g + 8), features c * 64 + 8u + 2q, + 1.
+#pragma unroll
+        for (int tt = 0; tt < kTT; ++tt) {
+          if (tt == 1 && !has1) break;
+          const int64_t t = t0 + tt;
+          uint32_t* r0 = reinterpret_cast<uint32_t*>(o0 + t * ds + c * 64 + 2 * q);
+          uint32_t* r1 = reinterpret_cast<uint32_t*>(o1 + t * ds + c * 64 + 2 * q);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            if (o0) r0[4 * u] = pack_bf16x2(acc[tt][u][0], acc[tt][u][1]);
+            if (o1) r1[4 * u] = pack_bf16x2(acc[tt][u][2], acc[tt][u][3]);
+          }
         }
       }
       __syncwarp();
@@ -730,7 +761,8 @@ bool finish_on_tensor_cores(const DsplitArgs& a) {
 template <int NK, int R>
 cudaError_t launch_finish_tc(const DsplitArgs& a, cudaStream_t s) {
   const PtGeom g = fin_geom(a.n_src, a.d_shard);
-  auto k = dsplit_finish_tc_kernel<NK, R>;
+  // Boxes of one token (more than 8 sources) take them one at a time.
+  auto k = g.TM >= 2 ? dsplit_finish_tc_kernel<NK, R, 2> : dsplit_finish_tc_kernel<NK, R, 1>;
   cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(k), g.total);
   if (e != cudaSuccess) return e;
   alignas(64) CUtensorMap map;
