@@ -17,8 +17,8 @@
 // Partials are stored token-major, partials[t][i][c] (c = 0: sum v^2, 1 + j:
 // dot_j), so one token's statistics are contiguous.
 // dsplit_partials_tc_kernel (bf16, shard width a multiple of 64): the sources
-// streamed by TMA into per-warp rings, the dots and sum v^2 as tensor-core
-// MMAs over 16-pair tiles.
+// streamed by TMA into a ring shared by up to 15 consumer warps behind one
+// producer warp, the dots and sum v^2 as tensor-core MMAs over 16-pair tiles.
 // dsplit_partials_kernel (the rest): 8 lanes per (token, source) row of the
 // shard (4 rows per warp), w * gamma of the shard in shared memory, sums over
 // the row's lanes with 3 shuffle steps.
@@ -40,6 +40,7 @@ namespace {
 
 constexpr int kDWarps = 8;
 constexpr int kDsplitSmemLimit = 227 * 1024;
+constexpr int kPartMaxWarps = 15;  // consumer warps of the partials (16 warps: 128 registers each)
 
 // bf16 elements per row of the w * gamma tables of the tensor-core partials:
 // a row pitch of 64 mod 128 bytes, so the two rows one 8-lane phase of a
@@ -106,8 +107,8 @@ __global__ void __launch_bounds__(kDWarps * 32) dsplit_partials_kernel(DsplitArg
 }
 
 // bf16 shards whose width is a multiple of 64: the dots on the tensor cores,
-// the sources streamed by TMA. Each warp owns a ring of stages; a stage holds
-// the box {64 features, n sources, TM tokens, d_s / 64 chunks} of TM tokens
+// the sources streamed by TMA. A stage holds the box {64 features, n
+// sources, TM tokens, d_s / 64 chunks} of TM tokens
 // (TM * n = P (token, source) pairs, about 16), stored with the 128-byte
 // swizzle: pair p's features of chunk c form 128-byte line L = c * P + p, and
 // its 16-byte unit u lies at unit u ^ (L & 7) of the line.
@@ -158,7 +159,27 @@ inline PtGeom ring_geom(int n, int ds, int tab_fixed, int tab_warp) {
   return g;
 }
 
-inline PtGeom pt_geom(int n, int ds, int NT) { return ring_geom(n, ds, 2 * NT * 8 * tc_pitch(ds) * 2, 0); }
+// The partials' ring, shared by the CTA's consumer warps behind one producer
+// warp: as many stages as fit; W consumer warps (at most kPartMaxWarps) such
+// that at least 4 boxes are in flight beyond the ones being worked on.
+inline PtGeom pt_geom(int n, int ds, int NT) {
+  PtGeom g{};
+  g.TM = n <= 16 ? 16 / n : 1;
+  g.P = g.TM * n;
+  g.mtiles = (g.P + 15) / 16;
+  g.box_bytes = g.P * ds * 2;
+  g.stage_bytes = (g.box_bytes + 1023) / 1024 * 1024;
+  const int tab = 2 * NT * 8 * tc_pitch(ds) * 2;
+  int nst = (kDsplitSmemLimit - 1024 - tab) / (g.stage_bytes + 16);
+  if (nst > 64) nst = 64;
+  g.nst = nst;
+  g.W = nst - 4 < kPartMaxWarps ? nst - 4 : kPartMaxWarps;
+  g.tab_off = nst * g.stage_bytes;
+  g.bar_off = g.tab_off + tab;
+  g.total = 1024 + g.bar_off + 2 * nst * 8;
+  if (g.W < 1) g.W = 0;
+  return g;
+}
 
 // Per-warp area of the tensor-core finish: bf16 weights [2 tokens][hi, lo][16
 // queries][8 NK sources], then the box's partials (at most 16 pairs x 17 floats).
@@ -216,7 +237,7 @@ __device__ __forceinline__ void red_add(float* p, float v) {
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 template <int NT>
-__global__ void __launch_bounds__(8 * 32, 1)
+__global__ void __launch_bounds__(kPartMaxWarps * 32 + 32, 1)
     dsplit_partials_tc_kernel(DsplitArgs a, PtGeom G, const __grid_constant__ CUtensorMap tmap) {
   extern __shared__ __align__(16) unsigned char dsm_raw[];
   unsigned char* dsm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
@@ -225,31 +246,57 @@ __global__ void __launch_bounds__(8 * 32, 1)
   bf16* whi = reinterpret_cast<bf16*>(dsm + G.tab_off);  // [NT * 8][pitch]
   bf16* wlo = whi + NT * 8 * pitch;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(dsm + G.bar_off) + warp * G.nst;
-  const uint32_t ring = smem_u32(dsm + static_cast<size_t>(warp) * G.nst * G.stage_bytes);
+  const int W = G.W;  // consumer warps; warp W is the producer
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(dsm + G.bar_off);  // [nst]
+  uint64_t* empty_bar = full_bar + G.nst;                              // [nst]
+  const uint32_t ring = smem_u32(dsm);
   const int64_t ntiles = (a.T + G.TM - 1) / G.TM;
-  const int64_t tstride = static_cast<int64_t>(gridDim.x) * G.W;
-  const int64_t first = static_cast<int64_t>(blockIdx.x) * G.W + warp;
+  // This CTA's boxes: tile blockIdx.x + i * gridDim.x for i < nmine; box i
+  // sits in slot i % nst and is taken by consumer warp i % W.
+  const int64_t nmine = blockIdx.x < ntiles ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
   pdl_trigger();
   pdl_wait();
-  if (lane == 0) {
-    for (int j = 0; j < G.nst; ++j) mbar_init(smem_u32(&bars[j]), 1);
-    mbar_fence_init();
+  if (threadIdx.x == 0) {
     for (int j = 0; j < G.nst; ++j) {
-      const int64_t tile = first + j * tstride;
-      if (tile >= ntiles) break;
-      mbar_arrive_expect_tx(smem_u32(&bars[j]), G.box_bytes);
-      tma_load_box(ring + j * G.stage_bytes, &tmap, static_cast<int>(tile * G.TM), smem_u32(&bars[j]));
+      mbar_init(smem_u32(&full_bar[j]), 1);
+      mbar_init(smem_u32(&empty_bar[j]), 1);
     }
+    mbar_fence_init();
   }
-  __syncwarp();
+  __syncthreads();
+  if (warp == W) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    bool pok = true;
+    int64_t issued = 0;
+    for (int64_t i = 0; i < nmine; ++i) {
+      const int slot = static_cast<int>(i % G.nst);
+      // A fresh barrier counts its (virtual) previous phase as complete.
+      if (!mbar_wait(smem_u32(&empty_bar[slot]), static_cast<uint32_t>(((i / G.nst) & 1) ^ 1))) {
+        pok = false;
+        break;
+      }
+      const int64_t tile = blockIdx.x + i * gridDim.x;
+      mbar_arrive_expect_tx(smem_u32(&full_bar[slot]), G.box_bytes);
+      tma_load_box(ring + slot * G.stage_bytes, &tmap, static_cast<int>(tile * G.TM), smem_u32(&full_bar[slot]));
+      ++issued;
+    }
+    if (!pok) {
+      atomicOr(&g_dsplit_timeout, 1u);
+      // Let the copies still in flight land before the CTA's memory goes.
+      for (int64_t i = issued > G.nst ? issued - G.nst : 0; i < issued; ++i)
+        (void)mbar_wait(smem_u32(&full_bar[i % G.nst]), static_cast<uint32_t>((i / G.nst) & 1));
+    }
+    return;
+  }
   // The tables, 4 features per thread and step (loads of all steps issued
-  // first), while the first boxes stream in.
-  for (int e0 = threadIdx.x * 4; e0 < NT * 8 * ds; e0 += blockDim.x * 4 * 4) {
+  // first), by the consumer warps while the first boxes stream in.
+  const int nct = W * 32;
+  for (int e0 = threadIdx.x * 4; e0 < NT * 8 * ds; e0 += nct * 4 * 4) {
     float w[4][4], gm[4][4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int e = e0 + u * blockDim.x * 4, j = e / ds;
+      const int e = e0 + u * nct * 4, j = e / ds;
       if (e < NT * 8 * ds && j < S) {
         ldg4(a.W + e, w[u]);
         ldg4(a.Gamma + e, gm[u]);
@@ -260,7 +307,7 @@ __global__ void __launch_bounds__(8 * 32, 1)
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int e = e0 + u * blockDim.x * 4, j = e / ds, k = e - j * ds;
+      const int e = e0 + u * nct * 4, j = e / ds, k = e - j * ds;
       if (e >= NT * 8 * ds) continue;
       float hi[4], lo[4];
 #pragma unroll
@@ -273,18 +320,16 @@ __global__ void __launch_bounds__(8 * 32, 1)
       st4(wlo + j * pitch + k, lo);
     }
   }
-  __syncthreads();
+  named_sync(1, nct);
 
   const int g = lane >> 2, q = lane & 3;
   const int sg = ((g & 1) << 2) | (g >> 1);  // pair of MMA row g within a 16-pair tile
   const int nsteps = ds / 32;
   bool ok = true;
-  int64_t j = 0;
-  for (;; ++j) {
-    const int64_t tile = first + j * tstride;
-    if (tile >= ntiles) break;
-    const int slot = static_cast<int>(j % G.nst);
-    if (!mbar_wait(smem_u32(&bars[slot]), static_cast<uint32_t>((j / G.nst) & 1))) {
+  for (int64_t i = warp; i < nmine; i += W) {
+    const int64_t tile = blockIdx.x + i * gridDim.x;
+    const int slot = static_cast<int>(i % G.nst);
+    if (!mbar_wait(smem_u32(&full_bar[slot]), static_cast<uint32_t>((i / G.nst) & 1))) {
       ok = false;
       break;
     }
@@ -378,21 +423,13 @@ __global__ void __launch_bounds__(8 * 32, 1)
         }
       }
     }
-    // The slot is free once every lane has read it: refill it.
+    // The slot is free once every lane has read it.
     __syncwarp();
-    const int64_t next = tile + G.nst * tstride;
-    if (lane == 0 && next < ntiles) {
-      fence_proxy_async();
-      mbar_arrive_expect_tx(smem_u32(&bars[slot]), G.box_bytes);
-      tma_load_box(box, &tmap, static_cast<int>(next * G.TM), smem_u32(&bars[slot]));
-    }
+    if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
   }
-  if (!ok) {
-    if (lane == 0) atomicOr(&g_dsplit_timeout, 1u);
-    // Let this warp's copies still in flight land before the CTA's memory goes.
-    for (int64_t jj = j; jj < j + G.nst && first + jj * tstride < ntiles; ++jj)
-      (void)mbar_wait(smem_u32(&bars[jj % G.nst]), static_cast<uint32_t>((jj / G.nst) & 1));
-  }
+  // A consumer that gave up leaves its slot held; the producer's own wait
+  // then runs out too and drains the copies in flight.
+  if (!ok && lane == 0) atomicOr(&g_dsplit_timeout, 1u);
 }
 
 // bf16 finish on the tensor cores (n <= 16 sources, shard width a multiple of
@@ -815,10 +852,11 @@ cudaError_t launch_partials_tc(const DsplitArgs& a, cudaStream_t s) {
   alignas(64) CUtensorMap map;
   if (!encode_shard_map(a, g, &map)) return cudaErrorInvalidValue;
   const int64_t tiles = (a.T + g.TM - 1) / g.TM;
-  int64_t grid = static_cast<int64_t>(sm_count()) * blocks_per_sm(reinterpret_cast<const void*>(k), g.W * 32, g.total);
+  const int threads = (g.W + 1) * 32;
+  int64_t grid = static_cast<int64_t>(sm_count()) * blocks_per_sm(reinterpret_cast<const void*>(k), threads, g.total);
   const int64_t need = (tiles + g.W - 1) / g.W;
   if (grid > need) grid = need;
-  return launch_pdl(k, static_cast<unsigned>(grid > 0 ? grid : 1), g.W * 32, g.total, s, a, g, map);
+  return launch_pdl(k, static_cast<unsigned>(grid > 0 ? grid : 1), threads, g.total, s, a, g, map);
 }
 
 }  // namespace
