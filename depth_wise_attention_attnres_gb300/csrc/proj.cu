@@ -158,17 +158,21 @@ namespace {
 
 __device__ unsigned int g_proj_timeout = 0;
 
-constexpr int kTBM = 128, kTBN = 128, kTBK = 64, kTStages = 4;
-constexpr int kTTileBytes = kTBM * kTBK * 2;           // one operand tile, 16 KB
-constexpr int kTStageBytes = 2 * kTTileBytes;          // A and B
-constexpr int kTSmem = 1024 + kTStages * kTStageBytes + 128;
+// Output tiles of 128 rows x BN columns (BN up to 256, the widest tcgen05
+// N; wider tiles read fewer operand bytes per product from L2).
+constexpr int kTBM = 128, kTBK = 64, kTStages = 4;
+constexpr int kTTileBytes = kTBM * kTBK * 2;           // the A tile of a stage, 16 KB
+template <int BN> struct TcTile {
+  static constexpr int kStageBytes = kTTileBytes + BN * kTBK * 2;  // A and B
+  static constexpr int kSmem = 1024 + kTStages * kStageBytes + 128;
+  static constexpr uint32_t kTmemCols = BN <= 128 ? 128u : 256u;     // a power of two >= BN
+  // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits
+  // 4-5), bf16 A (7-9) and B (10-12), both K-major (15, 16), N / 8 (17-22),
+  // M / 16 (24-28).
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                                     (static_cast<uint32_t>(kTBM >> 4) << 24);
+};
 constexpr int kTThreads = 128;
-constexpr uint32_t kTmemCols = 128;
-
-// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits 4-5),
-// bf16 A (7-9) and B (10-12), both K-major (15, 16), N / 8 (17-22), M / 16 (24-28).
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(kTBN >> 3) << 17) |
-                            (static_cast<uint32_t>(kTBM >> 4) << 24);
 
 // Shared-memory descriptor of a K-major operand tile in the 128-byte swizzle
 // (8-row atoms of 128-byte rows, 1024 bytes apart): start address / 16 (bits
@@ -187,11 +191,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-__device__ __forceinline__ void umma_bf16(uint32_t tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+__device__ __forceinline__ void umma_bf16(uint32_t tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
-      ::"r"(tmem), "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+      ::"r"(tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -214,9 +218,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+template <int BN>
 __global__ void __launch_bounds__(kTThreads, 1)
     proj_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, float* Q,
                    int64_t T, int d) {
+  using G = TcTile<BN>;
+  constexpr int kTStageBytes = G::kStageBytes;
+  constexpr uint32_t kTmemCols = G::kTmemCols;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kTStages * kTStageBytes);
@@ -224,7 +232,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
   uint64_t* done_bar = empty_bar + kTStages;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done_bar + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * kTBM, n0 = blockIdx.y * kTBN;
+  const int m0 = blockIdx.x * kTBM, n0 = blockIdx.y * BN;
   const int nk = d / kTBK;
 
   pdl_trigger();
@@ -289,7 +297,8 @@ __global__ void __launch_bounds__(kTThreads, 1)
       const uint64_t da = sw128_desc(st), db = sw128_desc(st + kTTileBytes);
 #pragma unroll
       for (int k = 0; k < kTBK / 16; ++k)
-        umma_bf16(tmem, da + static_cast<uint64_t>(k * 2), db + static_cast<uint64_t>(k * 2), (kt | k) != 0);
+        umma_bf16(tmem, da + static_cast<uint64_t>(k * 2), db + static_cast<uint64_t>(k * 2), G::kIdesc,
+                  (kt | k) != 0);
       umma_commit(smem_u32(&empty_bar[s]));
       if (++s == kTStages) {
         s = 0;
@@ -308,7 +317,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const int64_t row = static_cast<int64_t>(m0) + warp * 32 + lane;
 #pragma unroll 1
-    for (int c = 0; c < kTBN / 32; ++c) {
+    for (int c = 0; c < BN / 32; ++c) {
       float v[32];
       tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(c * 32), v);
       if (row < T) {
@@ -340,25 +349,35 @@ PFN_cuTensorMapEncodeTiled_v12000 proj_encode_fn() {
 }
 
 // A [rows, d] bf16 operand as a 2-d tensor, box {64, 128}, 128-byte swizzle.
-bool encode_operand(const void* base, int64_t rows, int d, CUtensorMap* map) {
+bool encode_operand(const void* base, int64_t rows, int d, int box_rows, CUtensorMap* map) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = proj_encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
-  const cuuint32_t box[2] = {kTBK, kTBM};
+  const cuuint32_t box[2] = {kTBK, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t es[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t launch_proj_tc(const void* H, const void* Wq, float* Q, int64_t T, int d, cudaStream_t s) {
+// The widest output tile that divides d.
+inline int proj_tile_n(int d) {
+  const int cands[5] = {256, 224, 192, 160, 128};
+  for (int c : cands)
+    if (d % c == 0) return c;
+  return 0;
+}
+
+template <int BN>
+cudaError_t launch_proj_tc_n(const void* H, const void* Wq, float* Q, int64_t T, int d, cudaStream_t s) {
   alignas(64) CUtensorMap ma, mb;
-  if (!encode_operand(H, T, d, &ma) || !encode_operand(Wq, d, d, &mb)) return cudaErrorInvalidValue;
-  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(&proj_tc_kernel), kTSmem);
+  if (!encode_operand(H, T, d, kTBM, &ma) || !encode_operand(Wq, d, d, BN, &mb)) return cudaErrorInvalidValue;
+  constexpr int kTSmem = TcTile<BN>::kSmem;
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(&proj_tc_kernel<BN>), kTSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((T + kTBM - 1) / kTBM), static_cast<unsigned>(d / kTBN));
+  cfg.gridDim = dim3(static_cast<unsigned>((T + kTBM - 1) / kTBM), static_cast<unsigned>(d / BN));
   cfg.blockDim = dim3(kTThreads);
   cfg.dynamicSmemBytes = kTSmem;
   cfg.stream = s;
@@ -367,13 +386,24 @@ cudaError_t launch_proj_tc(const void* H, const void* Wq, float* Q, int64_t T, i
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, proj_tc_kernel, ma, mb, Q, T, d);
+  return cudaLaunchKernelEx(&cfg, proj_tc_kernel<BN>, ma, mb, Q, T, d);
+}
+
+cudaError_t launch_proj_tc(const void* H, const void* Wq, float* Q, int64_t T, int d, cudaStream_t s) {
+  switch (proj_tile_n(d)) {
+    case 256: return launch_proj_tc_n<256>(H, Wq, Q, T, d, s);
+    case 224: return launch_proj_tc_n<224>(H, Wq, Q, T, d, s);
+    case 192: return launch_proj_tc_n<192>(H, Wq, Q, T, d, s);
+    case 160: return launch_proj_tc_n<160>(H, Wq, Q, T, d, s);
+    case 128: return launch_proj_tc_n<128>(H, Wq, Q, T, d, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
 bool proj_tc_ok(const void* H, const void* Wq, const float* Q, int64_t T, int d) {
-  return d % kTBN == 0 && aligned16(H) && aligned16(Wq) && aligned16(Q) && T < (int64_t(1) << 31) &&
+  return proj_tile_n(d) != 0 && aligned16(H) && aligned16(Wq) && aligned16(Q) && T < (int64_t(1) << 31) &&
          (T + kTBM - 1) / kTBM <= 0x7fffffff && proj_encode_fn() != nullptr;
 }
 

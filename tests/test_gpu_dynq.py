@@ -26,7 +26,8 @@ def _wq(d, g):
     return (inputs.randn((d, d), "f32", g, dev()) / d ** 0.5).to(torch.bfloat16).contiguous()
 
 
-@pytest.mark.parametrize("T,d", [(300, 128), (1000, 896), (129, 256), (50, 100), (7, 1024)])
+@pytest.mark.parametrize("T,d", [(300, 128), (1000, 896), (129, 256), (50, 100), (7, 1024), (200, 640), (77, 384),
+                                 (130, 2048)])
 def test_query_projection(T, d):
     g = inputs.generator(40, dev())
     H = inputs.randn((T, d), "bf16", g, dev())
