@@ -26,8 +26,10 @@ def _wq(d, g):
     return (inputs.randn((d, d), "f32", g, dev()) / d ** 0.5).to(torch.bfloat16).contiguous()
 
 
+# Small products take 128-wide output tiles; the large ones here take the
+# 256-, 224-, 192- and 160-wide tiles (the widest dividing d).
 @pytest.mark.parametrize("T,d", [(300, 128), (1000, 896), (129, 256), (50, 100), (7, 1024), (200, 640), (77, 384),
-                                 (130, 2048)])
+                                 (130, 2048), (4096, 2048), (16384, 896), (32768, 384), (16383, 640)])
 def test_query_projection(T, d):
     g = inputs.generator(40, dev())
     H = inputs.randn((T, d), "bf16", g, dev())
