@@ -41,7 +41,7 @@ def _forward(N, S, T, d, dt, seed):
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("N,S,T,d", [(3, 4, 33, 256), (2, 3, 17, 100), (4, 1, 9, 128), (1, 5, 20, 384),
-                                     (2, 2, 40, 1024)])
+                                     (2, 2, 40, 1024), (1, 1, 1, 64), (2, 2, 1, 37), (9, 2, 5, 128)])
 def test_block_bwd_vs_oracle(dt, N, S, T, d):
     Src, F, W, G, dOut = _forward(N, S, T, d, dt, 70)
     dEmb = torch.zeros(T, d, device=dev())
@@ -72,3 +72,18 @@ def test_block_bwd_accumulates():
                                          G.cpu().double().numpy(), 1e-6, dOut.cpu())
     assert rel_err(dEmb, rE + 0.5) <= TOL["f32"]
     assert rel_err(dF, rF - 0.25) <= TOL["f32"]
+
+
+def test_block_bwd_fp32_gradient_input_with_bf16_storage():
+    """dL/dout may be fp32 while the pass stores bf16."""
+    N, S, T, d = 2, 3, 21, 256
+    Src, F, W, G, _ = _forward(N, S, T, d, "bf16", 72)
+    dOut = inputs.randn((N * S, T, d), "f32", inputs.generator(73, dev()), dev())
+    dEmb = torch.zeros(T, d, device=dev())
+    dF = torch.zeros(N * S, T, d, device=dev())
+    ar.attnres_block_bwd(Src, F, N, S, W, G, 1e-6, dOut, dEmb, dF)
+    torch.cuda.synchronize()
+    rE, rF, _, _ = oracle.block_pass_bwd(Src.cpu(), F.cpu(), N, S, W.cpu().double().numpy(),
+                                         G.cpu().double().numpy(), 1e-6, dOut.cpu().double().numpy())
+    assert rel_err(dEmb, rE) <= TOL["f32"]
+    assert rel_err(dF, rF) <= TOL["f32"]

@@ -26,7 +26,8 @@ def _built():
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("n,S,T,d,P", [(8, 8, 70, 1024, 4), (3, 6, 33, 2048, 4), (5, 3, 41, 512, 2),
                                        (1, 1, 16, 256, 2), (12, 16, 9, 384, 3),
-                                       (4, 5, 37, 360, 3), (20, 4, 23, 512, 2)])
+                                       (4, 5, 37, 360, 3), (20, 4, 23, 512, 2), (8, 8, 1, 512, 2),
+                                       (16, 2, 5, 256, 2), (2, 16, 3, 128, 1)])
 def test_dsplit_stage1(dt, n, S, T, d, P):
     g = inputs.generator(50, dev())
     Src = inputs.history(n, T, d, dt, g, dev(), depth_scaled=True)
