@@ -68,7 +68,24 @@ DSPLIT_SHARDS = 4
 
 
 def block_bwd_bytes(N: int, S: int, T: int, d: int, es: int) -> dict:
-    """Algorithmic bytes of the Block pass backward as attnres_block_bwd runs it.
+    """Algorithmic bytes of the Block pass backward with all S reads of a block
+    in one pass (the batched kernel: d a multiple of 128 up to 1024, N <= 8,
+    S <= 8). Per block n: the n + 1 sources, the block's outputs but its last
+    (for the running sums) and the S gradients dL/dout read once, the gradient
+    of the block's summary read (n + 1 < N), the sources' fp32 gradient rows
+    and the S outputs' fp32 gradient rows read and written once. Once: those
+    rows zeroed; the embedding's gradient added at the end."""
+    E = T * d
+    read = route = 0
+    for n in range(N):
+        read += (n + 1) * E * es + (S - 1) * E * es + S * E * es + (4 * E if n + 1 < N else 0)
+        route += (n + 1) * 8 * E + S * 8 * E
+    route += N * 4 * E + 12 * E
+    return {"read": read, "route": route, "total": read + route}
+
+
+def block_bwd_bytes_per_read(N: int, S: int, T: int, d: int, es: int) -> dict:
+    """Algorithmic bytes of the Block pass backward read by read (the fallback).
 
     Per read k = nS + j over n_src = n + 1 (+ 1 for the running sum when j >= 1)
     fp32 sources: the read backward moves n_src rows (read) and their fp32
@@ -397,8 +414,11 @@ class BlockBwdStep:
         L = wl.N * wl.S
         self.launches = L + (L - wl.N) + wl.N * max(wl.S - 1, 0) + (wl.N - 1) + 2
         es = 2 if wl.dtype == "bf16" else 4
-        self.byte_parts = block_bwd_bytes(wl.N, wl.S, wl.T, wl.d, es)
+        batched = wl.d % 128 == 0 and wl.d <= 1024 and wl.N <= 8 and wl.S <= 8
+        self.byte_parts = (block_bwd_bytes if batched else block_bwd_bytes_per_read)(wl.N, wl.S, wl.T, wl.d, es)
         self.bytes = self.byte_parts["total"]
+        if batched:
+            self.launches = wl.N + 1
 
     def __call__(self):
         self.ar.attnres_block_bwd(self.Src, self.F, self.wl.N, self.wl.S, self.W, self.G, self.wl.eps, self.dOut,
@@ -689,12 +709,15 @@ def ours(args):
                     "average launch duration = step time / R (gaps included)"}
     elif isinstance(step, BlockBwdStep):
         g = step.byte_parts["total"] / (ms / 1e3) / 1e9
+        batched = step.launches == step.wl.N + 1
         line["roofline"] = {
-            "kernel": "full_bwd_bulk_kernel", "bound": "hbm", "achieved": g, "peak": peaks["hbm_gbs"],
+            "kernel": "block_bwd_batched_kernel" if batched else "full_bwd_bulk_kernel", "bound": "hbm",
+            "achieved": g, "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": g / peaks["hbm_gbs"], "frac_of_nominal_8000": g / NOMINAL_HBM_GBS,
             "peak_source": peaks["source"], "traffic": None,
             "byte_parts": step.byte_parts,
-            "note": "whole step: the per-read backward launches carry "
+            "note": "whole step: one batched launch per block (all S reads)" if batched else
+                    "whole step: the per-read backward launches carry "
                     f"{step.byte_parts['read'] / step.byte_parts['total']:.0%} of the algorithmic bytes"}
     elif isinstance(step, DsplitStep):
         times = time_dsplit_kernels(step, 3, stream)

@@ -454,6 +454,22 @@ int attnres_block_bwd(const void* Src, int64_t src_stride, const void* F, int64_
       if (overlap(outs[i], outs[j])) return ATTNRES_ERR_INVALID_ARG;
   }
   cudaStream_t s = as_stream(stream);
+  {
+    // Batched: each block's S reads in one pass over the tokens; the sources'
+    // gradients (embedding and summaries) gather in the scratch's first N rows.
+    BlockBwdArgs b{Src, N > 1 ? src_stride : 0, F, L > 1 ? f_stride : 0, W, Gamma, dOut,
+                   L > 1 ? dout_stride : 0, dout_dtype == ATTNRES_BF16, scratch, E, dF, L > 1 ? df_stride : 0,
+                   dW, dGamma, N, S, 0, T, d, dtype == ATTNRES_BF16, eps};
+    if (block_bwd_batched_ok(b)) {
+      if (cudaMemsetAsync(scratch, 0, N * E * 4, s) != cudaSuccess) return ATTNRES_ERR_CUDA;
+      for (int32_t n = N - 1; n >= 0; --n) {
+        b.n = n;
+        const int st = status_of(launch_block_bwd_batched(b, s));
+        if (st != ATTNRES_OK) return st;
+      }
+      return status_of(launch_spread(dEmb, 0, 1, scratch, E, s));
+    }
+  }
   // Scratch: fp32 sources Vs [N + 1][E] (embedding, b_1 .. b_{N-1}, and the
   // slot after block n's sources that holds its running sum), their
   // gradients dVs [N + 1][E], the running sums Ps [S][E] (Ps[j] = P of the

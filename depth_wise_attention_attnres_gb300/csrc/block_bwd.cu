@@ -158,3 +158,274 @@ cudaError_t launch_spread(float* dst, int64_t dst_stride, int R, const float* g,
 }
 
 }  // namespace attnres
+
+namespace attnres {
+namespace {
+
+// ------------------------------------------------ batched block backward --
+//
+// All S reads of block n in one pass over the tokens (d a multiple of 128 up
+// to 1024, at most 8 cross-block sources and 8 sublayers per block). A CTA
+// has d / 128 warps; warp w owns features 128 w .. 128 w + 127 (4 per lane)
+// for every token, so the query-gradient sums du_j stay in its registers for
+// the whole launch. Per token:
+//  1. each lane loads its features of the block's sources X_0 .. X_n, the
+//     running sums P_j (rebuilt from the outputs with the forward's fp32
+//     additions) and dL/dout_j, and forms its parts of every dot product the
+//     reads need: sum X_i^2, sum P_j^2, X_i . u_j, P_j . u_j, dz_j . X_i and
+//     dz_j . P_j (u_j = w_j * gamma_j); the parts are summed over the warp by
+//     a reduce-scatter of 32 values at a time and over the warps in shared
+//     memory;
+//  2. one thread per read forms its scores, softmax and score gradients, and
+//     from them the coefficients of dX_i = sum_j (a_ij dz_j + r_i de_ij u_j)
+//     - c_i X_i and of dP_j;
+//  3. each lane forms its features of dX_i (added to the sources' gradient
+//     rows), of dP_j, of du_j, and of every output's gradient dF_q = db +
+//     sum_{j > q} dP_j, db being the gradient of this block's summary that
+//     the later blocks accumulated.
+constexpr int kBX = 8;              // cross-block sources at most (n + 1)
+constexpr int kBQ = 8;              // sublayers (reads) per block at most
+constexpr int kBV = 160;            // reduced values per token (5 x 32)
+// Value layout: [0, 8) sum X_i^2; [8, 16) sum P_j^2 (j >= 1); [16, 80) X_i.u_j
+// at 16 + 8 j + i; [80, 144) dz_j.X_i at 80 + 8 j + i; [144, 152) P_j.u_j;
+// [152, 160) dz_j.P_j.
+constexpr int kOffSsP = 8, kOffEX = 16, kOffDaX = 80, kOffEP = 144, kOffDaP = 152;
+
+__device__ __forceinline__ float dot4(const float (&a)[4], const float (&b)[4]) {
+  return fmaf(a[0], b[0], fmaf(a[1], b[1], fmaf(a[2], b[2], a[3] * b[3])));
+}
+
+template <typename T, typename TZ>
+__global__ void __launch_bounds__(1024 / 128 * 32, 1) block_bwd_batched_kernel(BlockBwdArgs a) {
+  __shared__ float red[8][kBV];      // per-warp sums
+  __shared__ float tot[kBV];         // CTA sums
+  __shared__ float alpha[kBX][kBQ];  // coefficient of dz_j in dX_i
+  __shared__ float beta[kBX][kBQ];   // coefficient of u_j in dX_i (r_i de_ij; also of X_i in du_j)
+  __shared__ float ctmp[kBX][kBQ];   // de_ij e_ij r_i^2 / d, summed over j into cx[i]
+  __shared__ float cx[kBX];
+  __shared__ float pa[kBQ], pb[kBQ], pc[kBQ];  // the same for P_j (j >= 1)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int W = blockDim.x >> 5;
+  const int n1 = a.n + 1, S = a.S, d = a.d;
+  const int k = warp * 128 + lane * 4;
+  const int64_t k0 = static_cast<int64_t>(a.n) * S;
+  const float inv_d = 1.0f / static_cast<float>(d);
+  // u_j = w_j * gamma_j of this lane's features.
+  float u[kBQ][4], du[kBQ][4];
+#pragma unroll
+  for (int j = 0; j < kBQ; ++j) {
+    if (j < S) {
+      float w4[4], g4[4];
+      ldg4(a.W + (k0 + j) * d + k, w4);
+      ldg4(a.Gamma + (k0 + j) * d + k, g4);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) u[j][e] = w4[e] * g4[e];
+    } else {
+      u[j][0] = u[j][1] = u[j][2] = u[j][3] = 0.f;
+    }
+    du[j][0] = du[j][1] = du[j][2] = du[j][3] = 0.f;
+  }
+  const T* src = static_cast<const T*>(a.Src);
+  const T* F = static_cast<const T*>(a.F);
+  const TZ* dz = static_cast<const TZ*>(a.dOut);
+  for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
+    // ---- 1. loads and partial dot products
+    float x[kBX][4], p[kBQ][4], z[kBQ][4];
+#pragma unroll
+    for (int i = 0; i < kBX; ++i) {
+      if (i < n1) ldg4(src + i * a.src_stride + t * d + k, x[i]);
+      else x[i][0] = x[i][1] = x[i][2] = x[i][3] = 0.f;
+    }
+    p[0][0] = p[0][1] = p[0][2] = p[0][3] = 0.f;
+#pragma unroll
+    for (int j = 1; j < kBQ; ++j) {
+      if (j < S) {
+        float f[4];
+        ldg4(F + (k0 + j - 1) * a.f_stride + t * d + k, f);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) p[j][e] = j == 1 ? f[e] : p[j - 1][e] + f[e];
+      } else {
+        p[j][0] = p[j][1] = p[j][2] = p[j][3] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kBQ; ++j) {
+      if (j < S) ldg4(dz + (k0 + j) * a.dout_stride + t * d + k, z[j]);
+      else z[j][0] = z[j][1] = z[j][2] = z[j][3] = 0.f;
+    }
+#pragma unroll
+    for (int r = 0; r < kBV / 32; ++r) {
+      float v[32];
+#pragma unroll
+      for (int m = 0; m < 32; ++m) {
+        const int idx = r * 32 + m;
+        if (idx < kOffSsP) v[m] = dot4(x[idx], x[idx]);
+        else if (idx < kOffEX) v[m] = dot4(p[idx - kOffSsP], p[idx - kOffSsP]);
+        else if (idx < kOffDaX) v[m] = dot4(x[(idx - kOffEX) & 7], u[(idx - kOffEX) >> 3]);
+        else if (idx < kOffEP) v[m] = dot4(x[(idx - kOffDaX) & 7], z[(idx - kOffDaX) >> 3]);
+        else if (idx < kOffDaP) v[m] = dot4(p[idx - kOffEP], u[idx - kOffEP]);
+        else v[m] = dot4(p[idx - kOffDaP], z[idx - kOffDaP]);
+      }
+      // Reduce-scatter over the warp: lane l ends with the warp's sum of v[l].
+#pragma unroll
+      for (int off = 16, h = 16; off >= 1; off >>= 1, h >>= 1) {
+        const bool up = lane & off;
+#pragma unroll
+        for (int m = 0; m < 16; ++m)
+          if (m < h) {
+            const float send = up ? v[m] : v[m + h];
+            const float keep = up ? v[m + h] : v[m];
+            v[m] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+          }
+      }
+      red[warp][r * 32 + lane] = v[0];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kBV; i += blockDim.x) {
+      float s = 0.f;
+      for (int ww = 0; ww < W; ++ww) s += red[ww][i];
+      tot[i] = s;
+    }
+    __syncthreads();
+    // ---- 2. per read: scores, softmax, score gradients, coefficients
+    if (threadIdx.x < S) {
+      const int j = threadIdx.x;
+      float rr[kBX], e[kBX], aa[kBX];
+      float m = -INFINITY;
+      for (int i = 0; i < n1; ++i) {
+        rr[i] = rsqrtf(tot[i] * inv_d + a.eps);
+        e[i] = rr[i] * tot[kOffEX + 8 * j + i];
+        m = fmaxf(m, e[i]);
+      }
+      float rP = 0.f, eP = 0.f;
+      if (j >= 1) {
+        rP = rsqrtf(tot[kOffSsP + j] * inv_d + a.eps);
+        eP = rP * tot[kOffEP + j];
+        m = fmaxf(m, eP);
+      }
+      float zs = 0.f;
+      for (int i = 0; i < n1; ++i) {
+        aa[i] = __expf(e[i] - m);
+        zs += aa[i];
+      }
+      float aP = j >= 1 ? __expf(eP - m) : 0.f;
+      zs += aP;
+      const float inv = 1.0f / zs;
+      float sda = 0.f;
+      for (int i = 0; i < n1; ++i) {
+        aa[i] *= inv;
+        sda = fmaf(aa[i], tot[kOffDaX + 8 * j + i], sda);
+      }
+      aP *= inv;
+      if (j >= 1) sda = fmaf(aP, tot[kOffDaP + j], sda);
+      for (int i = 0; i < n1; ++i) {
+        const float de = aa[i] * (tot[kOffDaX + 8 * j + i] - sda);
+        alpha[i][j] = aa[i];
+        beta[i][j] = rr[i] * de;
+        ctmp[i][j] = de * e[i] * rr[i] * rr[i] * inv_d;
+      }
+      if (j >= 1) {
+        const float deP = aP * (tot[kOffDaP + j] - sda);
+        pa[j] = aP;
+        pb[j] = rP * deP;
+        pc[j] = deP * eP * rP * rP * inv_d;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < n1) {
+      float c = 0.f;
+      for (int j = 0; j < S; ++j) c += ctmp[threadIdx.x][j];
+      cx[threadIdx.x] = c;
+    }
+    __syncthreads();
+    // ---- 3. gradients of this lane's features
+#pragma unroll
+    for (int i = 0; i < kBX; ++i) {
+      if (i < n1) {
+        float g[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) g[e] = -cx[i] * x[i][e];
+#pragma unroll
+        for (int j = 0; j < kBQ; ++j)
+          if (j < S) {
+            const float al = alpha[i][j], be = beta[i][j];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              g[e] = fmaf(al, z[j][e], fmaf(be, u[j][e], g[e]));
+              du[j][e] = fmaf(be, x[i][e], du[j][e]);
+            }
+          }
+        float* dv = a.dVs + i * a.E + t * d + k;
+        const float4 o = *reinterpret_cast<const float4*>(dv);
+        *reinterpret_cast<float4*>(dv) = make_float4(o.x + g[0], o.y + g[1], o.z + g[2], o.w + g[3]);
+      }
+    }
+    // dP_j and the outputs' gradients: dF_q += db + sum_{j > q} dP_j.
+    float db[4] = {0.f, 0.f, 0.f, 0.f};
+    if (a.n + 1 < a.N) ldg4(a.dVs + (a.n + 1) * a.E + t * d + k, db);
+    float G[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int q = kBQ - 1; q >= 0; --q) {
+      if (q >= S) continue;
+      float* df = a.dF + (k0 + q) * a.df_stride + t * d + k;
+      const float4 o = *reinterpret_cast<const float4*>(df);
+      *reinterpret_cast<float4*>(df) =
+          make_float4(o.x + db[0] + G[0], o.y + db[1] + G[1], o.z + db[2] + G[2], o.w + db[3] + G[3]);
+      if (q >= 1) {
+        const float c1 = pa[q], c2 = pb[q], c3 = pc[q];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          G[e] += fmaf(c1, z[q][e], fmaf(c2, u[q][e], -c3 * p[q][e]));
+          du[q][e] = fmaf(c2, p[q][e], du[q][e]);
+        }
+      }
+    }
+    // The coefficient arrays are rewritten by the next token only after
+    // every thread has used them.
+    __syncthreads();
+  }
+  // dw_j += du_j * gamma_j, dgamma_j += du_j * w_j.
+#pragma unroll
+  for (int j = 0; j < kBQ; ++j) {
+    if (j >= S) continue;
+    float w4[4], g4[4];
+    ldg4(a.W + (k0 + j) * d + k, w4);
+    ldg4(a.Gamma + (k0 + j) * d + k, g4);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (a.dW) atomicAdd(a.dW + (k0 + j) * d + k + e, du[j][e] * g4[e]);
+      if (a.dGamma) atomicAdd(a.dGamma + (k0 + j) * d + k + e, du[j][e] * w4[e]);
+    }
+  }
+}
+
+}  // namespace
+
+bool block_bwd_batched_ok(const BlockBwdArgs& a) {
+  if (a.d % 128 != 0 || a.d > 1024 || a.N > kBX || a.S > kBQ) return false;
+  const int es = a.bf16 ? 2 : 4, zs = a.dz_bf16 ? 2 : 4;
+  return aligned16(a.Src) && aligned16(a.F) && aligned16(a.dOut) && aligned16(a.dVs) && aligned16(a.dF) &&
+         aligned16(a.W) && aligned16(a.Gamma) && (a.src_stride * es) % 16 == 0 && (a.f_stride * es) % 16 == 0 &&
+         (a.dout_stride * zs) % 16 == 0 && (a.df_stride * 4) % 16 == 0;
+}
+
+cudaError_t launch_block_bwd_batched(const BlockBwdArgs& a, cudaStream_t s) {
+  const int threads = a.d / 128 * 32;
+  const void* fn = a.bf16 ? (a.dz_bf16 ? reinterpret_cast<const void*>(&block_bwd_batched_kernel<bf16, bf16>)
+                                       : reinterpret_cast<const void*>(&block_bwd_batched_kernel<bf16, float>))
+                          : (a.dz_bf16 ? reinterpret_cast<const void*>(&block_bwd_batched_kernel<float, bf16>)
+                                       : reinterpret_cast<const void*>(&block_bwd_batched_kernel<float, float>));
+  int64_t grid = static_cast<int64_t>(sm_count()) * blocks_per_sm(fn, threads, 0);
+  if (grid > a.T) grid = a.T;
+  const unsigned g = static_cast<unsigned>(grid > 0 ? grid : 1);
+  if (a.bf16) {
+    if (a.dz_bf16) block_bwd_batched_kernel<bf16, bf16><<<g, threads, 0, s>>>(a);
+    else block_bwd_batched_kernel<bf16, float><<<g, threads, 0, s>>>(a);
+  } else {
+    if (a.dz_bf16) block_bwd_batched_kernel<float, bf16><<<g, threads, 0, s>>>(a);
+    else block_bwd_batched_kernel<float, float><<<g, threads, 0, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace attnres

@@ -162,6 +162,31 @@ cudaError_t launch_dsplit_partials(const DsplitArgs& a, cudaStream_t s);
 cudaError_t launch_dsplit_finish(const DsplitArgs& a, cudaStream_t s);
 cudaError_t take_timeout_dsplit(unsigned int* flag);
 cudaError_t launch_full_bwd(const BwdArgs& a, cudaStream_t s, bool fast);
+// One block's reads in the batched Block backward (block_bwd.cu).
+struct BlockBwdArgs {
+  const void* Src;      // [N][T][d] embedding and frozen summaries
+  int64_t src_stride;
+  const void* F;        // sublayer outputs, f_stride apart
+  int64_t f_stride;
+  const float* W;       // [N*S][d]
+  const float* Gamma;
+  const void* dOut;     // dL/dout, dout_stride apart
+  int64_t dout_stride;
+  int dz_bf16;
+  float* dVs;           // [N][E] gradients of the embedding and the summaries (+=)
+  int64_t E;
+  float* dF;            // df_stride apart (+=)
+  int64_t df_stride;
+  float* dW;            // may be nullptr
+  float* dGamma;        // may be nullptr
+  int N, S, n;          // n: the block
+  int64_t T;
+  int d;
+  int bf16;
+  float eps;
+};
+bool block_bwd_batched_ok(const BlockBwdArgs& a);
+cudaError_t launch_block_bwd_batched(const BlockBwdArgs& a, cudaStream_t s);
 // Block pass backward helpers (block_bwd.cu); E elements per row, fp32 rows E apart.
 cudaError_t launch_widen_rows(const void* src, int64_t src_stride, int is_bf16, float* dst, int R, int64_t E,
                               cudaStream_t s);
