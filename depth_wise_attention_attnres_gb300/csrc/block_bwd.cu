@@ -195,8 +195,20 @@ __device__ __forceinline__ float dot4(const float (&a)[4], const float (&b)[4]) 
   return fmaf(a[0], b[0], fmaf(a[1], b[1], fmaf(a[2], b[2], a[3] * b[3])));
 }
 
+// Dynamic shared memory of the batched kernel: the next token's inputs
+// (sources and outputs in T, dL/dout in TZ, double-buffered by cp.async) and
+// the current token's fp32 gradient rows to update (sources', outputs', and
+// the block summary's).
+inline int64_t block_bwd_smem(const BlockBwdArgs& a) {
+  const int n1 = a.N;  // sized for the largest block (n + 1 = N)
+  const int64_t es = a.bf16 ? 2 : 4, zs = a.dz_bf16 ? 2 : 4;
+  return 2 * static_cast<int64_t>(n1 + a.S - 1) * a.d * es + 2 * static_cast<int64_t>(a.S) * a.d * zs +
+         static_cast<int64_t>(n1 + a.S + 1) * a.d * 4;
+}
+
 template <typename T, typename TZ>
 __global__ void __launch_bounds__(1024 / 128 * 32, 1) block_bwd_batched_kernel(BlockBwdArgs a) {
+  extern __shared__ __align__(16) unsigned char bsm[];
   __shared__ float red[8][kBV];      // per-warp sums
   __shared__ float tot[kBV];         // CTA sums
   __shared__ float alpha[kBX][kBQ];  // coefficient of dz_j in dX_i
@@ -228,12 +240,55 @@ __global__ void __launch_bounds__(1024 / 128 * 32, 1) block_bwd_batched_kernel(B
   const T* src = static_cast<const T*>(a.Src);
   const T* F = static_cast<const T*>(a.F);
   const TZ* dz = static_cast<const TZ*>(a.dOut);
+  // Shared rows: inputs [2][rowsT][d] of T ([0, n1) sources, then the outputs
+  // k0 .. k0 + S - 2), [2][S][d] of TZ, and the gradient rows [n1 + S + 1][d]
+  // fp32 ([0, n1) the sources', then the outputs', then the summary's).
+  const int rowsT = a.N + S - 1;  // buffer rows, sized for the largest block
+  T* inT = reinterpret_cast<T*>(bsm);
+  TZ* inZ = reinterpret_cast<TZ*>(bsm + 2 * static_cast<int64_t>(rowsT) * d * sizeof(T));
+  float* gsm = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(inZ) + 2 * static_cast<int64_t>(S) * d * sizeof(TZ));
+  const bool has_db = a.n + 1 < a.N;
+  const int chT = d * static_cast<int>(sizeof(T)) / 16, chZ = d * static_cast<int>(sizeof(TZ)) / 16, chG = d / 4;
+  auto issue_inputs = [&](int64_t t, int buf) {
+    for (int c = threadIdx.x; c < (n1 + S - 1) * chT; c += blockDim.x) {
+      const int r = c / chT, ch = c - r * chT;
+      const T* g = r < n1 ? src + r * a.src_stride + t * d : F + (k0 + r - n1) * a.f_stride + t * d;
+      cp_async16(smem_u32(inT + (static_cast<int64_t>(buf) * rowsT + r) * d) + ch * 16,
+                 reinterpret_cast<const char*>(g) + ch * 16, true);
+    }
+    for (int c = threadIdx.x; c < S * chZ; c += blockDim.x) {
+      const int r = c / chZ, ch = c - r * chZ;
+      cp_async16(smem_u32(inZ + (static_cast<int64_t>(buf) * S + r) * d) + ch * 16,
+                 reinterpret_cast<const char*>(dz + (k0 + r) * a.dout_stride + t * d) + ch * 16, true);
+    }
+  };
+  auto issue_grads = [&](int64_t t) {
+    for (int c = threadIdx.x; c < (n1 + S + (has_db ? 1 : 0)) * chG; c += blockDim.x) {
+      const int r = c / chG, ch = c - r * chG;
+      const float* g = r < n1 ? a.dVs + r * a.E + t * d
+                              : (r < n1 + S ? a.dF + (k0 + r - n1) * a.df_stride + t * d : a.dVs + (a.n + 1) * a.E + t * d);
+      cp_async16(smem_u32(gsm + static_cast<int64_t>(r) * d) + ch * 16, reinterpret_cast<const char*>(g) + ch * 16, true);
+    }
+  };
+  int buf = 0;
+  if (static_cast<int64_t>(blockIdx.x) < a.T) issue_inputs(blockIdx.x, 0);
+  cp_async_commit();
   for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
-    // ---- 1. loads and partial dot products
+    // This token's gradient rows, then the next token's inputs, in flight
+    // while this token is worked on.
+    issue_grads(t);
+    cp_async_commit();
+    if (t + gridDim.x < a.T) issue_inputs(t + gridDim.x, buf ^ 1);
+    cp_async_commit();
+    cp_async_wait<2>();
+    __syncthreads();
+    const T* xs = inT + static_cast<int64_t>(buf) * rowsT * d;
+    const TZ* zsm = inZ + static_cast<int64_t>(buf) * S * d;
+    // ---- 1. partial dot products of this lane's features
     float x[kBX][4], p[kBQ][4], z[kBQ][4];
 #pragma unroll
     for (int i = 0; i < kBX; ++i) {
-      if (i < n1) ldg4(src + i * a.src_stride + t * d + k, x[i]);
+      if (i < n1) lds4(xs + i * d + k, x[i]);
       else x[i][0] = x[i][1] = x[i][2] = x[i][3] = 0.f;
     }
     p[0][0] = p[0][1] = p[0][2] = p[0][3] = 0.f;
@@ -241,7 +296,7 @@ __global__ void __launch_bounds__(1024 / 128 * 32, 1) block_bwd_batched_kernel(B
     for (int j = 1; j < kBQ; ++j) {
       if (j < S) {
         float f[4];
-        ldg4(F + (k0 + j - 1) * a.f_stride + t * d + k, f);
+        lds4(xs + (n1 + j - 1) * d + k, f);
 #pragma unroll
         for (int e = 0; e < 4; ++e) p[j][e] = j == 1 ? f[e] : p[j - 1][e] + f[e];
       } else {
@@ -250,7 +305,7 @@ __global__ void __launch_bounds__(1024 / 128 * 32, 1) block_bwd_batched_kernel(B
     }
 #pragma unroll
     for (int j = 0; j < kBQ; ++j) {
-      if (j < S) ldg4(dz + (k0 + j) * a.dout_stride + t * d + k, z[j]);
+      if (j < S) lds4(zsm + j * d + k, z[j]);
       else z[j][0] = z[j][1] = z[j][2] = z[j][3] = 0.f;
     }
 #pragma unroll
@@ -337,6 +392,7 @@ __global__ void __launch_bounds__(1024 / 128 * 32, 1) block_bwd_batched_kernel(B
       for (int j = 0; j < S; ++j) c += ctmp[threadIdx.x][j];
       cx[threadIdx.x] = c;
     }
+    cp_async_wait<1>();  // this token's gradient rows
     __syncthreads();
     // ---- 3. gradients of this lane's features
 #pragma unroll
@@ -355,21 +411,20 @@ __global__ void __launch_bounds__(1024 / 128 * 32, 1) block_bwd_batched_kernel(B
               du[j][e] = fmaf(be, x[i][e], du[j][e]);
             }
           }
-        float* dv = a.dVs + i * a.E + t * d + k;
-        const float4 o = *reinterpret_cast<const float4*>(dv);
-        *reinterpret_cast<float4*>(dv) = make_float4(o.x + g[0], o.y + g[1], o.z + g[2], o.w + g[3]);
+        const float4 o = *reinterpret_cast<const float4*>(gsm + i * d + k);
+        *reinterpret_cast<float4*>(a.dVs + i * a.E + t * d + k) =
+            make_float4(o.x + g[0], o.y + g[1], o.z + g[2], o.w + g[3]);
       }
     }
     // dP_j and the outputs' gradients: dF_q += db + sum_{j > q} dP_j.
     float db[4] = {0.f, 0.f, 0.f, 0.f};
-    if (a.n + 1 < a.N) ldg4(a.dVs + (a.n + 1) * a.E + t * d + k, db);
+    if (has_db) lds4(gsm + (n1 + S) * d + k, db);
     float G[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int q = kBQ - 1; q >= 0; --q) {
       if (q >= S) continue;
-      float* df = a.dF + (k0 + q) * a.df_stride + t * d + k;
-      const float4 o = *reinterpret_cast<const float4*>(df);
-      *reinterpret_cast<float4*>(df) =
+      const float4 o = *reinterpret_cast<const float4*>(gsm + (n1 + q) * d + k);
+      *reinterpret_cast<float4*>(a.dF + (k0 + q) * a.df_stride + t * d + k) =
           make_float4(o.x + db[0] + G[0], o.y + db[1] + G[1], o.z + db[2] + G[2], o.w + db[3] + G[3]);
       if (q >= 1) {
         const float c1 = pa[q], c2 = pb[q], c3 = pc[q];
@@ -380,10 +435,12 @@ __global__ void __launch_bounds__(1024 / 128 * 32, 1) block_bwd_batched_kernel(B
         }
       }
     }
-    // The coefficient arrays are rewritten by the next token only after
-    // every thread has used them.
+    // The coefficient arrays and this buffer are rewritten by the next
+    // token only after every thread has used them.
     __syncthreads();
+    buf ^= 1;
   }
+  cp_async_wait<0>();
   // dw_j += du_j * gamma_j, dgamma_j += du_j * w_j.
 #pragma unroll
   for (int j = 0; j < kBQ; ++j) {
@@ -403,6 +460,7 @@ __global__ void __launch_bounds__(1024 / 128 * 32, 1) block_bwd_batched_kernel(B
 
 bool block_bwd_batched_ok(const BlockBwdArgs& a) {
   if (a.d % 128 != 0 || a.d > 1024 || a.N > kBX || a.S > kBQ) return false;
+  if (block_bwd_smem(a) > 200 * 1024) return false;
   const int es = a.bf16 ? 2 : 4, zs = a.dz_bf16 ? 2 : 4;
   return aligned16(a.Src) && aligned16(a.F) && aligned16(a.dOut) && aligned16(a.dVs) && aligned16(a.dF) &&
          aligned16(a.W) && aligned16(a.Gamma) && (a.src_stride * es) % 16 == 0 && (a.f_stride * es) % 16 == 0 &&
@@ -415,15 +473,18 @@ cudaError_t launch_block_bwd_batched(const BlockBwdArgs& a, cudaStream_t s) {
                                        : reinterpret_cast<const void*>(&block_bwd_batched_kernel<bf16, float>))
                           : (a.dz_bf16 ? reinterpret_cast<const void*>(&block_bwd_batched_kernel<float, bf16>)
                                        : reinterpret_cast<const void*>(&block_bwd_batched_kernel<float, float>));
-  int64_t grid = static_cast<int64_t>(sm_count()) * blocks_per_sm(fn, threads, 0);
+  const int smem = static_cast<int>(block_bwd_smem(a));
+  cudaError_t e = allow_dynamic_smem(fn, smem);
+  if (e != cudaSuccess) return e;
+  int64_t grid = static_cast<int64_t>(sm_count()) * blocks_per_sm(fn, threads, smem);
   if (grid > a.T) grid = a.T;
   const unsigned g = static_cast<unsigned>(grid > 0 ? grid : 1);
   if (a.bf16) {
-    if (a.dz_bf16) block_bwd_batched_kernel<bf16, bf16><<<g, threads, 0, s>>>(a);
-    else block_bwd_batched_kernel<bf16, float><<<g, threads, 0, s>>>(a);
+    if (a.dz_bf16) block_bwd_batched_kernel<bf16, bf16><<<g, threads, smem, s>>>(a);
+    else block_bwd_batched_kernel<bf16, float><<<g, threads, smem, s>>>(a);
   } else {
-    if (a.dz_bf16) block_bwd_batched_kernel<float, bf16><<<g, threads, 0, s>>>(a);
-    else block_bwd_batched_kernel<float, float><<<g, threads, 0, s>>>(a);
+    if (a.dz_bf16) block_bwd_batched_kernel<float, bf16><<<g, threads, smem, s>>>(a);
+    else block_bwd_batched_kernel<float, float><<<g, threads, smem, s>>>(a);
   }
   return cudaGetLastError();
 }

@@ -185,6 +185,20 @@ __device__ __forceinline__ void st4(bf16* p, const float (&x)[4]) {
   *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
 }
 
+// ------------------------------------------------------------- cp.async --
+
+// 16 bytes global -> shared, asynchronous; full = false fills them with zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool full) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(full ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's committed groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ------------------------------------------- mma.sync m16n8k16 bf16 fragments --
 
 // c += A (16x16 bf16, row-major fragments a) * B (16x8 bf16, col-major

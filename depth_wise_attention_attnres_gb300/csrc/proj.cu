@@ -23,16 +23,6 @@ constexpr int kPPitch = kPBK + 8;  // elements per staged row (80 bytes)
 constexpr int kPThreads = 256;
 constexpr int kPSmem = kPStages * (kPBM + kPBN) * kPPitch * 2;
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool full) {
-  // src_size 0 fills the 16 bytes with zeros (rows past T).
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(full ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
 __global__ void __launch_bounds__(kPThreads) proj_kernel(const bf16* H, const bf16* Wq, float* Q, int64_t T,
                                                          int d) {
