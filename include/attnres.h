@@ -210,9 +210,14 @@ int attnres_full_bwd(const void* V, int64_t src_stride, int32_t n_src, int64_t T
  * P_k if j >= 1}, with b_m the plain sum of block (m-1)'s outputs and P_k the
  * sum of block n's outputs before k. By the chain rule the gradient of b_m
  * reaches every member of block m-1 unchanged and that of P_k every output of
- * block n before k. The reads run in reverse order through the Full read's
- * backward (attnres_full_bwd) over fp32 copies of their sources, with the
- * running sums rebuilt by the same fp32 additions the forward made.
+ * block n before k. All dL/dout_k are inputs (the vector-Jacobian product of
+ * the pass with F given, as the forward defines it; a model whose sublayers
+ * make F from the outputs runs the read backward per sublayer instead). For d
+ * a multiple of 128 up to 1024, at most 8 blocks and 8 sublayers per block,
+ * each block's S reads run in one batched pass over the tokens; otherwise the
+ * reads run in reverse order through the Full read's backward over fp32
+ * copies of their sources. Either way the running sums are rebuilt by the
+ * same fp32 additions the forward made.
  *
  *   Src       device, [N][T][d] dtype, rows src_stride apart: Src[0] the
  *             embedding, Src[m] the frozen summary b_m (as the forward pass
