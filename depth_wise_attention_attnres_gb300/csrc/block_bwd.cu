@@ -249,25 +249,29 @@ __global__ void __launch_bounds__(1024 / 128 * 32, 1) block_bwd_batched_kernel(B
   float* gsm = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(inZ) + 2 * static_cast<int64_t>(S) * d * sizeof(TZ));
   const bool has_db = a.n + 1 < a.N;
   const int chT = d * static_cast<int>(sizeof(T)) / 16, chZ = d * static_cast<int>(sizeof(TZ)) / 16, chG = d / 4;
+  // The CTA has d / 4 threads and a row has d * size / 16 chunks of 16 bytes,
+  // a divisor of it: thread c copies chunk c % chunks of rows c / chunks,
+  // c / chunks + threads / chunks, ...
+  const int cT = threadIdx.x % chT, rT0 = threadIdx.x / chT, rTs = blockDim.x / chT;
+  const int cZ = threadIdx.x % chZ, rZ0 = threadIdx.x / chZ, rZs = blockDim.x / chZ;
+  const int cG = threadIdx.x % chG, rG0 = threadIdx.x / chG, rGs = blockDim.x / chG;
   auto issue_inputs = [&](int64_t t, int buf) {
-    for (int c = threadIdx.x; c < (n1 + S - 1) * chT; c += blockDim.x) {
-      const int r = c / chT, ch = c - r * chT;
+    const uint32_t dT = smem_u32(inT + static_cast<int64_t>(buf) * rowsT * d) + cT * 16;
+    for (int r = rT0; r < n1 + S - 1; r += rTs) {
       const T* g = r < n1 ? src + r * a.src_stride + t * d : F + (k0 + r - n1) * a.f_stride + t * d;
-      cp_async16(smem_u32(inT + (static_cast<int64_t>(buf) * rowsT + r) * d) + ch * 16,
-                 reinterpret_cast<const char*>(g) + ch * 16, true);
+      cp_async16(dT + r * d * static_cast<int>(sizeof(T)), reinterpret_cast<const char*>(g) + cT * 16, true);
     }
-    for (int c = threadIdx.x; c < S * chZ; c += blockDim.x) {
-      const int r = c / chZ, ch = c - r * chZ;
-      cp_async16(smem_u32(inZ + (static_cast<int64_t>(buf) * S + r) * d) + ch * 16,
-                 reinterpret_cast<const char*>(dz + (k0 + r) * a.dout_stride + t * d) + ch * 16, true);
-    }
+    const uint32_t dZ = smem_u32(inZ + static_cast<int64_t>(buf) * S * d) + cZ * 16;
+    for (int r = rZ0; r < S; r += rZs)
+      cp_async16(dZ + r * d * static_cast<int>(sizeof(TZ)),
+                 reinterpret_cast<const char*>(dz + (k0 + r) * a.dout_stride + t * d) + cZ * 16, true);
   };
   auto issue_grads = [&](int64_t t) {
-    for (int c = threadIdx.x; c < (n1 + S + (has_db ? 1 : 0)) * chG; c += blockDim.x) {
-      const int r = c / chG, ch = c - r * chG;
+    const uint32_t dG = smem_u32(gsm) + cG * 16;
+    for (int r = rG0; r < n1 + S + (has_db ? 1 : 0); r += rGs) {
       const float* g = r < n1 ? a.dVs + r * a.E + t * d
                               : (r < n1 + S ? a.dF + (k0 + r - n1) * a.df_stride + t * d : a.dVs + (a.n + 1) * a.E + t * d);
-      cp_async16(smem_u32(gsm + static_cast<int64_t>(r) * d) + ch * 16, reinterpret_cast<const char*>(g) + ch * 16, true);
+      cp_async16(dG + r * d * 4, reinterpret_cast<const char*>(g) + cG * 16, true);
     }
   };
   int buf = 0;
