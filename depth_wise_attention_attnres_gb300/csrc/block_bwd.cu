@@ -185,11 +185,14 @@ namespace {
 //     the later blocks accumulated.
 constexpr int kBX = 8;              // cross-block sources at most (n + 1)
 constexpr int kBQ = 8;              // sublayers (reads) per block at most
-constexpr int kBV = 160;            // reduced values per token (5 x 32)
-// Value layout: [0, 8) sum X_i^2; [8, 16) sum P_j^2 (j >= 1); [16, 80) X_i.u_j
-// at 16 + 8 j + i; [80, 144) dz_j.X_i at 80 + 8 j + i; [144, 152) P_j.u_j;
-// [152, 160) dz_j.P_j.
-constexpr int kOffSsP = 8, kOffEX = 16, kOffDaX = 80, kOffEP = 144, kOffDaP = 152;
+// Values reduced per token, for at most NX cross-block sources: [0, NX)
+// sum X_i^2; then 8 sum P_j^2 (j >= 1); X_i.u_j at EX + NX j + i; dz_j.X_i at
+// DaX + NX j + i; 8 P_j.u_j; 8 dz_j.P_j. Reduced 32 at a time.
+template <int NX> struct BwdLayout {
+  static constexpr int SsP = NX, EX = NX + kBQ, DaX = EX + kBQ * NX, EP = DaX + kBQ * NX, DaP = EP + kBQ;
+  static constexpr int V = DaP + kBQ;
+  static constexpr int Rounds = (V + 31) / 32;
+};
 
 __device__ __forceinline__ float dot4(const float (&a)[4], const float (&b)[4]) {
   return fmaf(a[0], b[0], fmaf(a[1], b[1], fmaf(a[2], b[2], a[3] * b[3])));
@@ -206,8 +209,11 @@ inline int64_t block_bwd_smem(const BlockBwdArgs& a) {
          static_cast<int64_t>(n1 + a.S + 1) * a.d * 4;
 }
 
-template <typename T, typename TZ>
+template <typename T, typename TZ, int NX>
 __global__ void __launch_bounds__(1024 / 128 * 32, 1) block_bwd_batched_kernel(BlockBwdArgs a) {
+  using Lay = BwdLayout<NX>;
+  constexpr int kOffSsP = Lay::SsP, kOffEX = Lay::EX, kOffDaX = Lay::DaX, kOffEP = Lay::EP, kOffDaP = Lay::DaP;
+  constexpr int kBV = Lay::Rounds * 32;
   extern __shared__ __align__(16) unsigned char bsm[];
   __shared__ float red[8][kBV];      // per-warp sums
   __shared__ float tot[kBV];         // CTA sums
@@ -289,9 +295,9 @@ __global__ void __launch_bounds__(1024 / 128 * 32, 1) block_bwd_batched_kernel(B
     const T* xs = inT + static_cast<int64_t>(buf) * rowsT * d;
     const TZ* zsm = inZ + static_cast<int64_t>(buf) * S * d;
     // ---- 1. partial dot products of this lane's features
-    float x[kBX][4], p[kBQ][4], z[kBQ][4];
+    float x[NX][4], p[kBQ][4], z[kBQ][4];
 #pragma unroll
-    for (int i = 0; i < kBX; ++i) {
+    for (int i = 0; i < NX; ++i) {
       if (i < n1) lds4(xs + i * d + k, x[i]);
       else x[i][0] = x[i][1] = x[i][2] = x[i][3] = 0.f;
     }
@@ -313,17 +319,18 @@ __global__ void __launch_bounds__(1024 / 128 * 32, 1) block_bwd_batched_kernel(B
       else z[j][0] = z[j][1] = z[j][2] = z[j][3] = 0.f;
     }
 #pragma unroll
-    for (int r = 0; r < kBV / 32; ++r) {
+    for (int r = 0; r < Lay::Rounds; ++r) {
       float v[32];
 #pragma unroll
       for (int m = 0; m < 32; ++m) {
         const int idx = r * 32 + m;
         if (idx < kOffSsP) v[m] = dot4(x[idx], x[idx]);
         else if (idx < kOffEX) v[m] = dot4(p[idx - kOffSsP], p[idx - kOffSsP]);
-        else if (idx < kOffDaX) v[m] = dot4(x[(idx - kOffEX) & 7], u[(idx - kOffEX) >> 3]);
-        else if (idx < kOffEP) v[m] = dot4(x[(idx - kOffDaX) & 7], z[(idx - kOffDaX) >> 3]);
+        else if (idx < kOffDaX) v[m] = dot4(x[(idx - kOffEX) % NX], u[(idx - kOffEX) / NX]);
+        else if (idx < kOffEP) v[m] = dot4(x[(idx - kOffDaX) % NX], z[(idx - kOffDaX) / NX]);
         else if (idx < kOffDaP) v[m] = dot4(p[idx - kOffEP], u[idx - kOffEP]);
-        else v[m] = dot4(p[idx - kOffDaP], z[idx - kOffDaP]);
+        else if (idx < Lay::V) v[m] = dot4(p[idx - kOffDaP], z[idx - kOffDaP]);
+        else v[m] = 0.f;
       }
       // Reduce-scatter over the warp: lane l ends with the warp's sum of v[l].
 #pragma unroll
@@ -353,7 +360,7 @@ __global__ void __launch_bounds__(1024 / 128 * 32, 1) block_bwd_batched_kernel(B
       float m = -INFINITY;
       for (int i = 0; i < n1; ++i) {
         rr[i] = rsqrtf(tot[i] * inv_d + a.eps);
-        e[i] = rr[i] * tot[kOffEX + 8 * j + i];
+        e[i] = rr[i] * tot[kOffEX + NX * j + i];
         m = fmaxf(m, e[i]);
       }
       float rP = 0.f, eP = 0.f;
@@ -373,12 +380,12 @@ __global__ void __launch_bounds__(1024 / 128 * 32, 1) block_bwd_batched_kernel(B
       float sda = 0.f;
       for (int i = 0; i < n1; ++i) {
         aa[i] *= inv;
-        sda = fmaf(aa[i], tot[kOffDaX + 8 * j + i], sda);
+        sda = fmaf(aa[i], tot[kOffDaX + NX * j + i], sda);
       }
       aP *= inv;
       if (j >= 1) sda = fmaf(aP, tot[kOffDaP + j], sda);
       for (int i = 0; i < n1; ++i) {
-        const float de = aa[i] * (tot[kOffDaX + 8 * j + i] - sda);
+        const float de = aa[i] * (tot[kOffDaX + NX * j + i] - sda);
         alpha[i][j] = aa[i];
         beta[i][j] = rr[i] * de;
         ctmp[i][j] = de * e[i] * rr[i] * rr[i] * inv_d;
@@ -400,7 +407,7 @@ __global__ void __launch_bounds__(1024 / 128 * 32, 1) block_bwd_batched_kernel(B
     __syncthreads();
     // ---- 3. gradients of this lane's features
 #pragma unroll
-    for (int i = 0; i < kBX; ++i) {
+    for (int i = 0; i < NX; ++i) {
       if (i < n1) {
         float g[4];
 #pragma unroll
@@ -471,12 +478,15 @@ bool block_bwd_batched_ok(const BlockBwdArgs& a) {
          (a.dout_stride * zs) % 16 == 0 && (a.df_stride * 4) % 16 == 0;
 }
 
-cudaError_t launch_block_bwd_batched(const BlockBwdArgs& a, cudaStream_t s) {
+namespace {
+
+template <int NX>
+cudaError_t launch_block_bwd_nx(const BlockBwdArgs& a, cudaStream_t s) {
   const int threads = a.d / 128 * 32;
-  const void* fn = a.bf16 ? (a.dz_bf16 ? reinterpret_cast<const void*>(&block_bwd_batched_kernel<bf16, bf16>)
-                                       : reinterpret_cast<const void*>(&block_bwd_batched_kernel<bf16, float>))
-                          : (a.dz_bf16 ? reinterpret_cast<const void*>(&block_bwd_batched_kernel<float, bf16>)
-                                       : reinterpret_cast<const void*>(&block_bwd_batched_kernel<float, float>));
+  const void* fn = a.bf16 ? (a.dz_bf16 ? reinterpret_cast<const void*>(&block_bwd_batched_kernel<bf16, bf16, NX>)
+                                       : reinterpret_cast<const void*>(&block_bwd_batched_kernel<bf16, float, NX>))
+                          : (a.dz_bf16 ? reinterpret_cast<const void*>(&block_bwd_batched_kernel<float, bf16, NX>)
+                                       : reinterpret_cast<const void*>(&block_bwd_batched_kernel<float, float, NX>));
   const int smem = static_cast<int>(block_bwd_smem(a));
   cudaError_t e = allow_dynamic_smem(fn, smem);
   if (e != cudaSuccess) return e;
@@ -484,13 +494,20 @@ cudaError_t launch_block_bwd_batched(const BlockBwdArgs& a, cudaStream_t s) {
   if (grid > a.T) grid = a.T;
   const unsigned g = static_cast<unsigned>(grid > 0 ? grid : 1);
   if (a.bf16) {
-    if (a.dz_bf16) block_bwd_batched_kernel<bf16, bf16><<<g, threads, smem, s>>>(a);
-    else block_bwd_batched_kernel<bf16, float><<<g, threads, smem, s>>>(a);
+    if (a.dz_bf16) block_bwd_batched_kernel<bf16, bf16, NX><<<g, threads, smem, s>>>(a);
+    else block_bwd_batched_kernel<bf16, float, NX><<<g, threads, smem, s>>>(a);
   } else {
-    if (a.dz_bf16) block_bwd_batched_kernel<float, bf16><<<g, threads, smem, s>>>(a);
-    else block_bwd_batched_kernel<float, float><<<g, threads, smem, s>>>(a);
+    if (a.dz_bf16) block_bwd_batched_kernel<float, bf16, NX><<<g, threads, smem, s>>>(a);
+    else block_bwd_batched_kernel<float, float, NX><<<g, threads, smem, s>>>(a);
   }
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_block_bwd_batched(const BlockBwdArgs& a, cudaStream_t s) {
+  const int n1 = a.n + 1;
+  return n1 <= 2 ? launch_block_bwd_nx<2>(a, s) : n1 <= 4 ? launch_block_bwd_nx<4>(a, s) : launch_block_bwd_nx<8>(a, s);
 }
 
 }  // namespace attnres
