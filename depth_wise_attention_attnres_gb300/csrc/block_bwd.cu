@@ -1,5 +1,7 @@
-// Elementwise kernels of the Block pass backward (attnres_block_bwd in api.cu
-// drives them around the per-read backward of full_bwd.cu).
+// The Block pass backward (attnres_block_bwd in api.cu drives these): the
+// batched kernel below, which takes all S reads of a block in one pass, and
+// the elementwise kernels of the per-read path, which runs the Full read's
+// backward (full_bwd.cu) read by read for the other shapes.
 //
 // The Block pass reads, for sublayer k = n * S + j, the sources {embedding,
 // b_1 .. b_n, P_k if j >= 1} (DepthBench reading notes section 2.5; LLMRes
@@ -168,8 +170,10 @@ namespace {
 // to 1024, at most 8 cross-block sources and 8 sublayers per block). A CTA
 // has d / 128 warps; warp w owns features 128 w .. 128 w + 127 (4 per lane)
 // for every token, so the query-gradient sums du_j stay in its registers for
-// the whole launch. Per token:
-//  1. each lane loads its features of the block's sources X_0 .. X_n, the
+// the whole launch. A token's rows come into shared memory by cp.async: the
+// next token's sources, outputs and dL/dout double-buffered, the token's own
+// fp32 gradient rows fetched as it starts. Per token:
+//  1. each lane reads its features of the block's sources X_0 .. X_n, the
 //     running sums P_j (rebuilt from the outputs with the forward's fp32
 //     additions) and dL/dout_j, and forms its parts of every dot product the
 //     reads need: sum X_i^2, sum P_j^2, X_i . u_j, P_j . u_j, dz_j . X_i and
