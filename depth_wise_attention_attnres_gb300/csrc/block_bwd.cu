@@ -8,8 +8,8 @@
 // blog, "Block Attention Residuals"): b_m is the plain sum of block (m-1)'s
 // outputs and P_k the sum of the earlier outputs of block n. By the chain rule
 // the gradient of b_m reaches every member of block m-1 unchanged, and that of
-// P_k every output of block n before k. The backward runs the reads in
-// reverse order over fp32 copies of the sources; these kernels widen the
+// P_k every output of block n before k. The per-read path runs the reads in
+// reverse order over fp32 copies of the sources; its kernels widen the
 // sources, rebuild the running sums as the forward formed them (the same fp32
 // additions in the same order), and route the summaries' and running sums'
 // gradients to the outputs.
