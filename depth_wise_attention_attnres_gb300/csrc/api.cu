@@ -1,6 +1,8 @@
 // C ABI of the AttnRes aggregation library: argument checks, kernel choice,
 // pass sequencing and device status. Every computation runs in the kernels of
 // full_fwd.cu, stage1.cu, merge.cu and generic.cu.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <map>
@@ -48,12 +50,27 @@ cudaError_t allow_dynamic_smem(const void* kernel, int bytes) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  if (bytes > 48 * 1024) {
+  // Without the attribute, static and dynamic shared memory together are
+  // held to 48 KB, so it is set for any dynamic size.
+  if (bytes > 0) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
   }
   g_smem_set[key] = bytes;
   return cudaSuccess;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
 }
 
 int blocks_per_sm(const void* kernel, int threads, int smem_bytes) {
@@ -704,15 +721,15 @@ int attnres_device_status(void* stream) {
     cudaGetLastError();
     return ATTNRES_ERR_CUDA;
   }
-  unsigned int f1 = 0, f2 = 0, f3 = 0, f4 = 0, f5 = 0, f6 = 0, f7 = 0;
+  unsigned int f1 = 0, f2 = 0, f3 = 0, f4 = 0, f5 = 0, f6 = 0, f7 = 0, f8 = 0;
   if (take_timeout_full(&f1) != cudaSuccess || take_timeout_stage1(&f2) != cudaSuccess ||
       take_timeout_merge(&f3) != cudaSuccess || take_timeout_stage1tc(&f4) != cudaSuccess ||
       take_timeout_bwd(&f5) != cudaSuccess || take_timeout_proj(&f6) != cudaSuccess ||
-      take_timeout_dsplit(&f7) != cudaSuccess) {
+      take_timeout_dsplit(&f7) != cudaSuccess || take_timeout_blockbwd(&f8) != cudaSuccess) {
     cudaGetLastError();
     return ATTNRES_ERR_CUDA;
   }
-  if (f1 || f2 || f3 || f4 || f5 || f6 || f7) return ATTNRES_ERR_TIMEOUT;
+  if (f1 || f2 || f3 || f4 || f5 || f6 || f7 || f8) return ATTNRES_ERR_TIMEOUT;
   e = cudaGetLastError();
   return e == cudaSuccess ? ATTNRES_OK : ATTNRES_ERR_CUDA;
 }

@@ -187,22 +187,10 @@ constexpr int kFinPartFloats = 16 * (ATTNRES_MAX_QUERIES + 1);
 __host__ __device__ inline int fin_warp_bytes(int NK) { return 2 * 2 * 16 * 8 * NK * 2 + kFinPartFloats * 4; }
 inline PtGeom fin_geom(int n, int ds) { return ring_geom(n, ds, 0, fin_warp_bytes((n + 7) / 8)); }
 
-PFN_cuTensorMapEncodeTiled_v12000 dsplit_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 // The shard as a 4-d tensor (feature within a 64-feature chunk, source,
 // token, chunk) and the box {64, n, TM, d_s / 64}, 128-byte swizzle.
 bool encode_shard_map(const DsplitArgs& a, const PtGeom& g, CUtensorMap* map) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn = dsplit_encode_fn();
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(a.n_src), static_cast<cuuint64_t>(a.T),
                               static_cast<cuuint64_t>(a.d_shard / 64)};
@@ -792,7 +780,7 @@ __global__ void __launch_bounds__(kDWarps * 32) dsplit_finish_kernel(DsplitArgs 
 
 bool finish_on_tensor_cores(const DsplitArgs& a) {
   if (!a.bf16 || a.d_shard % 64 != 0 || a.n_src > 16 || a.T >= (int64_t(1) << 31)) return false;
-  return dsplit_encode_fn() != nullptr && fin_geom(a.n_src, a.d_shard).W >= 1;
+  return tensor_map_encode_fn() != nullptr && fin_geom(a.n_src, a.d_shard).W >= 1;
 }
 
 template <int NK, int R>
@@ -839,7 +827,7 @@ cudaError_t launch_finish_t(const DsplitArgs& a, cudaStream_t s) {
 
 bool partials_on_tensor_cores(const DsplitArgs& a) {
   if (!a.bf16 || a.d_shard % 64 != 0 || a.n_src > 256 || a.T >= (int64_t(1) << 31)) return false;
-  if (!aligned16(a.W) || !aligned16(a.Gamma) || dsplit_encode_fn() == nullptr) return false;
+  if (!aligned16(a.W) || !aligned16(a.Gamma) || tensor_map_encode_fn() == nullptr) return false;
   return pt_geom(a.n_src, a.d_shard, a.S <= 8 ? 1 : 2).W >= 1;
 }
 

@@ -1,6 +1,8 @@
 // Internal launcher interface between the C ABI layer and the kernel files.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -161,6 +163,10 @@ bool dsplit_ok(const DsplitArgs& a);
 cudaError_t launch_dsplit_partials(const DsplitArgs& a, cudaStream_t s);
 cudaError_t launch_dsplit_finish(const DsplitArgs& a, cudaStream_t s);
 cudaError_t take_timeout_dsplit(unsigned int* flag);
+cudaError_t take_timeout_blockbwd(unsigned int* flag);
+// The driver's cuTensorMapEncodeTiled, looked up once (nullptr if the driver
+// lacks it).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encode_fn();
 cudaError_t launch_full_bwd(const BwdArgs& a, cudaStream_t s, bool fast);
 // One block's reads in the batched Block backward (block_bwd.cu).
 struct BlockBwdArgs {

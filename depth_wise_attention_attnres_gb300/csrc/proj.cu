@@ -378,21 +378,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 proj_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 // A [rows, d] bf16 operand as a 2-d tensor, box {64, 128}, 128-byte swizzle.
 bool encode_operand(const void* base, int64_t rows, int d, int box_rows, CUtensorMap* map) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn = proj_encode_fn();
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
@@ -453,7 +441,7 @@ cudaError_t launch_proj_tc(const void* H, const void* Wq, float* Q, int64_t T, i
 
 bool proj_tc_ok(const void* H, const void* Wq, const float* Q, int64_t T, int d) {
   return proj_tile_n(d, T) != 0 && aligned16(H) && aligned16(Wq) && aligned16(Q) && T < (int64_t(1) << 31) &&
-         (T + kTBM - 1) / kTBM <= 0x7fffffff && proj_encode_fn() != nullptr;
+         (T + kTBM - 1) / kTBM <= 0x7fffffff && tensor_map_encode_fn() != nullptr;
 }
 
 cudaError_t take_timeout_proj(unsigned int* flag) {

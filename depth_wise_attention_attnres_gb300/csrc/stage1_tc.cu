@@ -582,22 +582,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!ok) atomicOr(&g_stage1tc_timeout, 1u);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 // The sources as a 4-d tensor (feature within chunk, source, token, chunk) and
 // the tile box {64, n, TM, d / 64}, 128-byte swizzle.
 bool encode_tile_map(const MultiArgs& a, const TcGeom& g, CUtensorMap* map) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(a.n_src), static_cast<cuuint64_t>(a.T),
                               static_cast<cuuint64_t>(a.d / 64)};
@@ -638,7 +626,7 @@ bool stage1_tc_ok(const MultiArgs& a) {
   for (int j = 0; j < a.S; ++j)
     if (!aligned16(a.out[j])) return false;
   const TcGeom g = tc_geom(a.n_src, a.d, a.S);
-  return g.TM >= 1 && g.nbuf >= 2 && g.total <= kSmemLimit && encode_fn() != nullptr;
+  return g.TM >= 1 && g.nbuf >= 2 && g.total <= kSmemLimit && tensor_map_encode_fn() != nullptr;
 }
 
 cudaError_t launch_stage1_tc(const MultiArgs& a, cudaStream_t s) {

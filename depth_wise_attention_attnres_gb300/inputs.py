@@ -65,6 +65,12 @@ WORKLOADS = {
     "block_pass_8x8x16384x1024_bf16": Workload(
         "block_pass_8x8x16384x1024_bf16", "block_pass", T=16384, d=1024,
         dtype="bf16", w_std=0.02, N=8, S=8, depth_scaled=False),
+    # The same blocks at 2048 tokens (about 1.2 GB on the device with the
+    # backward's buffers): a case small enough for profiler captures whose
+    # per-launch data still exceeds the 129 MB L2.
+    "block_pass_8x8x2048x1024_bf16": Workload(
+        "block_pass_8x8x2048x1024_bf16", "block_pass", T=2048, d=1024,
+        dtype="bf16", w_std=0.02, N=8, S=8, depth_scaled=False),
     # Deep-narrow 70 layers x d=640: 140 sublayers + the LM-head read.
     "full_pass_141x32768x640_bf16": Workload(
         "full_pass_141x32768x640_bf16", "full_pass", T=32768, d=640,

@@ -46,7 +46,9 @@ def test_standard_single_read_f32():
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("n,T,d", [(1, 37, 128), (2, 8, 256), (5, 100, 384), (9, 1000, 896),
-                                   (17, 257, 640), (3, 64, 1024), (4, 33, 2048)])
+                                   (17, 257, 640), (3, 64, 1024), (4, 33, 2048),
+                                   # many sources, one token
+                                   (64, 9, 1024), (300, 5, 128), (6, 1, 896)])
 def test_fast_read_vs_oracle(dt, n, T, d):
     out, ref = _read_case(n, T, d, dt)
     assert rel_err(out, ref) <= TOL[dt]
