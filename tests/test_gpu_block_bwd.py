@@ -41,7 +41,9 @@ def _forward(N, S, T, d, dt, seed):
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("N,S,T,d", [(3, 4, 33, 256), (2, 3, 17, 100), (4, 1, 9, 128), (1, 5, 20, 384),
-                                     (2, 2, 40, 1024), (1, 1, 1, 64), (2, 2, 1, 37), (9, 2, 5, 128)])
+                                     (2, 2, 40, 1024), (1, 1, 1, 64), (2, 2, 1, 37), (9, 2, 5, 128),
+                                     # batched: 8 blocks of 8 with fewer tokens than CTAs; one token
+                                     (8, 8, 19, 256), (3, 3, 1, 128)])
 def test_block_bwd_vs_oracle(dt, N, S, T, d):
     Src, F, W, G, dOut = _forward(N, S, T, d, dt, 70)
     dEmb = torch.zeros(T, d, device=dev())
