@@ -211,9 +211,11 @@ template <int NX> struct BwdLayout {
   static constexpr int Rounds = (V + 31) / 32;
 };
 // TC instance: the reduced matrix is R . [R | u | dz], 16 rows of 32 columns
-// (0-15 the Gram matrix, 16-23 R . u_j, 24-31 R . dz_j); a warp's partials are
-// stored with rows 40 floats apart, so its fragment stores hit distinct banks.
-constexpr int kTcCols = 32, kTcLd = 40;
+// (0-15 the Gram matrix, 16-23 R . u_j, 24-31 R . dz_j). A warp's partials
+// are stored with rows 40 floats apart, so its fragment stores hit distinct
+// banks; the CTA sums with rows 33 apart, so the lanes of a read's group,
+// one row each, do too.
+constexpr int kTcCols = 32, kTcLd = 40, kTcTot = 33;
 
 // Shared-memory row strides (elements): 16 bytes of padding, so the eight
 // 16-byte rows one ldmatrix reads fall in distinct banks.
@@ -291,12 +293,15 @@ __global__ void __launch_bounds__(1024 / 128 * 32, 1)
   constexpr int kOffSsP = Lay::SsP, kOffEX = Lay::EX, kOffDaX = Lay::DaX, kOffEP = Lay::EP, kOffDaP = Lay::DaP;
   constexpr int kBV = Lay::Rounds * 32;
   constexpr int kRedW = TC ? 16 * kTcLd : kBV, kTot = TC ? 16 * kTcCols : kBV;
+  constexpr int kTotSize = TC ? 16 * kTcTot : kBV;
   extern __shared__ __align__(16) unsigned char bsm[];
   __shared__ __align__(16) float red[8][kRedW];  // per-warp sums
-  __shared__ float tot[kTot];                    // CTA sums
-  __shared__ __align__(16) float alpha[kBX][kBQ];  // coefficient of dz_j in dX_i
-  __shared__ __align__(16) float beta[kBX][kBQ];   // coefficient of u_j in dX_i (r_i de_ij; also of X_i in du_j)
-  __shared__ float ctmp[kBX][kBQ];   // de_ij e_ij r_i^2 / d, summed over j into cx[i]
+  __shared__ float tot[kTotSize];                // CTA sums
+  // Coefficients, rows padded (12 and 9 floats) so the per-read step's
+  // writes, one source row a lane, hit distinct banks.
+  __shared__ __align__(16) float alpha[kBX][kBQ + 4];  // coefficient of dz_j in dX_i
+  __shared__ __align__(16) float beta[kBX][kBQ + 4];   // coefficient of u_j in dX_i (r_i de_ij; also of X_i in du_j)
+  __shared__ float ctmp[kBX][kBQ + 1];                 // de_ij e_ij r_i^2 / d, summed over j into cx[i]
   __shared__ float cx[kBX];
   __shared__ __align__(16) float pa[kBQ];  // the same for P_j (j >= 1)
   __shared__ __align__(16) float pb[kBQ];
@@ -526,7 +531,7 @@ __global__ void __launch_bounds__(1024 / 128 * 32, 1)
       const int ri = TC ? (i >> 5) * kTcLd + (i & 31) : i;
       float s = 0.f;
       for (int ww = 0; ww < W; ++ww) s += red[ww][ri];
-      tot[i] = s;
+      tot[TC ? (i >> 5) * kTcTot + (i & 31) : i] = s;
     }
     __syncthreads();
     // The next token's inputs, issued while the per-read step runs; their
@@ -536,9 +541,9 @@ __global__ void __launch_bounds__(1024 / 128 * 32, 1)
       if (buf) pend0 = true; else pend1 = true;
     }
     // The reduced dot products of the sources: sum X_i^2, X_i . u_j, dz_j . X_i.
-    auto ssx = [&](int i) { return TC ? tot[i * (kTcCols + 1)] : tot[i]; };
-    auto ex = [&](int i, int j) { return TC ? tot[i * kTcCols + 16 + j] : tot[kOffEX + NX * j + i]; };
-    auto dax = [&](int i, int j) { return TC ? tot[i * kTcCols + 24 + j] : tot[kOffDaX + NX * j + i]; };
+    auto ssx = [&](int i) { return TC ? tot[i * (kTcTot + 1)] : tot[i]; };
+    auto ex = [&](int i, int j) { return TC ? tot[i * kTcTot + 16 + j] : tot[kOffEX + NX * j + i]; };
+    auto dax = [&](int i, int j) { return TC ? tot[i * kTcTot + 24 + j] : tot[kOffDaX + NX * j + i]; };
     // ---- 2. per read: scores, softmax, score gradients, coefficients. Read
     // j goes to a group of 16 lanes: lane i < n1 takes source i, lane n1 the
     // running sum (j >= 1); the softmax sums run over the group by shuffles.
@@ -553,7 +558,7 @@ __global__ void __launch_bounds__(1024 / 128 * 32, 1)
         float ssp = 0.f, ep = 0.f, dap = 0.f;
         if constexpr (TC) {
           if (gl < j) {
-            const float* row = tot + (n1 + gl) * kTcCols;
+            const float* row = tot + (n1 + gl) * kTcTot;
 #pragma unroll
             for (int m2 = 0; m2 < kBQ - 1; ++m2)
               if (m2 < j) ssp += row[n1 + m2];
