@@ -141,8 +141,9 @@ cudaError_t launch_proj_generic(const void* H, const void* Wq, float* Q, int64_t
 // by 2-d TMA copies with the 128-byte swizzle into 4 stages; one thread issues
 // tcgen05.mma (M = 128, N = 128, K = 16, bf16 x bf16 -> fp32), and
 // tcgen05.commit frees a stage once the MMAs that read it are done. The four
-// warps then read their 32-lane quarter of the accumulator with tcgen05.ld and
-// store their rows. Every wait is bounded; whatever happens, the CTA waits for
+// epilogue warps then read their 32-lane quarter of the accumulator with
+// tcgen05.ld and store it through a small shared-memory staging block, as
+// whole 128-byte row segments. Every wait is bounded; whatever happens, the CTA waits for
 // the MMAs it issued and the copies in flight and frees its tensor memory.
 namespace {
 
@@ -152,9 +153,12 @@ __device__ unsigned int g_proj_timeout = 0;
 // N; wider tiles read fewer operand bytes per product from L2).
 constexpr int kTBM = 128, kTBK = 64, kTStages = 4;
 constexpr int kTTileBytes = kTBM * kTBK * 2;           // the A tile of a stage, 16 KB
+// Epilogue staging: per epilogue warp, a 32 x 32 fp32 block in rows of 36
+// floats (16-byte aligned; 16-byte accesses by 8 lanes hit distinct banks).
+constexpr int kEpiLd = 36, kEpiWarpFloats = 32 * kEpiLd;
 template <int BN> struct TcTile {
   static constexpr int kStageBytes = kTTileBytes + BN * kTBK * 2;  // A and B
-  static constexpr int kSmem = 1024 + kTStages * kStageBytes + 128;
+  static constexpr int kSmem = 1024 + kTStages * kStageBytes + 128 + 4 * kEpiWarpFloats * 4;
   static constexpr uint32_t kTmemCols = BN <= 128 ? 128u : 256u;     // a power of two >= BN
   // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits
   // 4-5), bf16 A (7-9) and B (10-12), both K-major (15, 16), N / 8 (17-22),
@@ -233,6 +237,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* tempty = tfull + 2;             // [2] accumulator drained
   uint64_t* done_bar = tempty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done_bar + 1);
+  float* epi_stage = reinterpret_cast<float*>(smem + kTStages * kTStageBytes + 128);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntn = d / BN;
   const int64_t ntiles = ((T + kTBM - 1) / kTBM) * ntn;
@@ -338,8 +343,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     __syncwarp();
   } else {
-    // Epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. of the tile.
+    // Epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. of the tile
+    // (lane = row), 32 columns at a time, and turns each 32 x 32 block
+    // around in shared memory so one store instruction writes four whole
+    // 128-byte row segments.
     const int q4 = warp & 3;
+    float* stg = epi_stage + (warp - 2) * kEpiWarpFloats;
     for (int64_t i = 0; i < mine; ++i) {
       const int acc = static_cast<int>(i & 1);
       const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull[acc]), static_cast<uint32_t>((i >> 1) & 1)));
@@ -349,18 +358,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int64_t tile = blockIdx.x + i * gridDim.x;
-      const int64_t row = (tile / ntn) * kTBM + q4 * 32 + lane;
+      const int64_t rbase = (tile / ntn) * kTBM + q4 * 32;
       const int n0 = static_cast<int>(tile % ntn) * BN;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(acc) * kAccCols;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         float v[32];
         tmem_ld32(taddr + static_cast<uint32_t>(c * 32), v);
-        if (row < T) {
-          float4* dst = reinterpret_cast<float4*>(Q + row * d + n0 + c * 32);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        for (int e = 0; e < 8; ++e)
+          *reinterpret_cast<float4*>(stg + lane * kEpiLd + 4 * e) =
+              make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          const int r = h * 4 + (lane >> 3);
+          const float4 x = *reinterpret_cast<const float4*>(stg + r * kEpiLd + 4 * (lane & 7));
+          if (rbase + r < T)
+            *reinterpret_cast<float4*>(Q + (rbase + r) * d + n0 + c * 32 + 4 * (lane & 7)) = x;
         }
+        __syncwarp();
       }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
@@ -392,11 +409,11 @@ bool encode_operand(const void* base, int64_t rows, int d, int box_rows, CUtenso
 }
 
 // Output tile width: the widest that divides d (fewer operand bytes per
-// product), except for small products, where 128-wide tiles (at most three
-// per CTA) spread more evenly over the SMs: at 8192 x 896 they took 20.3 us
-// against 22.5 us for 224-wide ones.
+// product), except when 128-wide tiles fit in one wave over the SMs, where
+// more tiles spread the work further. At 8192 x 896 the widest (224) takes
+// 14.4 us against 16.8 us for 128-wide tiles.
 inline int proj_tile_n(int d, int64_t T) {
-  if (d % 128 == 0 && ((T + kTBM - 1) / kTBM) * (d / 128) <= 3 * static_cast<int64_t>(sm_count())) return 128;
+  if (d % 128 == 0 && ((T + kTBM - 1) / kTBM) * (d / 128) <= static_cast<int64_t>(sm_count())) return 128;
   const int cands[5] = {256, 224, 192, 160, 128};
   for (int c : cands)
     if (d % c == 0) return c;
