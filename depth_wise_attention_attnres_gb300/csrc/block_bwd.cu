@@ -235,9 +235,9 @@ __device__ __forceinline__ float dot4(const float (&a)[4], const float (&b)[4]) 
 }
 
 // Dynamic shared memory of the batched kernel: the next token's inputs
-// (sources and outputs in T, dL/dout in TZ, double-buffered by cp.async) and
-// the current token's fp32 gradient rows to update (sources', outputs', and
-// the block summary's).
+// (sources and outputs in T, dL/dout in TZ, double-buffered, rows padded)
+// and the current token's fp32 gradient rows to update (sources', the block
+// summary's, outputs'), 128-byte aligned.
 inline int64_t block_bwd_smem(const BlockBwdArgs& a) {
   const int n1 = a.N;  // sized for the largest block (n + 1 = N)
   const int es = a.bf16 ? 2 : 4, zs = a.dz_bf16 ? 2 : 4;
