@@ -207,7 +207,13 @@ def measured_peaks() -> dict:
 # kernel source it was taken with: reported as null once the source changes.
 # full_fwd_bulk_kernel: the 21-source read (sublayer 20) of the 8192 x 896 pass,
 # 308.31 MB read + 11.15 MB written for 322.96 MB algorithmic.
-NCU_TRAFFIC = {("full_fwd_bulk_kernel", "7cc92f36c701ba29"): (308.313344 + 11.152128) / 322.961408}
+# block_bwd_batched_kernel: all 8 launches of one 8x8 Block backward at 2048
+# tokens, 1554.1 MB read + 420.6 MB written for the step's 2483.0 MB
+# algorithmic (reads equal the algorithmic reads; the rest of the writes were
+# still in L2 when ncu flushed it between launches). The per-launch traffic
+# grows with the tokens.
+NCU_TRAFFIC = {("full_fwd_bulk_kernel", "7cc92f36c701ba29"): (308.313344 + 11.152128) / 322.961408,
+               ("block_bwd_batched_kernel", "cb4b0fb7ff058c27"): (1554.098176 + 420.645888) / 2483.027968}
 
 
 def kernel_digest(name: str) -> str:
@@ -710,11 +716,13 @@ def ours(args):
     elif isinstance(step, BlockBwdStep):
         g = step.byte_parts["total"] / (ms / 1e3) / 1e9
         batched = step.launches == step.wl.N + 1
+        ratio = NCU_TRAFFIC.get(("block_bwd_batched_kernel", kernel_digest("block_bwd.cu"))) if batched else None
         line["roofline"] = {
             "kernel": "block_bwd_batched_kernel" if batched else "full_bwd_bulk_kernel", "bound": "hbm",
             "achieved": g, "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": g / peaks["hbm_gbs"], "frac_of_nominal_8000": g / NOMINAL_HBM_GBS,
-            "peak_source": peaks["source"], "traffic": None,
+            "peak_source": peaks["source"],
+            "traffic": None if ratio is None else ratio * step.byte_parts["total"] / step.wl.N,
             "byte_parts": step.byte_parts,
             "note": "whole step: one batched launch per block (all S reads)" if batched else
                     "whole step: the per-read backward launches carry "
