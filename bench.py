@@ -207,12 +207,16 @@ def measured_peaks() -> dict:
 # kernel source it was taken with: reported as null once the source changes.
 # full_fwd_bulk_kernel: the 21-source read (sublayer 20) of the 8192 x 896 pass,
 # 308.31 MB read + 11.15 MB written for 322.96 MB algorithmic.
+# full_bwd_bulk_kernel: the 44-source read (read 43) of the 8192 x 896 pass
+# backward, 2445.16 MB read + 1231.98 MB written for 3244.29 MB algorithmic
+# (the second pass over a tile's sources re-reads part of them from DRAM).
 # block_bwd_batched_kernel: all 8 launches of one 8x8 Block backward at 2048
 # tokens, 1554.1 MB read + 420.6 MB written for the step's 2483.0 MB
 # algorithmic (reads equal the algorithmic reads; the rest of the writes were
 # still in L2 when ncu flushed it between launches). The per-launch traffic
 # grows with the tokens.
 NCU_TRAFFIC = {("full_fwd_bulk_kernel", "7cc92f36c701ba29"): (308.313344 + 11.152128) / 322.961408,
+               ("full_bwd_bulk_kernel", "1d4588bb0e4b35ec"): (2445.157632 + 1231.980032) / 3244.294144,
                ("block_bwd_batched_kernel", "cb4b0fb7ff058c27"): (1554.098176 + 420.645888) / 2483.027968}
 
 
