@@ -4,11 +4,23 @@
 // per-layer d x d matrix instead of the fixed learned pseudo-query; LLMRes
 // blog, on the paper's ablation).
 //
-// A dense contraction, so it runs on the tensor cores: 128 x 128 output tiles
-// per CTA, 8 warps of 64 x 32, K in steps of 32 staged by a 3-deep cp.async
-// pipeline into shared rows padded to 80 bytes (ldmatrix without bank
-// conflicts), m16n8k16 bf16 MMAs with fp32 accumulation. bf16 products are
-// exact in fp32, so Q carries only the fp32 rounding of the sums.
+// A dense contraction, so it runs on the tensor cores. Three kernels, chosen
+// by attnres_query_projection in this order:
+//   proj_tc_kernel, the path that runs whenever d is a multiple of 128, 160,
+//     192, 224 or 256, the operands are 16-byte aligned and the driver can
+//     encode tensor maps: 5th-generation tensor cores. Persistent, one CTA
+//     per SM over 128 x BN output tiles; a TMA warp streams 128-byte-swizzled
+//     operand stages, one thread issues tcgen05.mma (M = 128, N = BN,
+//     K = 16) into one of two fp32 accumulators in tensor memory, and four
+//     epilogue warps drain the other with tcgen05.ld through a small shared
+//     staging block (section "tcgen05 path" below).
+//   proj_kernel (fallback when no tensor map is available, d a multiple of
+//     128): warp-level m16n8k16 bf16 MMAs, 128 x 128 tiles per CTA, 8 warps of
+//     64 x 32, K in steps of 32 staged by a 3-deep cp.async pipeline into
+//     rows padded to 80 bytes (ldmatrix without bank conflicts).
+//   proj_generic_kernel: any other shape, plain fp32 FMAs.
+// bf16 products are exact in fp32, so Q carries only the fp32 rounding of
+// the sums on every path.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
