@@ -1,24 +1,33 @@
 """Benchmark of the AttnRes depth-wise aggregation on GB300.
 
 One step = one pass of the aggregation hot path over one batch of synthetic
-inputs already resident in HBM. The default workload is the Full AttnRes pass
-of the 400M model at its 32-layer shape: 64 sublayer reads, read r aggregating
-the embedding and the r earlier outputs, d = 896, T = 4 x 2048 tokens, bf16
-storage with fp32 arithmetic. The Block AttnRes pass (8 blocks of 8, d = 1024,
-T = 16384) is measured in the same run and reported under "block".
+inputs already resident in HBM. The default (headline) workload is the
+long-context prefill Block AttnRes pass: T = 131072 tokens (128K), d = 2048,
+48 sublayers in 8 blocks of 6, bf16 storage with fp32 arithmetic; every
+sublayer's read runs by the two-stage computation (stage 1 per block, one
+online-softmax merge per later sublayer, a freeze per block summary). This is
+the largest single-GPU footprint of the standard workloads (about 60 GB
+resident). The other bench workloads are measured in the same run and
+reported under "extras": the deep-narrow Full pass (141 reads, 32768 x 640),
+the 400M Full pass (64 reads, 8192 x 896) and the 8 x 8 Block pass (16384 x
+1024).
 
 Prints one JSON line (rank 0). Metric: tokens/s (higher is better), with the
-HBM roofline of the dominant kernel. ``--impl reference`` times the fp64 CPU
+HBM roofline of the dominant kernel. The K timed steps follow the benchmark
+contract; a separate "sustained" measurement replays the same step for at
+least 2 s with its own clock samples. ``--impl reference`` times the fp64 CPU
 oracle on the same workload instead (a bounded sample of token rows per step).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--workload NAME]
+                       [--workload NAME] [--op OP] [--no-e2e] [--no-extras]
+                       [--no-cpu-baseline] [--no-sustained]
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -33,9 +42,12 @@ sys.path.insert(0, ROOT)
 from depth_wise_attention_attnres_gb300 import inputs  # noqa: E402
 
 METRIC = "AttnRes aggregation tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
-DEFAULT_WORKLOAD = "full_pass_64x8192x896_bf16"
+DEFAULT_WORKLOAD = "block_pass_8x6x131072x2048_bf16"
 NOMINAL_HBM_GBS = 8000.0  # the nominal HBM bandwidth the target is stated against
-BLOCK_WORKLOAD = "block_pass_8x8x16384x1024_bf16"
+# Measured in the same run as the headline (when it is not one of them).
+EXTRA_WORKLOADS = ["full_pass_141x32768x640_bf16", "full_pass_64x8192x896_bf16",
+                   "block_pass_8x8x16384x1024_bf16"]
+SUSTAINED_S = 2.0  # length of the separate sustained measurement
 
 
 # ----------------------------------------------------------------- bytes ----
@@ -46,21 +58,30 @@ def full_pass_bytes(R: int, T: int, d: int, es: int) -> int:
     return sum(r + 2 for r in range(R)) * T * d * es
 
 
-def block_pass_bytes(N: int, S: int, T: int, d: int, es: int, freeze_last: bool = False) -> dict:
+def block_pass_bytes(N: int, S: int, T: int, d: int, es: int, plan=None, freeze_last: bool = False) -> dict:
     """Algorithmic bytes per kernel of the two-stage Block pass.
 
     stage 1 of block n (n+1 sources): reads (n+1) rows, writes S output rows
-    and S lse values per token. Merge j=1: reads O_j and f (P empty), writes P
-    and out. Merge j>=2: also reads P. Freeze: reads P and f, writes b.
+    and S lse values per token. Merge j (1 <= j < S): reads O_j, lse_j and its
+    running sum P_j as the last kept sum P_m (fp32, if m > 0) plus the j - m
+    outputs since, writes out_j and, if the plan keeps P_j, P_j (fp32). The
+    freeze reads P_S the same way and writes the summary. plan[j] = 1 where
+    the pass keeps P_j (attnres_block_running_sum_plan); None keeps every sum
+    (the one-step merges).
     """
+    if plan is None:
+        plan = [0] + [1] * (S - 1) + [0]
     E = T * d
     st1 = merge = freeze = 0
     for n in range(N):
         st1 += (n + 1) * E * es + S * E * es + S * T * 4
+        m = 0
         for j in range(1, S):
-            merge += 2 * E * es + T * 4 + 4 * E + E * es + (4 * E if j >= 2 else 0)
+            merge += 2 * E * es + T * 4 + (j - m) * E * es + (4 * E if m > 0 else 0) + (4 * E if plan[j] else 0)
+            if plan[j]:
+                m = j
         if n + 1 < N or freeze_last:
-            freeze += (4 * E if S > 1 else 0) + E * es + E * es
+            freeze += (S - m) * E * es + (4 * E if m > 0 else 0) + E * es
     return {"stage1": st1, "merge": merge, "freeze": freeze, "total": st1 + merge + freeze}
 
 
@@ -220,6 +241,11 @@ NCU_TRAFFIC = {("full_fwd_bulk_kernel", "7cc92f36c701ba29"): (308.313344 + 11.15
                ("block_bwd_batched_kernel", "cb4b0fb7ff058c27"): (1554.098176 + 420.645888) / 2483.027968}
 
 
+KERNEL_FILES = {"full_fwd_bulk_kernel": "full_fwd.cu", "full_bwd_bulk_kernel": "full_bwd.cu",
+                "block_bwd_batched_kernel": "block_bwd.cu", "stage1_tc_kernel": "stage1_tc.cu",
+                "merge_tile_kernel": "merge.cu", "accum_fast_kernel": "merge.cu"}
+
+
 def kernel_digest(name: str) -> str:
     path = os.path.join(ROOT, "depth_wise_attention_attnres_gb300", "csrc", name)
     with open(path, "rb") as fh:
@@ -344,12 +370,35 @@ class BlockPassStep:
         self.out = torch.empty(wl.N * wl.S, wl.T, wl.d, device=dev, dtype=dt)
         self.launches = wl.N + wl.N * (wl.S - 1) + (wl.N - 1)
         es = 2 if wl.dtype == "bf16" else 4
-        self.byte_parts = block_pass_bytes(wl.N, wl.S, wl.T, wl.d, es)
+        self.plan = binding.attnres_block_running_sum_plan(wl.S, binding.BF16 if es == 2 else binding.F32)
+        self.byte_parts = block_pass_bytes(wl.N, wl.S, wl.T, wl.d, es, self.plan)
         self.bytes = self.byte_parts["total"]
 
     def __call__(self):
         self.ar.attnres_block_pass(self.F, self.wl.N, self.wl.S, self.W, self.G, self.wl.eps,
                                    self.Src, self.O, self.lse, self.P, self.out)
+
+    def launch_groups(self):
+        """The pass's launches by kernel kind, each as the per-sublayer API
+        call that makes it (for graph-timing one kind at a time)."""
+        ar, wl, plan = self.ar, self.wl, self.plan
+        groups = {"stage1": [], "merge": [], "freeze": []}
+        for n in range(wl.N):
+            k0 = n * wl.S
+            O = [self.out[k0]] + [self.O[j - 1] for j in range(1, wl.S)]
+            groups["stage1"].append(lambda n=n, k0=k0, O=O: ar.attnres_block_stage1(
+                self.Src, n + 1, self.W[k0:k0 + wl.S], self.G[k0:k0 + wl.S], wl.eps, O, self.lse))
+            m = 0
+            for j in range(1, wl.S):
+                groups["merge"].append(lambda k0=k0, j=j, m=m: ar.attnres_block_merge_parts(
+                    self.O[j - 1], self.lse[j], self.P if m > 0 else None, self.F[k0 + m:], j - m,
+                    self.P if plan[j] else None, self.W[k0 + j], self.G[k0 + j], wl.eps, self.out[k0 + j]))
+                if plan[j]:
+                    m = j
+            if n + 1 < wl.N:
+                groups["freeze"].append(lambda n=n, k0=k0, m=m: ar.attnres_block_summary_parts(
+                    self.P if m > 0 else None, self.F[k0 + m:], wl.S - m, summary_out=self.Src[n + 1]))
+        return groups
 
 
 class DsplitStep:
@@ -500,42 +549,72 @@ def time_graph(step, steps, warmup, world, stream):
 
 
 def time_block_kernels(step, reps, stream):
-    """Per-kernel device time of the Block pass (events around each launch)."""
-    ar, wl = step.ar, step.wl
-    T, d = wl.T, wl.d
-    acc = {"stage1": 0.0, "merge": 0.0, "freeze": 0.0}
-    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    marks = []
+    """Device time per kernel kind of the Block pass, measured the way the
+    step is: each kind's launches of one pass (its stage-1 reads, its merges,
+    its freezes) are captured in a CUDA graph of their own and replayed `reps`
+    times between CUDA events on the launching stream. Returns ms per pass
+    and launches per pass for each kind. The kinds' sum differs from the
+    step's own graph time by the overlap of neighbouring launches."""
+    out = {}
+    for kind, calls in step.launch_groups().items():
+        if not calls:
+            out[kind] = {"ms": 0.0, "launches": 0}
+            continue
+        with torch.cuda.stream(stream):
+            for c in calls:
+                c()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for c in calls:
+                c()
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                graph.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        out[kind] = {"ms": a.elapsed_time(b) / reps, "launches": len(calls)}
+        del graph
+    # Leave the pass's buffers as a full pass leaves them.
     with torch.cuda.stream(stream):
-        for _ in range(reps):
-            for n in range(wl.N):
-                k0 = n * wl.S
-                O = [step.out[k0]] + [step.O[j - 1] for j in range(1, wl.S)]
-                a, b = ev(), ev()
-                a.record(stream)
-                ar.attnres_block_stage1(step.Src, n + 1, step.W[k0:k0 + wl.S], step.G[k0:k0 + wl.S],
-                                        wl.eps, O, step.lse, stream=stream)
-                b.record(stream)
-                marks.append(("stage1", a, b))
-                for j in range(1, wl.S):
-                    a, b = ev(), ev()
-                    a.record(stream)
-                    ar.attnres_block_merge(step.O[j - 1], step.lse[j], step.P, step.F[k0 + j - 1], j == 1,
-                                           step.W[k0 + j], step.G[k0 + j], wl.eps, step.out[k0 + j],
-                                           stream=stream)
-                    b.record(stream)
-                    marks.append(("merge", a, b))
-                if n + 1 < wl.N:
-                    a, b = ev(), ev()
-                    a.record(stream)
-                    ar.attnres_block_summary_accumulate(step.P, step.F[k0 + wl.S - 1], wl.S == 1,
-                                                        step.Src[n + 1], stream=stream)
-                    b.record(stream)
-                    marks.append(("freeze", a, b))
+        step()
     torch.cuda.synchronize()
-    for kind, a, b in marks:
-        acc[kind] += a.elapsed_time(b)
-    return {k: v / reps for k, v in acc.items()}
+    return out
+
+
+def block_roofline(step, ms_step, stream, peaks, reps=3):
+    """Roofline block of a Block-pass line: the kernel kind with the largest
+    share of the step, its algorithmic bytes per launch over its average
+    launch duration (graph-timed), and every kind's time and share."""
+    times = time_block_kernels(step, reps, stream)
+    parts = step.byte_parts
+    total = sum(v["ms"] for v in times.values()) or 1.0
+    kernels = {}
+    for k, v in times.items():
+        if not v["launches"]:
+            continue
+        kernels[k] = {"ms": v["ms"], "launches": v["launches"],
+                      "gbs": parts[k] / (v["ms"] / 1e3) / 1e9 if v["ms"] else None,
+                      "share": v["ms"] / total,
+                      "ms_in_step": v["ms"] / total * ms_step}
+    top = max(kernels, key=lambda k: kernels[k]["ms"])
+    g = kernels[top]["gbs"]
+    name = {"stage1": "stage1_tc_kernel", "merge": "merge_tile_kernel", "freeze": "accum_fast_kernel"}[top]
+    ratio = NCU_TRAFFIC.get((name, kernel_digest(KERNEL_FILES[name])))
+    per_launch = parts[top] / kernels[top]["launches"]
+    return {"kernel": name, "bound": "hbm", "achieved": g, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": g / peaks["hbm_gbs"], "frac_of_nominal_8000": g / NOMINAL_HBM_GBS,
+            "peak_source": peaks["source"], "per_launch_bytes": per_launch,
+            "traffic": None if ratio is None else ratio * per_launch,
+            "per_kernel": kernels, "kinds_sum_over_step": total / ms_step,
+            "note": "each kernel kind's launches of one pass graph-timed on their own; 'share' is of the "
+                    "kinds' sum, 'ms_in_step' that share of the step's own graph time"}
 
 
 def _device_tensors(step):
@@ -558,11 +637,16 @@ def run_e2e(step, steps, warmup, stream):
     for name, t in _device_tensors(step).items():
         setattr(sets[1], name, torch.empty_like(t))
     names = _input_names(step)
+
+    def pinned_copy(t):
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        return h
     if isinstance(step, BlockPassStep):
-        host_in = {"F": step.F.cpu().pin_memory(), "W": step.W.cpu().pin_memory(),
-                   "G": step.G.cpu().pin_memory(), "Src": step.Src[0].cpu().pin_memory()}
+        host_in = {"F": pinned_copy(step.F), "W": pinned_copy(step.W), "G": pinned_copy(step.G),
+                   "Src": pinned_copy(step.Src[0])}
     else:
-        host_in = {n: getattr(step, n).cpu().pin_memory() for n in names}
+        host_in = {n: pinned_copy(getattr(step, n)) for n in names}
     host_out = [torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True) for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = host_out[0].numel() * host_out[0].element_size()
@@ -623,47 +707,125 @@ def run_e2e(step, steps, warmup, stream):
     return start.elapsed_time(end) / steps, h2d, d2h
 
 
-def cpu_baseline(name, target_s=12.0):
-    """The fp64 oracle, as it stands, on a bounded sample of token rows."""
+MAX_ORACLE_ROWS = 8192  # token rows gathered for the oracle at most
+
+
+def oracle_inputs(name, device, rows_cap=MAX_ORACLE_ROWS, step=None):
+    """The workload's stored inputs restricted to a stride sample of at most
+    rows_cap token rows, as CPU tensors. They are drawn where the bench draws
+    them (on the GPU when there is one, so the oracle sees the same bits) and
+    only the sampled rows are copied back; `step` reuses tensors already on
+    the device. Returns (kind-specific inputs, rows)."""
+    wl = inputs.WORKLOADS[name]
+    rows = inputs.sample_rows(wl.T, rows_cap)
+    if wl.kind == "full_pass":
+        V, W, G = (step.V, step.W, step.G) if step is not None else inputs.full_inputs(wl, device)
+        r = rows.to(V.device)
+        got = (V[:, r].cpu(), W.cpu().double(), G.cpu().double())
+    else:
+        if step is not None:
+            emb, F, W, G = step.Src[0], step.F, step.W, step.G
+        else:
+            emb, F, W, G = inputs.block_inputs(wl, device)
+        r = rows.to(F.device)
+        got = (emb[r].cpu(), F[:, r].cpu(), W.cpu().double(), G.cpu().double())
+    return got, rows
+
+
+def cpu_baseline(name, target_s=12.0, device="cpu", step=None):
+    """The fp64 oracle, as it stands, on a bounded sample of token rows (at
+    most MAX_ORACLE_ROWS, sized to take about target_s seconds)."""
     import oracle
     oracle.build()
     wl = inputs.WORKLOADS[name]
+    data, all_rows = oracle_inputs(name, device, step=step)
     if wl.kind == "full_pass":
-        V, W, G = inputs.full_inputs(wl, "cpu")
-        W64, G64 = W.double(), G.double()
+        V, W64, G64 = data
 
-        def run(rows):
-            oracle.full_pass(V, wl.R, W64, G64, wl.eps, rows)
+        def run(sel):
+            oracle.full_pass(V[:, sel], wl.R, W64, G64, wl.eps)
     else:
-        emb, F, W, G = inputs.block_inputs(wl, "cpu")
-        W64, G64 = W.double(), G.double()
+        emb, F, W64, G64 = data
 
-        def run(rows):
-            oracle.block_pass(emb[rows], F[:, rows, :], wl.N, wl.S, W64, G64, wl.eps)
-    probe = inputs.sample_rows(wl.T, 16)
+        def run(sel):
+            oracle.block_pass(emb[sel], F[:, sel, :], wl.N, wl.S, W64, G64, wl.eps)
+    m = len(all_rows)
+    probe = torch.linspace(0, m - 1, min(16, m)).round().long().unique()
     t0 = time.perf_counter()
     run(probe)
     dt = max(time.perf_counter() - t0, 1e-6)
-    nrows = int(min(wl.T, max(16, 16 * target_s / dt)))
-    rows = inputs.sample_rows(wl.T, nrows)
+    nrows = int(min(m, max(16, len(probe) * target_s / dt)))
+    sel = torch.linspace(0, m - 1, nrows).round().long().unique()
     t0 = time.perf_counter()
-    run(rows)
+    run(sel)
     dt = time.perf_counter() - t0
     cores = oracle.threads()
     # The same oracle on one thread, on a smaller sample (about 1/8 of the time).
-    one_rows = inputs.sample_rows(wl.T, max(16, len(rows) // (8 * max(cores, 1)) + 1))
+    one = sel[:max(16, len(sel) // (8 * max(cores, 1)) + 1)]
     oracle.set_threads(1)
     try:
         t1 = time.perf_counter()
-        run(one_rows)
+        run(one)
         dt1 = time.perf_counter() - t1
     finally:
         oracle.set_threads(cores)
-    return {"value": len(rows) / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{len(rows)} of {wl.T} token rows (stride-sampled) of {name}, fp64, "
+    return {"value": len(sel) / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(sel)} of {wl.T} token rows (stride-sampled) of {name}, fp64, "
                       f"{dt:.1f} s; tokens are independent so tokens/s scales",
-            "single_thread": {"value": len(one_rows) / dt1, "unit": "tokens/s",
-                              "sample": f"{len(one_rows)} token rows, {dt1:.1f} s"}}, (run, rows)
+            "single_thread": {"value": len(one) / dt1, "unit": "tokens/s",
+                              "sample": f"{len(one)} token rows, {dt1:.1f} s"}}, (run, sel)
+
+
+def time_sustained(graph, ms_probe, seconds, stream):
+    """Replays an already captured step graph for at least `seconds` between
+    CUDA events (after the regular timing, which warmed it up)."""
+    steps = max(1, int(math.ceil(seconds * 1e3 / max(ms_probe, 1e-3))))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, steps
+
+
+def full_roofline(step, ms, peaks, op):
+    kname = "full_bwd_bulk_kernel" if op == "bwd" else "full_fwd_bulk_kernel"
+    gbs = step.bytes / (ms / 1e3) / 1e9
+    traffic = NCU_TRAFFIC.get((kname, kernel_digest(KERNEL_FILES[kname])))
+    return {"kernel": kname, "bound": "hbm", "achieved": gbs,
+            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+            "frac_of_nominal_8000": gbs / NOMINAL_HBM_GBS,
+            "peak_source": peaks["source"],
+            "traffic": None if traffic is None else traffic * step.bytes / step.launches,
+            "per_launch_bytes": step.bytes / step.launches,
+            "note": "the step is R launches of this one kernel back to back in a CUDA graph; "
+                    "average launch duration = step time / R (gaps included)"}
+
+
+def measure_extra(name, dev, steps, warmup, world, stream, peaks):
+    """One more bench workload in the same run: its step graph-timed like the
+    headline (K steps after W warm-up replays); Block passes add their
+    per-kernel roofline."""
+    step = make_step(name, dev)
+    ms, graph = time_graph(step, steps, warmup, world, stream)
+    del graph
+    ms = max_over_ranks(ms, world)
+    gbs = step.bytes / (ms / 1e3) / 1e9
+    wl = step.wl
+    rec = {"ms_per_step": ms, "steps": steps, "tokens_per_s": wl.T * world / (ms / 1e3),
+           "algorithmic_gbs": gbs, "frac": gbs / peaks["hbm_gbs"], "frac_of_nominal_8000": gbs / NOMINAL_HBM_GBS,
+           "gpu_launches": step.launches * steps}
+    if isinstance(step, BlockPassStep):
+        rec["roofline"] = block_roofline(step, ms, stream, peaks)
+    else:
+        rec["roofline"] = full_roofline(step, ms, peaks, "read")
+    del step
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
 
 
 def ours(args):
@@ -698,25 +860,25 @@ def ours(args):
                    "l2": "inputs larger than L2 (129 MB); no flush",
                    "timing": "CUDA graph of one step, CUDA events on the launching stream"},
         "algorithmic_gbs": gbs,
+        "timed_region_s": ms * args.steps / 1e3,
         "gpu_launches": step.launches * args.steps,
     }
+    line["clocks"] = clocks.summary()
+    if not args.no_sustained:
+        with ClockSampler(local) as sclocks:
+            sms, ssteps = time_sustained(graph, ms, SUSTAINED_S, stream)
+        sms = max_over_ranks(sms, world)
+        line["sustained"] = {"ms_per_step": sms, "steps": ssteps, "timed_region_s": sms * ssteps / 1e3,
+                             "value": job_throughput(wl.T, world, sms), "unit": "tokens/s",
+                             "algorithmic_gbs": step.bytes / (sms / 1e3) / 1e9,
+                             "clocks": sclocks.summary(),
+                             "note": "the same step graph replayed back to back for at least "
+                                     f"{SUSTAINED_S:.0f} s after the K timed steps"}
     del graph
     torch.cuda.synchronize()
 
     if wl.kind == "full_pass":
-        kname, kfile = (("full_bwd_bulk_kernel", "full_bwd.cu") if args.op == "bwd"
-                        else ("full_fwd_bulk_kernel", "full_fwd.cu"))
-        digest = kernel_digest(kfile)
-        traffic = NCU_TRAFFIC.get((kname, digest))
-        line["roofline"] = {
-            "kernel": kname, "bound": "hbm", "achieved": gbs,
-            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
-            "frac_of_nominal_8000": gbs / NOMINAL_HBM_GBS,
-            "peak_source": peaks["source"],
-            "traffic": None if traffic is None else traffic * step.bytes / step.launches,
-            "per_launch_bytes": step.bytes / step.launches,
-            "note": "the step is R launches of this one kernel back to back in a CUDA graph; "
-                    "average launch duration = step time / R (gaps included)"}
+        line["roofline"] = full_roofline(step, ms, peaks, args.op)
     elif isinstance(step, BlockBwdStep):
         g = step.byte_parts["total"] / (ms / 1e3) / 1e9
         batched = step.launches == step.wl.N + 1
@@ -744,34 +906,7 @@ def ours(args):
             "frac": g / peaks["hbm_gbs"], "frac_of_nominal_8000": g / NOMINAL_HBM_GBS,
             "peak_source": peaks["source"], "traffic": None, "per_kernel": kernels}
     else:
-        times = time_block_kernels(step, 3, stream)
-        parts = step.byte_parts
-        kernels = {k: {"ms": times[k], "gbs": parts[k] / (times[k] / 1e3) / 1e9 if times[k] else None}
-                   for k in ("stage1", "merge", "freeze")}
-        top = max(kernels, key=lambda k: kernels[k]["ms"])
-        g = kernels[top]["gbs"]
-        line["roofline"] = {
-            "kernel": {"stage1": "stage1_tc_kernel", "merge": "merge_tile_kernel",
-                       "freeze": "accum_fast_kernel"}[top],
-            "bound": "hbm", "achieved": g, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": g / peaks["hbm_gbs"], "frac_of_nominal_8000": g / NOMINAL_HBM_GBS,
-            "peak_source": peaks["source"], "traffic": None, "per_kernel": kernels}
-
-    if not args.no_block and wl.kind == "full_pass" and world >= 1:
-        bstep = make_step(BLOCK_WORKLOAD, dev)
-        bms, bgraph = time_graph(bstep, args.steps, args.warmup, world, stream)
-        del bgraph
-        times = time_block_kernels(bstep, 3, stream)
-        parts = bstep.byte_parts
-        line["block"] = {
-            "workload": BLOCK_WORKLOAD, "ms_per_step": bms, "tokens_per_s": bstep.wl.T * world / (bms / 1e3),
-            "algorithmic_gbs": bstep.bytes / (bms / 1e3) / 1e9,
-            "frac": bstep.bytes / (bms / 1e3) / 1e9 / peaks["hbm_gbs"],
-            "frac_of_nominal_8000": bstep.bytes / (bms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
-            "per_kernel_ms": times,
-            "per_kernel_gbs": {k: parts[k] / (times[k] / 1e3) / 1e9 for k in times if times[k]}}
-        del bstep
-        torch.cuda.empty_cache()
+        line["roofline"] = block_roofline(step, ms, stream, peaks)
 
     if not args.no_e2e:
         ems, h2d, d2h = run_e2e(step, max(4, min(args.steps, 20)), 3, stream)
@@ -779,9 +914,24 @@ def ours(args):
         line["e2e"] = {"value": tokens / (ems / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": ems,
                        "note": "uploads, passes and downloads of consecutive steps overlap on three streams"}
-    line["clocks"] = clocks.summary()
-    if rank == 0 and world >= 1 and not args.no_cpu_baseline:
-        base, _ = cpu_baseline(args.workload)
+        torch.cuda.empty_cache()
+    base_data = None
+    if rank == 0 and not args.no_cpu_baseline:
+        # The oracle's rows are taken from the inputs already on the device.
+        base_data = step
+    base = None
+    if base_data is not None:
+        base, _ = cpu_baseline(args.workload, step=base_data)
+    del step, base_data
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+    if not args.no_extras and args.op == "read":
+        line["extras"] = {}
+        for name in EXTRA_WORKLOADS:
+            if name != args.workload:
+                line["extras"][name] = measure_extra(name, dev, args.steps, args.warmup, world, stream, peaks)
+    if base is not None:
         line["cpu_baseline"] = base
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -795,7 +945,12 @@ def reference(args):
     if rank != 0:
         return
     wl = inputs.WORKLOADS[args.workload]
-    base, (run, rows) = cpu_baseline(args.workload, target_s=4.0)
+    # The inputs are drawn on the GPU when there is one (the same bits as the
+    # bench's own arm); only the oracle's fp64 CPU run is timed.
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    base, (run, rows) = cpu_baseline(args.workload, target_s=4.0, device=device)
+    if device == "cuda":
+        torch.cuda.empty_cache()
     for _ in range(args.warmup):
         run(rows[:8])
     t0 = time.perf_counter()
@@ -819,8 +974,8 @@ def reference(args):
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=100)
-    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(
         n for n, w in inputs.WORKLOADS.items() if w.kind != "full_read"))
@@ -830,13 +985,15 @@ def main():
                         "input-dependent queries (projection + read). Block pass: dsplit, the stage-1 "
                         "reads with the features split over 4 shards; bwd, the pass backward")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--no-block", action="store_true")
+    p.add_argument("--no-extras", "--no-block", dest="no_extras", action="store_true",
+                   help="skip the other bench workloads measured after the headline")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-sustained", action="store_true")
     args = p.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     if args.op != "read":
         # The variants are measured on the device alone.
-        args.no_e2e = args.no_block = args.no_cpu_baseline = True
+        args.no_e2e = args.no_extras = args.no_cpu_baseline = True
     if args.impl == "reference":
         reference(args)
     else:

@@ -49,12 +49,18 @@ _SIGNATURES = {
     "attnres_block_merge_prenorm": [_VP, _VP, _VP, _VP, _I32, _VP, _VP, _F, _VP, _F, _I64, _I32, _I32,
                                     _VP, _VP, _VP],
     "attnres_block_summary_accumulate": [_VP, _VP, _I32, _VP, _I64, _I32, _I32, _VP],
+    "attnres_block_merge_parts": [_VP, _VP, _VP, _VP, _I64, _I32, _VP, _VP, _VP, _F, _I64, _I32, _I32, _VP,
+                                  _VP],
+    "attnres_block_summary_parts": [_VP, _VP, _I64, _I32, _VP, _VP, _I64, _I32, _I32, _VP],
+    "attnres_block_running_sum_plan": [_I32, _I32, ctypes.POINTER(_I32)],
     "attnres_block_pass": [_VP, _I64, _I32, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _I64,
                            _I32, _VP, _VP, _VP, _VP, _I64, _VP],
     "attnres_block_pass_noalloc": [_VP, _I64, _I32, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP,
                                    _I64, _I32, _VP, _I64, _VP],
     "attnres_device_status": [_VP],
     "attnres_selftest_wait_timeout": [_VP],
+    "attnres_test_fail_launch": [_I64],
+    "attnres_test_withhold_stage": [_I32, _I64],
     "attnres_status_string": [_I32],
     "attnres_kernel_path": [_I32, _VP, _VP, _I32, _I32, _I64, _I32, _I32],
     "attnres_abi_version": [],
@@ -87,7 +93,8 @@ def lib() -> ctypes.CDLL:
                 fn = getattr(handle, name)
                 fn.argtypes = args
                 fn.restype = (ctypes.c_char_p if name == "attnres_status_string" else
-                              ctypes.c_int64 if name == "attnres_block_bwd_scratch_floats" else ctypes.c_int)
+                              ctypes.c_int64 if name in ("attnres_block_bwd_scratch_floats",
+                                                         "attnres_test_fail_launch") else ctypes.c_int)
             _lib = handle
     return _lib
 
@@ -373,6 +380,47 @@ def attnres_block_summary_accumulate(P, f: torch.Tensor, p_is_empty: bool, summa
         _stream(stream)))
 
 
+def _parts(F_parts: torch.Tensor, n_parts: int) -> tuple[int, int, int, int]:
+    """(T, d, part stride, dtype code) of the first n_parts slices of F_parts."""
+    if F_parts.dim() == 2:
+        if n_parts > 1:
+            raise ValueError("several parts need an [n, T, d] tensor")
+        T, d = _rows(F_parts)
+        return T, d, T * d, _dtype(F_parts)
+    n, T, d, stride = _slices(F_parts)
+    if n < n_parts:
+        raise ValueError(f"F_parts holds {n} slices, {n_parts} requested")
+    return T, d, stride, _dtype(F_parts)
+
+
+def attnres_block_merge_parts(O_j: torch.Tensor, lse_j: torch.Tensor, P_base, F_parts: torch.Tensor,
+                              n_parts: int, P_out, w: torch.Tensor, gamma: torch.Tensor, eps: float,
+                              out: torch.Tensor, stream=None) -> torch.Tensor:
+    """Merge with the running sum P_base + F_parts[0] + ... + F_parts[n_parts-1]
+    (P_base may be None), storing it to P_out when given."""
+    T, d, pstride, code = _parts(F_parts, n_parts)
+    _check("attnres_block_merge_parts", lib().attnres_block_merge_parts(
+        _ptr(O_j), _ptr(lse_j), _ptr(P_base), _ptr(F_parts), pstride, n_parts, _ptr(P_out), _ptr(w),
+        _ptr(gamma), eps, T, d, code, _ptr(out), _stream(stream)))
+    return out
+
+
+def attnres_block_summary_parts(P_base, F_parts: torch.Tensor, n_parts: int, P_out=None, summary_out=None,
+                                stream=None) -> None:
+    """summary_out <- round(P_base + parts), or P_out <- that sum in fp32."""
+    T, d, pstride, code = _parts(F_parts, n_parts)
+    _check("attnres_block_summary_parts", lib().attnres_block_summary_parts(
+        _ptr(P_base), _ptr(F_parts), pstride, n_parts, _ptr(P_out), _ptr(summary_out), T, d, code,
+        _stream(stream)))
+
+
+def attnres_block_running_sum_plan(S: int, dtype: int = BF16) -> list[int]:
+    """stored[j] (0 <= j <= S): whether the Block pass keeps running sum P_j."""
+    arr = (ctypes.c_int32 * (S + 1))()
+    _check("attnres_block_running_sum_plan", lib().attnres_block_running_sum_plan(S, dtype, arr))
+    return list(arr)
+
+
 def attnres_block_pass(F: torch.Tensor, N: int, S: int, W: torch.Tensor, Gamma: torch.Tensor,
                        eps: float, Src: torch.Tensor, O_scratch, lse_scratch: torch.Tensor,
                        P_scratch, out: torch.Tensor, freeze_last: bool = False,
@@ -408,6 +456,23 @@ def attnres_device_status(stream=None) -> int:
 def attnres_selftest_wait_timeout(stream=None) -> None:
     """Run the bounded-wait self-test kernel (its wait runs out after ~2 s)."""
     _check("attnres_selftest_wait_timeout", lib().attnres_selftest_wait_timeout(_stream(stream)))
+
+
+def attnres_test_fail_launch(after: int) -> int:
+    """Test hook: the launch after `after` more successful ones fails with
+    ATTNRES_ERR_CUDA without being made (after < 0 disarms). Returns the
+    previous setting (-1 once an armed failure has fired)."""
+    return int(lib().attnres_test_fail_launch(int(after)))
+
+
+# Kernels whose copy producer attnres_test_withhold_stage can starve.
+WITHHOLD_NONE, WITHHOLD_FULL, WITHHOLD_STAGE1_TC, WITHHOLD_MERGE = 0, 1, 2, 3
+
+
+def attnres_test_withhold_stage(kernel: int, index: int = 0) -> None:
+    """Test hook: the producer of `kernel` leaves its copy number `index` (per
+    CTA) unissued, so the consumers' bounded wait runs out (kernel 0: off)."""
+    _check("attnres_test_withhold_stage", lib().attnres_test_withhold_stage(int(kernel), int(index)))
 
 
 def status_string(status: int) -> str:

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -89,6 +90,16 @@ int blocks_per_sm(const void* kernel, int threads, int smem_bytes) {
   return n;
 }
 
+// Failure-path test hook (attnres_test_withhold_stage), off by default.
+namespace {
+std::atomic<int> g_withhold_kernel{kWithholdNone};
+std::atomic<int64_t> g_withhold_index{-1};
+}  // namespace
+
+int64_t withhold_for(WithholdKernel k) {
+  return g_withhold_kernel.load() == k ? g_withhold_index.load() : -1;
+}
+
 }  // namespace attnres
 
 using namespace attnres;
@@ -123,6 +134,27 @@ int status_of(cudaError_t e) {
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
+// Failure-path test hook (attnres_test_fail_launch): the launch after
+// g_fail_after more successful ones reports a CUDA error without being
+// made. -1, the default, injects nothing.
+std::atomic<int64_t> g_fail_after{-1};
+
+bool injected_failure() {
+  int64_t v = g_fail_after.load();
+  while (v >= 0) {
+    if (g_fail_after.compare_exchange_weak(v, v - 1)) return v == 0;
+  }
+  return false;
+}
+
+// Every launch (kernel, memset or copy) the library makes goes through here:
+// the test hook first, then the launch and its status.
+template <typename F>
+int launched(F&& launch) {
+  if (injected_failure()) return ATTNRES_ERR_CUDA;
+  return status_of(launch());
+}
+
 // Checks and fills the arguments of one full read. Returns a status.
 int make_full(const void* V, int64_t src_stride, int32_t n_src, int64_t T, int32_t d,
               int32_t v_dtype, const float* w, const float* gamma, float eps, void* out,
@@ -140,11 +172,12 @@ int make_full(const void* V, int64_t src_stride, int32_t n_src, int64_t T, int32
   if (overlap(rv, ro)) return ATTNRES_ERR_INVALID_ARG;
   *a = FullArgs{V, src_stride, n_src, T, d, v_dtype == ATTNRES_BF16, w, gamma, eps, out,
                 out_dtype == ATTNRES_BF16, 0};
+  a->withhold = withhold_for(kWithholdFull);
   return ATTNRES_OK;
 }
 
 int run_full(const FullArgs& a, cudaStream_t s) {
-  if (full_fast_ok(a)) return status_of(launch_full_fast(a, s));
+  if (full_fast_ok(a)) return launched([&] { return launch_full_fast(a, s); });
   // General kernel: writes in the storage dtype of the sources.
   if (a.out_bf16 != a.v_bf16) return ATTNRES_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(a.n_src) * 4 > kGenericScoreLimit) return ATTNRES_ERR_UNSUPPORTED;
@@ -163,7 +196,7 @@ int run_full(const FullArgs& a, cudaStream_t s) {
   m.lse = nullptr;
   m.pre = a.pre;
   m.Q = a.Q;
-  return status_of(launch_multi_generic(m, s));
+  return launched([&] { return launch_multi_generic(m, s); });
 }
 
 int make_stage1(const void* Src, int64_t src_stride, int32_t n_src, int64_t T, int32_t d,
@@ -200,15 +233,47 @@ int make_stage1(const void* Src, int64_t src_stride, int32_t n_src, int64_t T, i
   m->eps = eps;
   for (int j = 0; j < S; ++j) m->out[j] = O[j];
   m->lse = lse;
+  m->withhold = withhold_for(kWithholdStage1Tc);
   return ATTNRES_OK;
 }
 
 int run_stage1(const MultiArgs& m, cudaStream_t s) {
-  if (stage1_fast_ok(m)) return status_of(launch_stage1_fast(m, s));
+  if (stage1_fast_ok(m)) return launched([&] { return launch_stage1_fast(m, s); });
   if (static_cast<int64_t>(m.n_src) * m.S * 4 > kGenericScoreLimit) return ATTNRES_ERR_UNSUPPORTED;
-  return status_of(launch_multi_generic(m, s));
+  return launched([&] { return launch_multi_generic(m, s); });
 }
 
+// Checks and fills a merge whose running sum is P_base + the n_parts
+// sublayer outputs at F_parts (part_stride apart), stored to P_out if given.
+int make_merge_parts(const void* O_j, const float* lse_j, const float* P_base, const void* F_parts,
+                     int64_t part_stride, int32_t n_parts, float* P_out, const float* w, const float* gamma,
+                     float eps, int64_t T, int32_t d, int32_t dtype, void* out, MergeArgs* a) {
+  if (d < 1 || T < 0 || !valid_dtype(dtype) || !valid_eps(eps) || n_parts < 0 || n_parts > kMaxMergeParts)
+    return ATTNRES_ERR_INVALID_ARG;
+  if (n_parts == 0 && !P_base) return ATTNRES_ERR_INVALID_ARG;
+  if (T == 0) return ATTNRES_OK;
+  if (!O_j || !lse_j || !w || !gamma || !out || (n_parts > 0 && !F_parts)) return ATTNRES_ERR_INVALID_ARG;
+  const int64_t E = T * d;
+  if (n_parts > 1 && part_stride < E) return ATTNRES_ERR_INVALID_ARG;
+  const int es = elem_size(dtype);
+  const Range ro = range_of(O_j, E * es), rl = range_of(lse_j, T * 4), rout = range_of(out, E * es);
+  const Range rb = P_base ? range_of(P_base, E * 4) : Range{};
+  const Range rf = n_parts > 0 ? range_of(F_parts, ((n_parts - 1) * (n_parts > 1 ? part_stride : 0) + E) * es)
+                               : Range{};
+  const Range rp = P_out ? range_of(P_out, E * 4) : Range{};
+  // out and P_out are written: they overlap nothing else, except that P_out
+  // may be P_base itself (the running sum advanced in place).
+  if (overlap(rout, ro) || overlap(rout, rl) || overlap(rout, rb) || overlap(rout, rf) || overlap(rout, rp))
+    return ATTNRES_ERR_INVALID_ARG;
+  if (overlap(rp, ro) || overlap(rp, rl) || overlap(rp, rf) || (overlap(rp, rb) && P_out != P_base))
+    return ATTNRES_ERR_INVALID_ARG;
+  *a = MergeArgs{O_j, lse_j, P_base, F_parts, n_parts > 1 ? part_stride : 0, n_parts, P_out, w, gamma, eps, T, d,
+                 dtype == ATTNRES_BF16, out};
+  a->withhold = withhold_for(kWithholdMerge);
+  return ATTNRES_OK;
+}
+
+// The single-step merge: P (in/out) advanced by f_prev, or started from it.
 int make_merge(const void* O_j, const float* lse_j, float* P, const void* f_prev, int32_t p_is_empty,
                const float* w, const float* gamma, float eps, int64_t T, int32_t d, int32_t dtype,
                void* out, MergeArgs* a) {
@@ -223,7 +288,29 @@ int make_merge(const void* O_j, const float* lse_j, float* P, const void* f_prev
   if (overlap(rout, ro) || overlap(rout, rp) || overlap(rout, rf) || overlap(rout, rl) ||
       overlap(rp, ro) || overlap(rp, rf) || overlap(rp, rl))
     return ATTNRES_ERR_INVALID_ARG;
-  *a = MergeArgs{O_j, lse_j, P, f_prev, p_is_empty != 0, w, gamma, eps, T, d, dtype == ATTNRES_BF16, out};
+  return make_merge_parts(O_j, lse_j, p_is_empty ? nullptr : P, f_prev, 0, f_prev ? 1 : 0, f_prev ? P : nullptr, w,
+                          gamma, eps, T, d, dtype, out, a);
+}
+
+// Checks and fills a running-sum step: P_base + the n_parts outputs, into
+// P_out (fp32) or, rounded, into summary.
+int make_accum_parts(const float* P_base, const void* F_parts, int64_t part_stride, int32_t n_parts, float* P_out,
+                     void* summary, int64_t T, int32_t d, int32_t dtype, AccumArgs* a) {
+  if (d < 1 || T < 0 || !valid_dtype(dtype) || n_parts < 1 || n_parts > kMaxMergeParts)
+    return ATTNRES_ERR_INVALID_ARG;
+  if (T == 0) return ATTNRES_OK;
+  if (!F_parts || (!summary && !P_out)) return ATTNRES_ERR_INVALID_ARG;
+  const int64_t E = T * d;
+  if (n_parts > 1 && part_stride < E) return ATTNRES_ERR_INVALID_ARG;
+  const int es = elem_size(dtype);
+  const Range rb = P_base ? range_of(P_base, E * 4) : Range{};
+  const Range rf = range_of(F_parts, ((n_parts - 1) * (n_parts > 1 ? part_stride : 0) + E) * es);
+  const Range rs = summary ? range_of(summary, E * es) : Range{};
+  const Range rp = !summary ? range_of(P_out, E * 4) : Range{};
+  if (overlap(rs, rb) || overlap(rs, rf) || overlap(rp, rf) || (overlap(rp, rb) && P_out != P_base))
+    return ATTNRES_ERR_INVALID_ARG;
+  *a = AccumArgs{P_base, F_parts, n_parts > 1 ? part_stride : 0, n_parts, summary ? nullptr : P_out, summary, T, d,
+                 dtype == ATTNRES_BF16};
   return ATTNRES_OK;
 }
 
@@ -238,8 +325,52 @@ int make_accum(float* P, const void* f, int32_t p_is_empty, void* summary_out, i
   const Range rp = P ? range_of(P, E * 4) : Range{}, rf = range_of(f, E * es),
               rs = summary_out ? range_of(summary_out, E * es) : Range{};
   if (overlap(rp, rf) || overlap(rs, rf) || overlap(rs, rp)) return ATTNRES_ERR_INVALID_ARG;
-  *a = AccumArgs{P, f, p_is_empty != 0, summary_out, T, d, dtype == ATTNRES_BF16};
-  return ATTNRES_OK;
+  return make_accum_parts(p_is_empty ? nullptr : P, f, 0, 1, P, summary_out, T, d, dtype, a);
+}
+
+// Which running sums a Block pass stores (see attnres_block_running_sum_plan):
+// stored[j] for 1 <= j < S. Position j (1 <= j <= S) needs P_j, the sum of
+// the block's first j outputs; position S is the freeze. Bytes per element
+// beyond the fixed O_j / out / summary traffic: each output re-read costs es,
+// a stored sum costs 4 to write and 4 to read back. Minimised over all
+// choices (dynamic programming over the last stored position); among equal
+// costs the plan with fewer stored sums wins, then the one found first.
+void running_sum_plan(int S, int es, int* stored) {
+  for (int j = 0; j <= S; ++j) stored[j] = 0;
+  constexpr int kMax = ATTNRES_MAX_QUERIES + 1;
+  int64_t best[kMax];
+  int nst[kMax], prev[kMax];
+  // Cost of positions m'+1 .. j with base m' and nothing stored between.
+  auto run_cost = [&](int mp, int j) {
+    int64_t c = 0;
+    for (int q = mp + 1; q <= j; ++q) c += static_cast<int64_t>(es) * (q - mp) + (mp > 0 ? 4 : 0);
+    return c;
+  };
+  best[0] = 0;
+  nst[0] = 0;
+  prev[0] = -1;
+  for (int m = 1; m < S; ++m) {
+    best[m] = -1;
+    for (int mp = 0; mp < m; ++mp) {
+      const int64_t c = best[mp] + run_cost(mp, m) + 4;
+      if (best[m] < 0 || c < best[m] || (c == best[m] && nst[mp] + 1 < nst[m])) {
+        best[m] = c;
+        nst[m] = nst[mp] + 1;
+        prev[m] = mp;
+      }
+    }
+  }
+  int64_t cost = -1;
+  int last = 0, n_last = 0;
+  for (int mp = 0; mp < S; ++mp) {
+    const int64_t c = best[mp] + run_cost(mp, S);
+    if (cost < 0 || c < cost || (c == cost && nst[mp] < n_last)) {
+      cost = c;
+      last = mp;
+      n_last = nst[mp];
+    }
+  }
+  for (int m = last; m > 0; m = prev[m]) stored[m] = 1;
 }
 
 }  // namespace
@@ -376,8 +507,10 @@ int attnres_query_projection(const void* H, int64_t T, int32_t d, int32_t h_dtyp
   if (overlap(rq, range_of(H, T * d * 2)) || overlap(rq, range_of(Wq, static_cast<int64_t>(d) * d * 2)))
     return ATTNRES_ERR_INVALID_ARG;
   cudaStream_t s = as_stream(stream);
-  if (proj_tc_ok(H, Wq, Q, T, d)) return status_of(launch_proj_tensor(H, Wq, Q, T, d, s));
-  return status_of(proj_ok(H, Wq, Q, d) ? launch_proj(H, Wq, Q, T, d, s) : launch_proj_generic(H, Wq, Q, T, d, s));
+  if (proj_tc_ok(H, Wq, Q, T, d)) return launched([&] { return launch_proj_tensor(H, Wq, Q, T, d, s); });
+  return launched([&] {
+    return proj_ok(H, Wq, Q, d) ? launch_proj(H, Wq, Q, T, d, s) : launch_proj_generic(H, Wq, Q, T, d, s);
+  });
 }
 
 int attnres_full_fwd_dynq(const void* V, int64_t src_stride, int32_t n_src, int64_t T, int32_t d, int32_t v_dtype,
@@ -402,7 +535,7 @@ int attnres_rmsnorm(const void* x, int64_t T, int32_t d, int32_t dtype, const fl
   const int64_t bytes = T * d * elem_size(dtype);
   // In place (out == x) is allowed; a partial overlap is not.
   if (out != x && overlap(range_of(x, bytes), range_of(out, bytes))) return ATTNRES_ERR_INVALID_ARG;
-  return status_of(launch_rmsnorm(x, T, d, dtype == ATTNRES_BF16, gamma, eps, out, as_stream(stream)));
+  return launched([&] { return launch_rmsnorm(x, T, d, dtype == ATTNRES_BF16, gamma, eps, out, as_stream(stream)); });
 }
 
 int attnres_full_bwd(const void* V, int64_t src_stride, int32_t n_src, int64_t T, int32_t d,
@@ -430,7 +563,7 @@ int attnres_full_bwd(const void* V, int64_t src_stride, int32_t n_src, int64_t T
                   dV, dstr, dw, dgamma};
   const bool fast = full_bwd_fast_ok(a);
   if (!fast && d > kMaxBwdGenericD) return ATTNRES_ERR_UNSUPPORTED;
-  return status_of(launch_full_bwd(a, as_stream(stream), fast));
+  return launched([&] { return launch_full_bwd(a, as_stream(stream), fast); });
 }
 
 int64_t attnres_block_bwd_scratch_floats(int32_t N, int32_t S, int64_t T, int32_t d) {
@@ -478,13 +611,13 @@ int attnres_block_bwd(const void* Src, int64_t src_stride, const void* F, int64_
                    L > 1 ? dout_stride : 0, dout_dtype == ATTNRES_BF16, scratch, E, dF, L > 1 ? df_stride : 0,
                    dW, dGamma, N, S, 0, T, d, dtype == ATTNRES_BF16, eps};
     if (block_bwd_batched_ok(b)) {
-      if (cudaMemsetAsync(scratch, 0, N * E * 4, s) != cudaSuccess) return ATTNRES_ERR_CUDA;
+      if (launched([&] { return cudaMemsetAsync(scratch, 0, N * E * 4, s); }) != ATTNRES_OK) return ATTNRES_ERR_CUDA;
       for (int32_t n = N - 1; n >= 0; --n) {
         b.n = n;
-        const int st = status_of(launch_block_bwd_batched(b, s));
+        const int st = launched([&] { return launch_block_bwd_batched(b, s); });
         if (st != ATTNRES_OK) return st;
       }
-      return status_of(launch_spread(dEmb, 0, 1, scratch, E, s));
+      return launched([&] { return launch_spread(dEmb, 0, 1, scratch, E, s); });
     }
   }
   // Scratch: fp32 sources Vs [N + 1][E] (embedding, b_1 .. b_{N-1}, and the
@@ -499,40 +632,45 @@ int attnres_block_bwd(const void* Src, int64_t src_stride, const void* F, int64_
   const char* Fb = static_cast<const char*>(F);
   const char* Zb = static_cast<const char*>(dOut);
   const int is_bf16 = dtype == ATTNRES_BF16;
-  if (cudaMemsetAsync(dVs, 0, (N + 1) * E * 4, s) != cudaSuccess) return ATTNRES_ERR_CUDA;
-  int st = status_of(launch_widen_rows(Src, N > 1 ? src_stride : 0, is_bf16, Vs, N, E, s));
+  if (launched([&] { return cudaMemsetAsync(dVs, 0, (N + 1) * E * 4, s); }) != ATTNRES_OK) return ATTNRES_ERR_CUDA;
+  int st = launched([&] { return launch_widen_rows(Src, N > 1 ? src_stride : 0, is_bf16, Vs, N, E, s); });
   if (st != ATTNRES_OK) return st;
   for (int32_t n = N - 1; n >= 0; --n) {
     const int64_t k0 = static_cast<int64_t>(n) * S;
     // The gradient of b_{n+1}, complete now that every later block is done,
     // goes to each member of block n; its slot then holds block n's running sum.
     if (n + 1 < N) {
-      st = status_of(launch_spread(dF + k0 * df_stride, df_stride, S, dVs + (n + 1) * E, E, s));
+      st = launched([&] { return launch_spread(dF + k0 * df_stride, df_stride, S, dVs + (n + 1) * E, E, s); });
       if (st != ATTNRES_OK) return st;
-      if (cudaMemsetAsync(dVs + (n + 1) * E, 0, E * 4, s) != cudaSuccess) return ATTNRES_ERR_CUDA;
+      if (launched([&] { return cudaMemsetAsync(dVs + (n + 1) * E, 0, E * 4, s); }) != ATTNRES_OK)
+        return ATTNRES_ERR_CUDA;
     }
     // Running sums as the forward formed them: P_1 = f_{k0}, P_j = P_{j-1} + f_{k0+j-1}.
     for (int32_t j = 1; j < S; ++j) {
-      st = status_of(launch_psum(Ps + j * E, j == 1 ? nullptr : Ps + (j - 1) * E, Fb + (k0 + j - 1) * f_stride * es,
-                                 is_bf16, E, s));
+      st = launched([&] {
+        return launch_psum(Ps + j * E, j == 1 ? nullptr : Ps + (j - 1) * E, Fb + (k0 + j - 1) * f_stride * es,
+                           is_bf16, E, s);
+      });
       if (st != ATTNRES_OK) return st;
     }
-    if (cudaMemsetAsync(G, 0, E * 4, s) != cudaSuccess) return ATTNRES_ERR_CUDA;
+    if (launched([&] { return cudaMemsetAsync(G, 0, E * 4, s); }) != ATTNRES_OK) return ATTNRES_ERR_CUDA;
     for (int32_t j = S - 1; j >= 0; --j) {
       const int64_t k = k0 + j;
-      if (j >= 1 && cudaMemcpyAsync(Vs + (n + 1) * E, Ps + j * E, E * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      if (j >= 1 && launched([&] {
+                      return cudaMemcpyAsync(Vs + (n + 1) * E, Ps + j * E, E * 4, cudaMemcpyDeviceToDevice, s);
+                    }) != ATTNRES_OK)
         return ATTNRES_ERR_CUDA;
       st = attnres_full_bwd(Vs, E, n + 1 + (j >= 1 ? 1 : 0), T, d, ATTNRES_F32, W + k * d, Gamma + k * d, eps,
                             Zb + k * dout_stride * elem_size(dout_dtype), dout_dtype, dVs, E,
                             dW ? dW + k * d : nullptr, dGamma ? dGamma + k * d : nullptr, stream);
       if (st != ATTNRES_OK) return st;
       if (j >= 1) {
-        st = status_of(launch_gupdate(G, dVs + (n + 1) * E, dF + (k - 1) * df_stride, E, s));
+        st = launched([&] { return launch_gupdate(G, dVs + (n + 1) * E, dF + (k - 1) * df_stride, E, s); });
         if (st != ATTNRES_OK) return st;
       }
     }
   }
-  return status_of(launch_spread(dEmb, 0, 1, dVs, E, s));
+  return launched([&] { return launch_spread(dEmb, 0, 1, dVs, E, s); });
 }
 
 // Shared checks of the two d-split calls: the shard's sources and queries.
@@ -574,7 +712,7 @@ int attnres_stage1_dsplit_partials(const void* Src, int64_t src_stride, int32_t 
   if (!W || !Gamma) return ATTNRES_ERR_INVALID_ARG;
   a.accumulate = accumulate != 0;
   if (!dsplit_ok(a)) return ATTNRES_ERR_UNSUPPORTED;
-  return status_of(launch_dsplit_partials(a, as_stream(stream)));
+  return launched([&] { return launch_dsplit_partials(a, as_stream(stream)); });
 }
 
 int attnres_stage1_dsplit_finish(const void* Src, int64_t src_stride, int32_t n_src, int64_t T, int32_t d_shard,
@@ -601,7 +739,7 @@ int attnres_stage1_dsplit_finish(const void* Src, int64_t src_stride, int32_t n_
   }
   a.lse = lse;
   if (!dsplit_ok(a)) return ATTNRES_ERR_UNSUPPORTED;
-  return status_of(launch_dsplit_finish(a, as_stream(stream)));
+  return launched([&] { return launch_dsplit_finish(a, as_stream(stream)); });
 }
 
 int attnres_block_stage1(const void* Src, int64_t src_stride, int32_t n_src, int64_t T, int32_t d,
@@ -619,7 +757,7 @@ int attnres_block_merge(const void* O_j, const float* lse_j, float* P, const voi
   MergeArgs a{};
   const int st = make_merge(O_j, lse_j, P, f_prev, p_is_empty, w, gamma, eps, T, d, dtype, out, &a);
   if (st != ATTNRES_OK || T == 0) return st;
-  return status_of(launch_merge(a, as_stream(stream), merge_fast_ok(a)));
+  return launched([&] { return launch_merge(a, as_stream(stream), merge_fast_ok(a)); });
 }
 
 int attnres_block_merge_prenorm(const void* O_j, const float* lse_j, float* P, const void* f_prev,
@@ -642,7 +780,35 @@ int attnres_block_merge_prenorm(const void* O_j, const float* lse_j, float* P, c
   }
   a.out = out;
   a.pre = PreNorm{gamma_pre, eps_pre, out_normed};
-  return status_of(launch_merge(a, as_stream(stream), merge_fast_ok(a)));
+  return launched([&] { return launch_merge(a, as_stream(stream), merge_fast_ok(a)); });
+}
+
+int attnres_block_merge_parts(const void* O_j, const float* lse_j, const float* P_base, const void* F_parts,
+                              int64_t part_stride, int32_t n_parts, float* P_out, const float* w,
+                              const float* gamma, float eps, int64_t T, int32_t d, int32_t dtype, void* out,
+                              void* stream) {
+  MergeArgs a{};
+  const int st = make_merge_parts(O_j, lse_j, P_base, F_parts, part_stride, n_parts, P_out, w, gamma, eps, T, d,
+                                  dtype, out, &a);
+  if (st != ATTNRES_OK || T == 0) return st;
+  return launched([&] { return launch_merge(a, as_stream(stream), merge_fast_ok(a)); });
+}
+
+int attnres_block_summary_parts(const float* P_base, const void* F_parts, int64_t part_stride, int32_t n_parts,
+                                float* P_out, void* summary_out, int64_t T, int32_t d, int32_t dtype,
+                                void* stream) {
+  AccumArgs a{};
+  const int st = make_accum_parts(P_base, F_parts, part_stride, n_parts, P_out, summary_out, T, d, dtype, &a);
+  if (st != ATTNRES_OK || T == 0) return st;
+  return launched([&] { return launch_accum(a, as_stream(stream), accum_fast_ok(a)); });
+}
+
+int attnres_block_running_sum_plan(int32_t S, int32_t dtype, int32_t* stored) {
+  if (S < 1 || S > ATTNRES_MAX_QUERIES || !valid_dtype(dtype) || !stored) return ATTNRES_ERR_INVALID_ARG;
+  int plan[ATTNRES_MAX_QUERIES + 1];
+  running_sum_plan(S, elem_size(dtype), plan);
+  for (int j = 0; j <= S; ++j) stored[j] = plan[j];
+  return ATTNRES_OK;
 }
 
 int attnres_block_summary_accumulate(float* P, const void* f, int32_t p_is_empty, void* summary_out,
@@ -650,7 +816,7 @@ int attnres_block_summary_accumulate(float* P, const void* f, int32_t p_is_empty
   AccumArgs a{};
   const int st = make_accum(P, f, p_is_empty, summary_out, T, d, dtype, &a);
   if (st != ATTNRES_OK || T == 0) return st;
-  return status_of(launch_accum(a, as_stream(stream), accum_fast_ok(a)));
+  return launched([&] { return launch_accum(a, as_stream(stream), accum_fast_ok(a)); });
 }
 
 int attnres_block_pass(const void* F, int64_t f_stride, int32_t N, int32_t S, int64_t T, int32_t d,
@@ -683,6 +849,10 @@ int attnres_block_pass(const void* F, int64_t f_stride, int32_t N, int32_t S, in
   const char* Fb = static_cast<const char*>(F);
   char* Srcb = static_cast<char*>(Src);
   char* Ob = static_cast<char*>(O_scratch);
+  // Which running sums P_j are kept in P_scratch; the others are formed from
+  // the last kept one (or from nothing) plus the block's outputs since then.
+  int plan[ATTNRES_MAX_QUERIES + 1];
+  running_sum_plan(S, es, plan);
   for (int32_t n = 0; n < N; ++n) {
     const int64_t k0 = static_cast<int64_t>(n) * S;  // first sublayer of the block
     // Stage 1: the block's S queries over embedding + n completed block sums.
@@ -692,23 +862,26 @@ int attnres_block_pass(const void* F, int64_t f_stride, int32_t N, int32_t S, in
     int st = attnres_block_stage1(Src, src_stride, n + 1, T, d, dtype, W + k0 * d, Gamma + k0 * d, S, eps,
                                   O, lse_scratch, stream);
     if (st != ATTNRES_OK) return st;
-    // Stage 2: fold the running sum in, one sublayer at a time.
+    // Stage 2: merge each later sublayer's read with its running sum P_j =
+    // P_m + f_{k0+m} + ... + f_{k0+j-1}, m the last kept position (0: none).
+    int m = 0;
     for (int j = 1; j < S; ++j) {
-      MergeArgs m{};
-      st = make_merge(O[j], lse_scratch + j * T, P_scratch, Fb + (k0 + j - 1) * f_stride * es, j == 1,
-                      W + (k0 + j) * d, Gamma + (k0 + j) * d, eps, T, d, dtype, outb + (k0 + j) * out_stride * es,
-                      &m);
+      MergeArgs a{};
+      st = make_merge_parts(O[j], lse_scratch + j * T, m > 0 ? P_scratch : nullptr, Fb + (k0 + m) * f_stride * es,
+                            f_stride, j - m, plan[j] ? P_scratch : nullptr, W + (k0 + j) * d, Gamma + (k0 + j) * d,
+                            eps, T, d, dtype, outb + (k0 + j) * out_stride * es, &a);
       if (st != ATTNRES_OK) return st;
-      // The merge before this one writes neither O[j] nor f; stage 1 (before
-      // merge 1) writes O[j].
-      m.early = j >= 2;
-      st = status_of(launch_merge(m, as_stream(stream), merge_fast_ok(m)));
+      // The merge before this one writes neither O[j] nor any output f;
+      // stage 1 (before merge 1) writes O[j].
+      a.early = j >= 2;
+      st = launched([&] { return launch_merge(a, as_stream(stream), merge_fast_ok(a)); });
       if (st != ATTNRES_OK) return st;
+      if (plan[j]) m = j;
     }
-    // Freeze the block summary b_{n+1} = P + f_last into Src[n + 1].
+    // Freeze the block summary b_{n+1} = P_S into Src[n + 1].
     if (n + 1 < N || freeze_last) {
-      st = attnres_block_summary_accumulate(P_scratch, Fb + (k0 + S - 1) * f_stride * es, S == 1,
-                                            Srcb + (n + 1) * src_stride * es, T, d, dtype, stream);
+      st = attnres_block_summary_parts(m > 0 ? P_scratch : nullptr, Fb + (k0 + m) * f_stride * es, f_stride, S - m,
+                                       nullptr, Srcb + (n + 1) * src_stride * es, T, d, dtype, stream);
       if (st != ATTNRES_OK) return st;
     }
   }
@@ -734,8 +907,20 @@ int attnres_device_status(void* stream) {
   return e == cudaSuccess ? ATTNRES_OK : ATTNRES_ERR_CUDA;
 }
 
+int64_t attnres_test_fail_launch(int64_t after) {
+  return g_fail_after.exchange(after < 0 ? -1 : after);
+}
+
+int attnres_test_withhold_stage(int32_t kernel, int64_t index) {
+  if (kernel < kWithholdNone || kernel > kWithholdMerge || (kernel != kWithholdNone && index < 0))
+    return ATTNRES_ERR_INVALID_ARG;
+  g_withhold_index.store(kernel == kWithholdNone ? -1 : index);
+  g_withhold_kernel.store(kernel);
+  return ATTNRES_OK;
+}
+
 int attnres_selftest_wait_timeout(void* stream) {
-  return status_of(launch_wait_timeout_selftest(as_stream(stream)));
+  return launched([&] { return launch_wait_timeout_selftest(as_stream(stream)); });
 }
 
 int attnres_kernel_path(int32_t op, const void* src, const void* out, int32_t n_or_s, int32_t s,
@@ -767,12 +952,12 @@ int attnres_kernel_path(int32_t op, const void* src, const void* out, int32_t n_
       return stage1_fast_ok(m) ? 1 : 0;
     }
     case 2: {
-      MergeArgs a{src, wp, const_cast<float*>(wp), src, 0, wp, wp, 0.f, T, d, dtype == ATTNRES_BF16,
+      MergeArgs a{src, wp, wp, src, 0, 1, const_cast<float*>(wp), wp, wp, 0.f, T, d, dtype == ATTNRES_BF16,
                   const_cast<void*>(out)};
       return merge_fast_ok(a) ? 1 : 0;
     }
     case 3: {
-      AccumArgs a{const_cast<float*>(wp), src, 0, const_cast<void*>(out), T, d, dtype == ATTNRES_BF16};
+      AccumArgs a{wp, src, 0, 1, nullptr, const_cast<void*>(out), T, d, dtype == ATTNRES_BF16};
       return accum_fast_ok(a) ? 1 : 0;
     }
     default: return -1;

@@ -123,9 +123,11 @@ __global__ void __launch_bounds__((FullTraits<CH>::kNW + 1) * kWarp, FullTraits<
       const int rows = static_cast<int>(r0 + (tile + 1) * R / ntiles - row0);
       const uint32_t bytes = static_cast<uint32_t>(rows) * D * sizeof(Tin);
       const uint32_t fb = smem_u32(&full_bar[stage]);
-      mbar_arrive_expect_tx(fb, bytes);
-      bulk_g2s(smem_u32(stages + static_cast<size_t>(stage) * kStageElems),
-               V + (static_cast<int64_t>(src) * a.src_stride + row0 * D) * sizeof(Tin), bytes, fb);
+      if (it != a.withhold) {  // the test hook leaves this stage unfilled
+        mbar_arrive_expect_tx(fb, bytes);
+        bulk_g2s(smem_u32(stages + static_cast<size_t>(stage) * kStageElems),
+                 V + (static_cast<int64_t>(src) * a.src_stride + row0 * D) * sizeof(Tin), bytes, fb);
+      }
       ++issued;
       if (++stage == nstage) {
         stage = 0;
@@ -134,9 +136,11 @@ __global__ void __launch_bounds__((FullTraits<CH>::kNW + 1) * kWarp, FullTraits<
     }
     if (!ok) {
       atomicOr(&g_full_timeout, 1u);
-      // Let the copies still in flight land before this CTA's memory goes.
+      // Let the copies still in flight land before this CTA's memory goes
+      // (a withheld copy was never issued).
       for (int64_t it = issued > nstage ? issued - nstage : 0; it < issued; ++it)
-        (void)mbar_wait(smem_u32(&full_bar[it % nstage]), static_cast<uint32_t>((it / nstage) & 1));
+        if (it != a.withhold)
+          (void)mbar_wait(smem_u32(&full_bar[it % nstage]), static_cast<uint32_t>((it / nstage) & 1));
     }
     return;
   }

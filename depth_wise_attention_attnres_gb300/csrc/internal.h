@@ -41,6 +41,10 @@ struct FullArgs {
   int late_wait;
   PreNorm pre;          // out may be nullptr when pre.gamma is set
   const float* Q;       // [T, d] fp32 per-token query (input-dependent); w then unused
+  // Failure-path test hook (attnres_test_withhold_stage): the producer of each
+  // CTA leaves its copy number `withhold` unissued, so the consumers' bounded
+  // wait for it runs out. -1 (the default) withholds nothing.
+  int64_t withhold = -1;
 };
 
 // S queries over the same n_src sources (stage 1; the general kernel also
@@ -60,14 +64,21 @@ struct MultiArgs {
   float* lse;           // [S, T] or nullptr
   PreNorm pre;          // S == 1 only (a Full read); out[0] may then be nullptr
   const float* Q;       // S == 1 only: [T, d] fp32 per-token query instead of W
+  int64_t withhold = -1;  // test hook of the tensor-core stage 1 (as FullArgs)
 };
 
+// Stage-2 merge of one sublayer (merge.cu). The running sum it merges is
+// formed as base + f_0 + ... + f_{q-1}, added in that order in fp32 (the
+// order the forward's sequential running sum uses, so any split between a
+// stored base and re-read outputs gives the same bits).
 struct MergeArgs {
   const void* O;
   const float* lse;
-  float* P;
-  const void* f;        // nullptr: P used as is
-  int p_empty;
+  const float* P;       // stored fp32 running sum to start from; nullptr: none
+  const void* parts;    // the q sublayer outputs added to it, part_stride apart
+  int64_t part_stride;  // elements
+  int nparts;           // q >= 0; q == 0 needs P
+  float* P_out;         // the resulting running sum (fp32, may be P); nullptr: not stored
   const float* w;
   const float* gamma;
   float eps;
@@ -76,11 +87,13 @@ struct MergeArgs {
   int bf16;
   void* out;            // may be nullptr when pre.gamma is set
   PreNorm pre;
-  // Fetch the first tiles of O_j and f before waiting for the previous
-  // kernel: only when that kernel writes neither (in a Block pass, the merge
-  // before, never stage 1, which writes O_j).
+  // Fetch the first tiles of O_j and the parts before waiting for the previous
+  // kernel: only when that kernel writes none of them (in a Block pass, the
+  // merge before, never stage 1, which writes O_j).
   int early;
+  int64_t withhold = -1;  // test hook of the tiled merge (as FullArgs)
 };
+constexpr int kMaxMergeParts = 16;
 
 // Backward of one read (full_bwd.cu): dV, dw, dgamma accumulated in fp32.
 struct BwdArgs {
@@ -123,11 +136,15 @@ struct DsplitArgs {
 };
 constexpr int kMaxDsplitShard = 512;
 
+// Running-sum update or freeze (merge.cu): base + f_0 + ... + f_{q-1} in
+// fp32, in that order, into P_out (fp32) or, rounded, into summary.
 struct AccumArgs {
-  float* P;
-  const void* f;
-  int p_empty;
-  void* summary;        // nullptr: accumulate into P
+  const float* P;       // base; nullptr: none
+  const void* parts;    // q >= 1 sublayer outputs, part_stride apart
+  int64_t part_stride;
+  int nparts;
+  float* P_out;         // fp32 result (may be P); used when summary is nullptr
+  void* summary;        // storage-dtype result; nullptr: write P_out
   int64_t T;
   int d;
   int bf16;
@@ -200,6 +217,11 @@ cudaError_t launch_psum(float* dst, const float* prev, const void* f, int is_bf1
 cudaError_t launch_gupdate(float* G, float* ds, float* dfp, int64_t E, cudaStream_t s);
 cudaError_t launch_spread(float* dst, int64_t dst_stride, int R, const float* g, int64_t E, cudaStream_t s);
 cudaError_t take_timeout_bwd(unsigned int* flag);
+
+// Failure-path test hooks (api.cu), off by default. Which producer, if any,
+// withholds a copy: the tile index to leave unissued, or -1.
+enum WithholdKernel { kWithholdNone = 0, kWithholdFull = 1, kWithholdStage1Tc = 2, kWithholdMerge = 3 };
+int64_t withhold_for(WithholdKernel k);
 
 // Device-side timeout records of each kernel file: read and clear (blocking).
 cudaError_t take_timeout_full(unsigned int* flag);

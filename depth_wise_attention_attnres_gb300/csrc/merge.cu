@@ -52,10 +52,11 @@ struct MergeGeom {
   int wq_off, red_off, stage_off, total;
 };
 
-// pre: room for gamma_pre next to w * gamma (the pre-norm merge).
-inline MergeGeom merge_geom(int d, int es, bool pre) {
+// A stage holds TM rows of O_j, of each of the q parts and (with a stored
+// base) of P. pre: room for gamma_pre next to w * gamma (the pre-norm merge).
+inline MergeGeom merge_geom(int d, int es, bool pre, int nparts, bool with_base) {
   MergeGeom g{};
-  const int row_bytes = d * (2 * es + 4);
+  const int row_bytes = d * (es * (1 + nparts) + (with_base ? 4 : 0));
   g.TM = 8;
   while (g.TM > 1 && g.TM * row_bytes > kMStageBudget) g.TM >>= 1;
   g.wpr = kMNW / g.TM;
@@ -84,8 +85,11 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
   const int d = a.d, TM = g.TM;
   const uint32_t row_t = static_cast<uint32_t>(d) * sizeof(T);
   const uint32_t row_p = static_cast<uint32_t>(d) * 4u;
-  const bool with_f = a.f != nullptr;
-  const bool with_p = !(with_f && a.p_empty);
+  const int np = a.nparts;
+  const bool with_p = a.P != nullptr;
+  // Stage layout: O rows, then each part's rows, then P rows.
+  const uint32_t p_off = static_cast<uint32_t>(TM) * row_t * static_cast<uint32_t>(1 + np);
+  const uint32_t tx_row = row_t * static_cast<uint32_t>(1 + np) + (with_p ? row_p : 0u);
   const int64_t ntok = a.T;
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * ntok / gridDim.x;
   const int64_t r1 = static_cast<int64_t>(blockIdx.x + 1) * ntok / gridDim.x;
@@ -108,19 +112,24 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
     uint32_t phase = 0;
     int issued = 0;
     bool ok = true;
-    // With a.early the first stages' O_j and f rows (which no kernel still
+    // O_j rows and the parts' rows of tile t into stage st.
+    auto load_inputs = [&](unsigned char* st, int64_t row0, uint32_t rows, uint32_t fb) {
+      bulk_g2s(smem_u32(st), static_cast<const T*>(a.O) + row0 * d, rows * row_t, fb);
+      for (int u = 0; u < np; ++u)
+        bulk_g2s(smem_u32(st + static_cast<uint32_t>(1 + u) * TM * row_t),
+                 static_cast<const T*>(a.parts) + u * a.part_stride + row0 * d, rows * row_t, fb);
+    };
+    // With a.early the first stages' O_j and part rows (which no kernel still
     // running writes) are fetched before the previous kernel has finished;
-    // their P rows, which it writes, after.
+    // their P rows, which it may write, after.
     const int t_pre = a.early ? min(kMStages, ntiles) : 0;
     for (int t = 0; t < t_pre; ++t) {
       const int64_t row0 = r0 + static_cast<int64_t>(t) * R / ntiles;
       const uint32_t rows = static_cast<uint32_t>(r0 + static_cast<int64_t>(t + 1) * R / ntiles - row0);
       unsigned char* st = stages + static_cast<size_t>(t) * g.stage_bytes;
       const uint32_t fb = smem_u32(&full_bar[t]);
-      mbar_arrive_expect_tx(fb, rows * (row_t + (with_f ? row_t : 0u) + (with_p ? row_p : 0u)));
-      bulk_g2s(smem_u32(st), static_cast<const T*>(a.O) + row0 * d, rows * row_t, fb);
-      if (with_f)
-        bulk_g2s(smem_u32(st + TM * row_t), static_cast<const T*>(a.f) + row0 * d, rows * row_t, fb);
+      mbar_arrive_expect_tx(fb, rows * tx_row);
+      load_inputs(st, row0, rows, fb);
     }
     pdl_wait();
     pdl_trigger();
@@ -128,7 +137,7 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
       const int64_t row0 = r0 + static_cast<int64_t>(t) * R / ntiles;
       const uint32_t rows = static_cast<uint32_t>(r0 + static_cast<int64_t>(t + 1) * R / ntiles - row0);
       unsigned char* st = stages + static_cast<size_t>(t) * g.stage_bytes;
-      if (with_p) bulk_g2s(smem_u32(st + 2 * TM * row_t), a.P + row0 * d, rows * row_p, smem_u32(&full_bar[t]));
+      if (with_p) bulk_g2s(smem_u32(st + p_off), a.P + row0 * d, rows * row_p, smem_u32(&full_bar[t]));
     }
     issued = t_pre;
     s = t_pre % kMStages;
@@ -142,11 +151,11 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
       const uint32_t rows = static_cast<uint32_t>(r0 + static_cast<int64_t>(t + 1) * R / ntiles - row0);
       unsigned char* st = stages + static_cast<size_t>(s) * g.stage_bytes;
       const uint32_t fb = smem_u32(&full_bar[s]);
-      mbar_arrive_expect_tx(fb, rows * (row_t + (with_f ? row_t : 0u) + (with_p ? row_p : 0u)));
-      bulk_g2s(smem_u32(st), static_cast<const T*>(a.O) + row0 * d, rows * row_t, fb);
-      if (with_f)
-        bulk_g2s(smem_u32(st + TM * row_t), static_cast<const T*>(a.f) + row0 * d, rows * row_t, fb);
-      if (with_p) bulk_g2s(smem_u32(st + 2 * TM * row_t), a.P + row0 * d, rows * row_p, fb);
+      if (t != a.withhold) {  // the test hook leaves this stage unfilled
+        mbar_arrive_expect_tx(fb, rows * tx_row);
+        load_inputs(st, row0, rows, fb);
+        if (with_p) bulk_g2s(smem_u32(st + p_off), a.P + row0 * d, rows * row_p, fb);
+      }
       ++issued;
       if (++s == kMStages) {
         s = 0;
@@ -155,8 +164,10 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
     }
     if (!ok) {
       atomicOr(&g_merge_timeout, 1u);
+      // Let the copies still in flight land (a withheld tile was never issued).
       for (int it = issued > kMStages ? issued - kMStages : 0; it < issued; ++it)
-        (void)mbar_wait(smem_u32(&full_bar[it % kMStages]), static_cast<uint32_t>((it / kMStages) & 1));
+        if (it != a.withhold)
+          (void)mbar_wait(smem_u32(&full_bar[it % kMStages]), static_cast<uint32_t>((it / kMStages) & 1));
     }
     return;
   }
@@ -193,8 +204,7 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
     const bool wok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[s]), phase));
     const unsigned char* st = stages + static_cast<size_t>(s) * g.stage_bytes;
     const T* so = reinterpret_cast<const T*>(st) + rslot * d;
-    const T* sf = reinterpret_cast<const T*>(st + TM * row_t) + rslot * d;
-    const float* sp = reinterpret_cast<const float*>(st + 2 * TM * row_t) + rslot * d;
+    const float* sp = reinterpret_cast<const float*>(st + p_off) + rslot * d;
     float p[Q][4];
     float ss = 0.f, dot = 0.f;
     if (wok && live) {
@@ -202,17 +212,21 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
       for (int q = 0; q < Q; ++q) {
         const int k = kbeg + (q * 32 + lane) * 4;
         if (k < kend) {
+          // The running sum: the stored base (or the first part as is), then
+          // the parts in order, each added in fp32.
+          int u0 = 0;
           if (with_p) {
             lds4(sp + k, p[q]);
           } else {
-            p[q][0] = p[q][1] = p[q][2] = p[q][3] = 0.f;
+            lds4(reinterpret_cast<const T*>(st + TM * row_t) + rslot * d + k, p[q]);
+            u0 = 1;
           }
-          if (with_f) {
+          for (int u = u0; u < np; ++u) {
             float f[4];
-            lds4(sf + k, f);
+            lds4(reinterpret_cast<const T*>(st + static_cast<uint32_t>(1 + u) * TM * row_t) + rslot * d + k, f);
             p[q][0] += f[0]; p[q][1] += f[1]; p[q][2] += f[2]; p[q][3] += f[3];
-            st4(a.P + row * d + k, p[q]);
           }
+          if (a.P_out) st4(a.P_out + row * d + k, p[q]);
           const float4 w4 = *reinterpret_cast<const float4*>(wq + k);
           ss = fmaf(p[q][0], p[q][0], ss); ss = fmaf(p[q][1], p[q][1], ss);
           ss = fmaf(p[q][2], p[q][2], ss); ss = fmaf(p[q][3], p[q][3], ss);
@@ -304,24 +318,38 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
 
 // ---------------------------------------------------------- general merge --
 
+// The running sum of one element: the stored base (or the first part as is),
+// then the parts in order, each added in fp32.
+template <typename T>
+__device__ __forceinline__ float running_sum_at(const float* P, const void* parts, int64_t part_stride, int np,
+                                                int64_t off) {
+  const T* f = static_cast<const T*>(parts);
+  float p;
+  int u = 0;
+  if (P) {
+    p = P[off];
+  } else {
+    p = to_f32(f[off]);
+    u = 1;
+  }
+  for (; u < np; ++u) p += to_f32(f[u * part_stride + off]);
+  return p;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kBlock) merge_generic_kernel(MergeArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = a.d;
   const float inv_d = 1.0f / static_cast<float>(d);
+  // Each lane forms and writes only the elements it owns, so P_out may be P;
+  // with no P_out the running sum is formed again where it is needed.
   for (int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + warp; row < a.T;
        row += static_cast<int64_t>(gridDim.x) * kWarps) {
     float ss = 0.f, dot = 0.f;
     for (int k = lane; k < d; k += 32) {
       const int64_t off = row * d + k;
-      float p;
-      if (a.f) {
-        const float f = to_f32(static_cast<const T*>(a.f)[off]);
-        p = a.p_empty ? f : a.P[off] + f;
-        a.P[off] = p;
-      } else {
-        p = a.P[off];
-      }
+      const float p = running_sum_at<T>(a.P, a.parts, a.part_stride, a.nparts, off);
+      if (a.P_out) a.P_out[off] = p;
       ss = fmaf(p, p, ss);
       dot = fmaf(a.w[k] * a.gamma[k], p, dot);
     }
@@ -332,11 +360,14 @@ __global__ void __launch_bounds__(kBlock) merge_generic_kernel(MergeArgs a) {
     const float M = fmaxf(lse, s);
     const float ea = __expf(lse - M), eb = __expf(s - M);
     const float inv = 1.0f / (ea + eb);
+    // The running sum again: from P_out where it was stored (P may be P_out).
+    const float* Pn = a.P_out;
     float zq = 0.f;
     for (int k = lane; k < d; k += 32) {
       const int64_t off = row * d + k;
       const float o = to_f32(static_cast<const T*>(a.O)[off]);
-      const float z = fmaf(ea * inv, o, eb * inv * a.P[off]);
+      const float p = Pn ? Pn[off] : running_sum_at<T>(a.P, a.parts, a.part_stride, a.nparts, off);
+      const float z = fmaf(ea * inv, o, eb * inv * p);
       if (a.out) static_cast<T*>(a.out)[off] = from_f32<T>(z);
       zq = fmaf(z, z, zq);
     }
@@ -346,7 +377,8 @@ __global__ void __launch_bounds__(kBlock) merge_generic_kernel(MergeArgs a) {
       for (int k = lane; k < d; k += 32) {
         const int64_t off = row * d + k;
         const float o = to_f32(static_cast<const T*>(a.O)[off]);
-        const float z = fmaf(ea * inv, o, eb * inv * a.P[off]);
+        const float p = Pn ? Pn[off] : running_sum_at<T>(a.P, a.parts, a.part_stride, a.nparts, off);
+        const float z = fmaf(ea * inv, o, eb * inv * p);
         static_cast<T*>(a.pre.out)[off] = from_f32<T>(a.pre.gamma[k] * (z * rr));
       }
     }
@@ -384,21 +416,27 @@ template <typename T>
 __global__ void __launch_bounds__(kBlock) accum_fast_kernel(AccumArgs a, int64_t nchunks) {
   pdl_trigger();
   pdl_wait();
+  const T* f = static_cast<const T*>(a.parts);
   for (int64_t c = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x; c < nchunks;
        c += static_cast<int64_t>(gridDim.x) * kBlock) {
     const int64_t off = c * 4;
-    float f[4], p[4];
-    ldg4(static_cast<const T*>(a.f) + off, f);
-    if (a.p_empty) {
-      p[0] = f[0]; p[1] = f[1]; p[2] = f[2]; p[3] = f[3];
-    } else {
+    float p[4];
+    int u = 0;
+    if (a.P) {
       ldg4(a.P + off, p);
-      p[0] += f[0]; p[1] += f[1]; p[2] += f[2]; p[3] += f[3];
+    } else {
+      ldg4(f + off, p);
+      u = 1;
+    }
+    for (; u < a.nparts; ++u) {
+      float x[4];
+      ldg4(f + u * a.part_stride + off, x);
+      p[0] += x[0]; p[1] += x[1]; p[2] += x[2]; p[3] += x[3];
     }
     if (a.summary)
       st4(static_cast<T*>(a.summary) + off, p);
     else
-      st4(a.P + off, p);
+      st4(a.P_out + off, p);
   }
 }
 
@@ -406,12 +444,11 @@ template <typename T>
 __global__ void __launch_bounds__(kBlock) accum_generic_kernel(AccumArgs a, int64_t n) {
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * kBlock) {
-    const float f = to_f32(static_cast<const T*>(a.f)[i]);
-    const float p = a.p_empty ? f : a.P[i] + f;
+    const float p = running_sum_at<T>(a.P, a.parts, a.part_stride, a.nparts, i);
     if (a.summary)
       static_cast<T*>(a.summary)[i] = from_f32<T>(p);
     else
-      a.P[i] = p;
+      a.P_out[i] = p;
   }
 }
 
@@ -429,17 +466,19 @@ unsigned grid_for(int64_t work_items, int per_block, const void* kernel) {
 bool merge_fast_ok(const MergeArgs& a) {
   const int es = a.bf16 ? 2 : 4;
   if (a.d % 4 != 0 || (a.d * es) % 16 != 0) return false;
-  const MergeGeom g = merge_geom(a.d, es, a.pre.gamma != nullptr);
+  if ((a.part_stride * es) % 16 != 0) return false;
+  const MergeGeom g = merge_geom(a.d, es, a.pre.gamma != nullptr, a.nparts, a.P != nullptr);
   const int per_warp = (a.d + g.wpr - 1) / g.wpr;
   // Every part of a row starts on a 4-feature chunk (aligned vector loads).
   if (per_warp % 4 != 0 || per_warp > 8 * 128 || g.total > 227 * 1024) return false;
-  return aligned16(a.O) && aligned16(a.P) && aligned16(a.out) && (a.f == nullptr || aligned16(a.f)) &&
-         (!a.pre.gamma || (aligned16(a.pre.gamma) && aligned16(a.pre.out)));
+  return aligned16(a.O) && aligned16(a.P) && aligned16(a.P_out) && aligned16(a.out) &&
+         (a.nparts == 0 || aligned16(a.parts)) && (!a.pre.gamma || (aligned16(a.pre.gamma) && aligned16(a.pre.out)));
 }
 
 bool accum_fast_ok(const AccumArgs& a) {
-  if (a.d % 4 != 0) return false;
-  return aligned16(a.P) && aligned16(a.f) && (a.summary == nullptr || aligned16(a.summary));
+  const int es = a.bf16 ? 2 : 4;
+  if (a.d % 4 != 0 || (a.part_stride * es) % 16 != 0) return false;
+  return aligned16(a.P) && aligned16(a.P_out) && aligned16(a.parts) && aligned16(a.summary);
 }
 
 namespace {
@@ -456,7 +495,7 @@ cudaError_t launch_merge_tiles(const MergeArgs& a, const MergeGeom& g, cudaStrea
 
 template <typename T>
 cudaError_t launch_merge_dtype(const MergeArgs& a, cudaStream_t s) {
-  const MergeGeom g = merge_geom(a.d, sizeof(T), a.pre.gamma != nullptr);
+  const MergeGeom g = merge_geom(a.d, sizeof(T), a.pre.gamma != nullptr, a.nparts, a.P != nullptr);
   const int per_warp = (a.d + g.wpr - 1) / g.wpr;
   int q = 1;
   while (q * 128 < per_warp) q <<= 1;

@@ -52,19 +52,20 @@ constexpr int kThreads = (kSW + kOW + 1) * kWarp;   // + producer warp
 constexpr int kMaxPairs = 16;                       // pairs of a tile: one m16 MMA tile
 constexpr int kQ = 8;                               // MMA query columns (queries >= S are zero)
 constexpr int kF = 8;                               // features per thread on the CUDA-core output path
-constexpr int kMaxBuf = 6;                          // tile buffers
+constexpr int kMaxBuf = 8;                          // tile buffers
 constexpr int kBarBytes = 256;
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kBtBytes = 16 * 256;                  // MMA weight fragments of a tile: TM * ceil(n / 8) <= 16 blocks
+constexpr int kStgPitch = 2 * 128 + 16;             // output staging row: two 64-feature chunks, padded
 // full + empty per buffer, two weight handovers each way, then the abort flag
 static_assert((2 * kMaxBuf + 4) * 8 + 4 <= kBarBytes, "barrier area too small");
 
 struct TcGeom {
-  int npair;       // pairs a tile buffer holds (16 or 8)
-  int TM;          // tokens per tile (npair / n)
+  int npair;       // pairs a tile holds (TM * n <= 16)
+  int TM;          // tokens per tile
   int P;           // pairs of a tile (TM * n)
   int pitch;       // bytes between the rows of w * gamma (d * 2 + 16)
-  int spitch;      // bytes between the query rows of an output warp's staging area
+  int srows;       // staging rows per output warp: the S queries (+ one row that absorbs unused ones)
   int buf_bytes;   // one tile buffer (npair rows of d bf16 in swizzled 128-byte lines)
   int nbuf;        // tile buffers
   int w_off, red_off, al_off, bt_off, stg_off, buf_off, total;
@@ -72,34 +73,37 @@ struct TcGeom {
 
 inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
-inline TcGeom tc_geom_for(int n, int d, int S, int npair) {
+// The fixed areas hold only what the S queries need: the hi and lo rows of
+// w * gamma of each query (2S rows) and S staging rows per output warp.
+inline TcGeom tc_geom_for(int n, int d, int S, int TM) {
   TcGeom g{};
-  g.npair = npair;
+  g.TM = TM;
+  g.P = TM * n;
+  g.npair = g.P;
   g.pitch = d * 2 + 16;
-  g.spitch = ((d / 64 + kOW - 1) / kOW) * 128 + 16;
-  g.TM = n > 0 ? npair / n : 0;
-  g.P = g.TM * n;
-  g.w_off = kBarBytes;                                  // bf16 hi rows [kQ], then lo rows [kQ]
-  g.red_off = g.w_off + 2 * kQ * g.pitch;               // fp32 [npair][S + 1][kSW] partials
-  g.al_off = g.red_off + kSW * npair * (S + 1) * 4;     // float2 [2][npair][S2] weights as (a, a)
-  g.bt_off = g.al_off + 2 * npair * round_up(S, 2) * 8;  // bf16 MMA weight fragments [2][kBtBytes]
-  g.stg_off = g.bt_off + 2 * kBtBytes;                  // bf16 [kOW][kQ][spitch] output staging
-  g.buf_off = round_up(g.stg_off + kOW * kQ * g.spitch, 1024);
-  g.buf_bytes = npair * d * 2;
+  g.srows = S < kQ ? S + 1 : kQ;
+  g.w_off = kBarBytes;                                  // bf16 hi rows [S], then lo rows [S]
+  g.red_off = g.w_off + 2 * S * g.pitch;                // fp32 [npair][S + 1][kSW] partials
+  g.al_off = g.red_off + kSW * g.npair * (S + 1) * 4;   // float2 [2][npair][S2] weights as (a, a)
+  g.bt_off = g.al_off + 2 * g.npair * round_up(S, 2) * 8;  // bf16 MMA weight fragments [2][kBtBytes]
+  g.stg_off = g.bt_off + 2 * kBtBytes;                  // bf16 [kOW][srows][kStgPitch] output staging
+  g.buf_off = round_up(g.stg_off + kOW * g.srows * kStgPitch, 1024);
+  g.buf_bytes = g.npair * d * 2;
   g.nbuf = (kSmemLimit - 1024 - g.buf_off) / g.buf_bytes;  // 1 KB slack to align the base
   if (g.nbuf > kMaxBuf) g.nbuf = kMaxBuf;
   g.total = g.buf_off + g.nbuf * g.buf_bytes + 1024;
   return g;
 }
 
-// 16-pair tiles when three buffers fit, else 8-pair tiles when they hold a
-// row of every source and three of them fit, else 16-pair tiles in two.
+// The most tokens per tile (at most 16 pairs) that leave four buffers, so
+// that the score and output roles each hold one while two more load; else
+// one token per tile with as many buffers as fit.
 inline TcGeom tc_geom(int n, int d, int S) {
-  const TcGeom g = tc_geom_for(n, d, S, 16);
-  if (g.TM >= 1 && g.nbuf >= 3) return g;
-  const TcGeom h = tc_geom_for(n, d, S, 8);
-  if (h.TM >= 1 && h.nbuf >= 3) return h;
-  return g;
+  for (int TM = kMaxPairs / n; TM > 1; --TM) {
+    const TcGeom g = tc_geom_for(n, d, S, TM);
+    if (g.nbuf >= 4) return g;
+  }
+  return tc_geom_for(n, d, S, 1);
 }
 
 // Which output path a launch takes (the tensor cores pay off from about 32
@@ -185,8 +189,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Rows past T are zero-filled; the transaction always counts the whole box.
       const uint32_t fb = smem_u32(&full_bar[b]);
-      mbar_arrive_expect_tx(fb, box_bytes);
-      tma_load_tile(smem_u32(bufs + b * g.buf_bytes), &tmap, static_cast<int>(tile * TM), fb);
+      if (issued != a.withhold) {  // the test hook leaves this buffer unfilled
+        mbar_arrive_expect_tx(fb, box_bytes);
+        tma_load_tile(smem_u32(bufs + b * g.buf_bytes), &tmap, static_cast<int>(tile * TM), fb);
+      }
       ++issued;
       if (++b == nbuf) {
         b = 0;
@@ -195,27 +201,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok) {
       atomicOr(&g_stage1tc_timeout, 1u);
-      // Let the copies still in flight land before this CTA's memory goes.
+      // Let the copies still in flight land before this CTA's memory goes
+      // (a withheld copy was never issued).
       for (int64_t it = issued > nbuf ? issued - nbuf : 0; it < issued; ++it)
-        (void)mbar_wait(smem_u32(&full_bar[it % nbuf]), static_cast<uint32_t>((it / nbuf) & 1));
+        if (it != a.withhold)
+          (void)mbar_wait(smem_u32(&full_bar[it % nbuf]), static_cast<uint32_t>((it / nbuf) & 1));
     }
     return;
   }
 
-  // w * gamma as bf16 hi + lo rows (queries >= S are zero), by the score and
-  // output warps while the producer already fills the pipeline; loads are
-  // issued in groups of four per thread before any of them is used.
+  // w * gamma as bf16 hi + lo rows (row q: hi part of query q, row S + q:
+  // its lo part), by the score and output warps while the producer already
+  // fills the pipeline; loads are issued in groups of four per thread before
+  // any of them is used.
   {
     constexpr int kCT = kScoreThreads + kOutThreads;
-    const int nv = kQ * d / 4;
+    const int nv = S * d / 4;
     for (int base = tid; base < nv; base += 4 * kCT) {
       float4 wv[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int v = base + u * kCT;
-        const int q = v < nv ? (v * 4) / d : kQ;
         wv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (q < S) {
+        if (v < nv) {
           const float4 x = *reinterpret_cast<const float4*>(a.W + v * 4);
           const float4 y = *reinterpret_cast<const float4*>(a.Gamma + v * 4);
           wv[u] = make_float4(x.x * y.x, x.y * y.y, x.z * y.z, x.w * y.w);
@@ -234,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             lo[e] = w[e] - hi[e];
           }
           st4(reinterpret_cast<bf16*>(wsm + q * g.pitch) + k, hi);
-          st4(reinterpret_cast<bf16*>(wsm + (kQ + q) * g.pitch) + k, lo);
+          st4(reinterpret_cast<bf16*>(wsm + (S + q) * g.pitch) + k, lo);
         }
       }
     }
@@ -249,7 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cb = warp * nchunk / kSW, ce = (warp + 1) * nchunk / kSW;  // this warp's chunks
     const int a_row = (lane & 7) + ((lane >> 3) & 1) * 8;
     const int a_koff = (lane >> 4) * 8;
-    const int b_row = (lane & 7) + ((lane >> 4) & 1) * kQ;  // hi rows, then lo rows
+    // Hi rows, then lo rows. Lanes of queries >= S read query 0's rows: what
+    // they feed lands only in the MMA rows or columns of queries >= S, which
+    // are never read.
+    const int b_row = ((lane & 7) < S ? (lane & 7) : 0) + ((lane >> 4) & 1) * S;
     const int b_koff = ((lane >> 3) & 1) * 8;
     const uint32_t b_base = smem_u32(wsm + b_row * g.pitch) + (cb * 64 + b_koff) * 2;
     const uint32_t a_x = static_cast<uint32_t>(a_koff) * 2u;  // this lane's 16-byte unit within a k-step
@@ -425,16 +436,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ncw = ce - cb;
       const int f_beg = cb * 64;
       const int nk = (n + 7) >> 3;
-      unsigned char* stg = smem + g.stg_off + ow * kQ * g.spitch;
+      unsigned char* stg = smem + g.stg_off + ow * g.srows * kStgPitch;
       const int l8 = lane & 7, lhalf = (lane >> 3) & 1;
-      const uint32_t st_base = smem_u32(stg) + l8 * g.spitch + lhalf * 16;
+      // Staging row of query l8; queries >= S share the last row, whose
+      // contents are never copied out.
+      const uint32_t st_base = smem_u32(stg) + (l8 < S ? l8 : g.srows - 1) * kStgPitch + lhalf * 16;
       const uint32_t lx = static_cast<uint32_t>(lhalf) << 4;
-      const int pq = ncw * 8;  // 16-byte pieces of one query row of this warp
-      int lg_pq = -1;
-      if ((pq & (pq - 1)) == 0) {
-        lg_pq = 0;
-        while ((1 << lg_pq) < pq) ++lg_pq;
-      }
       for (int64_t tile = t0; tile < t1; ++tile, ++it) {
         const int ab = it & 1;
         const uint32_t aph = static_cast<uint32_t>((it >> 1) & 1);
@@ -453,8 +460,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint2 bf[2];
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb) bf[kb] = kb < nk ? bt[(r * nk + kb) * 32 + lane] : make_uint2(0u, 0u);
+          const int64_t row = row0 + r;
           // Two chunks (8 blocks) at a time: all fragment loads, then the
-          // independent MMAs, then the transposing stores.
+          // independent MMAs, then the transposing stores into the staging
+          // rows, which then go out as 16-byte pieces of 256-byte row runs.
           for (int c = 0; c < ncw; c += 2) {
             float acc[8][4];
 #pragma unroll
@@ -484,21 +493,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               }
             }
+            __syncwarp();  // the previous copy-out has read the staging rows
 #pragma unroll
             for (int u = 0; u < 8; ++u)
               if (u < 4 || two)
-                stsm_x2_trans(st_base + static_cast<uint32_t>(c * 128 + u * 32), pack_bf16x2(acc[u][0], acc[u][1]),
+                stsm_x2_trans(st_base + static_cast<uint32_t>(u * 32), pack_bf16x2(acc[u][0], acc[u][1]),
                               pack_bf16x2(acc[u][2], acc[u][3]));
+            __syncwarp();
+            const int pq = two ? 16 : 8;  // 16-byte pieces per query row
+            for (int idx = lane; idx < S * pq; idx += kWarp) {
+              const int q = two ? idx >> 4 : idx >> 3;
+              const int ch = idx - q * pq;
+              const uint4 v = *reinterpret_cast<const uint4*>(stg + q * kStgPitch + ch * 16);
+              *reinterpret_cast<uint4*>(static_cast<bf16*>(a.out[q]) + row * d + f_beg + c * 64 + ch * 8) = v;
+            }
           }
-          __syncwarp();
-          const int64_t row = row0 + r;
-          for (int idx = lane; idx < S * pq; idx += kWarp) {
-            const int q = lg_pq >= 0 ? idx >> lg_pq : idx / pq;
-            const int ch = idx - q * pq;
-            const uint4 v = *reinterpret_cast<const uint4*>(stg + q * g.spitch + ch * 16);
-            *reinterpret_cast<uint4*>(static_cast<bf16*>(a.out[q]) + row * d + f_beg + ch * 8) = v;
-          }
-          __syncwarp();
         }
         __syncwarp();
         if (lane == 0) {

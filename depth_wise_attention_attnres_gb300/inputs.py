@@ -75,6 +75,12 @@ WORKLOADS = {
     "full_pass_141x32768x640_bf16": Workload(
         "full_pass_141x32768x640_bf16", "full_pass", T=32768, d=640,
         dtype="bf16", w_std=0.05, R=141),
+    # The long-context blocks at 8192 tokens (about 4 GB on the device): a case
+    # small enough for profiler captures of every launch of a pass, whose
+    # per-launch data still exceeds the 129 MB L2.
+    "block_pass_8x6x8192x2048_bf16": Workload(
+        "block_pass_8x6x8192x2048_bf16", "block_pass", T=8192, d=2048,
+        dtype="bf16", w_std=0.02, N=8, S=6, depth_scaled=False),
     # Long-context prefill, 128K tokens, d=2048, 48 sublayers in 8 blocks of 6.
     "block_pass_8x6x131072x2048_bf16": Workload(
         "block_pass_8x6x131072x2048_bf16", "block_pass", T=131072, d=2048,

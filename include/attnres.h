@@ -350,6 +350,55 @@ int attnres_block_summary_accumulate(float* P, const void* f, int32_t p_is_empty
                                      void* stream);
 
 /*
+ * attnres_block_merge_parts - the stage-2 merge with the running sum given in
+ * parts: P_j = P_base + f_0 + ... + f_{n_parts-1}, the sum of the block's
+ * first j outputs (LLMRes blog "Block Attention Residuals": the running sum
+ * of the current block is one more softmax source, DepthBench reading notes
+ * section 2.5), formed in fp32 and added in that order. This is the order in
+ * which the one-step calls above build it, so keeping a sum in P or forming
+ * it again from the outputs gives the same bits. Re-reading a few bf16
+ * outputs moves fewer bytes than storing and reloading an fp32 sum; the Block
+ * pass chooses by attnres_block_running_sum_plan.
+ *
+ *   O_j, lse_j  as in attnres_block_merge.
+ *   P_base      device, fp32 [T, d]: a stored running sum to start from, or
+ *               NULL (the sum starts from the first part; n_parts >= 1).
+ *   F_parts     device, the n_parts outputs [T, d] dtype, part_stride >= T*d
+ *               elements apart (part_stride unused when n_parts <= 1); n_parts
+ *               from 0 (P_base used as it is) to 16.
+ *   P_out       device, fp32 [T, d], or NULL: where P_j is stored. It may be
+ *               P_base itself (in place) but must not overlap anything else.
+ *   w, gamma    device, fp32 [d] of this sublayer.
+ *   out         device, [T, d] dtype; overlaps no other argument.
+ * Errors as attnres_block_merge.
+ */
+int attnres_block_merge_parts(const void* O_j, const float* lse_j, const float* P_base,
+                              const void* F_parts, int64_t part_stride, int32_t n_parts,
+                              float* P_out, const float* w, const float* gamma, float eps,
+                              int64_t T, int32_t d, int32_t dtype, void* out, void* stream);
+
+/*
+ * attnres_block_summary_parts - a running sum from parts (as in
+ * attnres_block_merge_parts, n_parts from 1 to 16): summary_out <- P_base +
+ * f_0 + ... rounded to dtype (the freeze of a block summary), or, with
+ * summary_out NULL, P_out <- that sum in fp32 (P_out may be P_base).
+ */
+int attnres_block_summary_parts(const float* P_base, const void* F_parts, int64_t part_stride,
+                                int32_t n_parts, float* P_out, void* summary_out, int64_t T,
+                                int32_t d, int32_t dtype, void* stream);
+
+/*
+ * attnres_block_running_sum_plan - which running sums attnres_block_pass keeps
+ * in P_scratch for blocks of S sublayers stored as dtype: stored[j] = 1 for
+ * each 1 <= j < S whose P_j is written (stored[0] = stored[S] = 0). Every
+ * other P_j is formed from the last kept one, or from nothing, plus the
+ * outputs since; the plan minimises the bytes each element moves (an output
+ * re-read costs 2 or 4 bytes, a kept fp32 sum 4 to write and 4 to read).
+ * Example: bf16, S = 6 keeps P_4 only. stored has S + 1 entries (host).
+ */
+int attnres_block_running_sum_plan(int32_t S, int32_t dtype, int32_t* stored);
+
+/*
  * attnres_block_pass - the reads of N blocks of S sublayers by the two-stage
  * computation, for stored sublayer outputs F (the synthetic sequencing a
  * model would interleave with its sublayers). Block n (0-based) runs stage 1
@@ -362,8 +411,12 @@ int attnres_block_summary_accumulate(float* P, const void* f, int32_t p_is_empty
  *               Src[0] holds the embedding (input); Src[1 ..] are written.
  *   O_scratch   device, [max(S-1,1), T, d] dtype workspace (stage-1 results).
  *   lse_scratch device, fp32 [S, T] workspace.
- *   P_scratch   device, fp32 [T, d] workspace (running sum).
+ *   P_scratch   device, fp32 [T, d] workspace (the running sums that
+ *               attnres_block_running_sum_plan says to keep).
  *   out         device, N*S outputs [T, d] dtype, out_stride >= T*d apart.
+ * Merge j of a block takes its running sum as the last kept one plus the
+ * outputs since (attnres_block_merge_parts); the freeze likewise
+ * (attnres_block_summary_parts).
  */
 int attnres_block_pass(const void* F, int64_t f_stride, int32_t N, int32_t S, int64_t T,
                        int32_t d, int32_t dtype, const float* W, const float* Gamma,
@@ -391,13 +444,27 @@ int attnres_block_pass(const void* F, int64_t f_stride, int32_t N, int32_t S, in
  *     (S > 1 ? (S-1)*T*d*es + 4*T*d : 0) + 4*S*T bytes (es = 2 for bf16, 4
  *     for fp32; each part rounded up to 256 bytes). A call that needs more
  *     than ATTNRES_NOALLOC_SCRATCH_BYTES returns ATTNRES_ERR_UNSUPPORTED and
- *     launches nothing. Example: bf16, d = 1024, S = 8 fits up to T = 3600.
- *   - Memory: every GPU on which the library is used holds the array
- *     (64 MiB) from the first use until the process exits.
- *   - Set-up: the first call on a device, with that device current, looks up
- *     the array's device address (cudaGetSymbolAddress) and caches it. Make
- *     that first call before any stream capture begins.
- *   - Sharing: all calls on a device share the one array, and it keeps the
+ *     launches nothing. Example: bf16, d = 1024, S = 8 fits up to T = 3634.
+ *     The pointer, dtype, eps and stride checks come first, so a call that is
+ *     both malformed and too large returns ATTNRES_ERR_INVALID_ARG (except
+ *     when T or d alone exceeds the array's size: ATTNRES_ERR_UNSUPPORTED).
+ *   - Memory: every CUDA context that loads the library's device code holds
+ *     the array (64 MiB) until the context is destroyed or the process
+ *     exits. With lazy module loading (the CUDA default) the array is
+ *     allocated when this entry point first runs in a context, and that first
+ *     call may synchronise the device while the module loads; with
+ *     CUDA_MODULE_LOADING=EAGER it is allocated when the context is created,
+ *     in every process that loads the library. A caller that budgets device
+ *     memory up front, or that must not synchronise later, should therefore
+ *     make one small warm-up call (for example T = 1) at start-up, before it
+ *     reserves its memory or starts its no-sync thread.
+ *   - Set-up: the first call in a CUDA context, with that context current,
+ *     looks up the array's device address (cudaGetSymbolAddress) and caches
+ *     it under the context's id. Make that first call before any stream
+ *     capture begins. After cudaDeviceReset, or when a primary context is
+ *     released and created again, the array is a new one: the next call looks
+ *     its address up again (and is then such a first call).
+ *   - Sharing: all calls in a context share the one array, and it keeps the
  *     contents of the last call. Nothing in it needs to start at zero (every
  *     byte a call reads was written earlier in the same call). Calls whose
  *     work overlaps on the GPU (for example on two streams) race on the
@@ -427,6 +494,38 @@ int attnres_device_status(void* stream);
  * record; the context stays usable. Returns the launch status.
  */
 int attnres_selftest_wait_timeout(void* stream);
+
+/*
+ * Failure-path test hooks. The pages define no error handling; these exist so
+ * that tests can drive the library's error paths without faulting a GPU. Both
+ * are off by default, process-wide (all devices and threads), and meant for
+ * tests only.
+ *
+ * attnres_test_fail_launch - arms a simulated launch failure: after `after`
+ * more launches succeed (kernels, and the memsets and copies of the Block
+ * backward), the next launch is not made and its call returns
+ * ATTNRES_ERR_CUDA, as a real launch error would; the hook then disarms
+ * itself. A call that makes several launches (a Full or Block pass) stops at
+ * the failed one: the launches before it ran, nothing after it is enqueued.
+ * after < 0 disarms. Returns the previous setting (-1 once an armed failure
+ * has fired), so a test can tell whether it was consumed.
+ */
+int64_t attnres_test_fail_launch(int64_t after);
+
+/*
+ * attnres_test_withhold_stage - makes the copy producer of one pipelined
+ * kernel leave one stage unfilled, so the consumers' bounded wait for it runs
+ * out (after about 2 s): the kernel records a timeout and returns, and
+ * attnres_device_status reports ATTNRES_ERR_TIMEOUT. kernel: 0 = off, 1 = the
+ * Full-read bulk kernel (index counts the (tile, source) copies of each CTA),
+ * 2 = the tensor-core stage 1 (index counts each CTA's tiles), 3 = the tiled
+ * merge (index counts each CTA's tiles; tiles fetched before the previous
+ * kernel finishes, in a Block pass, are never withheld). Every CTA with more
+ * than `index` copies withholds its copy number `index`; its other copies are
+ * issued and waited for before the CTA exits. Stays set until changed.
+ * Returns ATTNRES_ERR_INVALID_ARG for an unknown kernel or a negative index.
+ */
+int attnres_test_withhold_stage(int32_t kernel, int64_t index);
 
 /* Static description of a status code (never NULL). */
 const char* attnres_status_string(int32_t status);

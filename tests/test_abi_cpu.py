@@ -179,3 +179,115 @@ def test_kernel_selection(lib):
     assert binding.attnres_kernel_path(3, A, 2 * A, 0, 0, 16384, 1024, 1) == 1
     assert binding.attnres_kernel_path(2, A, 2 * A, 0, 0, 10, 3, 1) == 0
     assert binding.attnres_kernel_path(9, A, 2 * A, 0, 0, 10, 3, 1) == -1
+
+
+def test_injected_launch_failure_reports_cuda_error(lib):
+    """The launch-failure test hook: an armed failure makes the next launch
+    return ATTNRES_ERR_CUDA without being made (before any CUDA call, so this
+    runs without a GPU), and disarms itself once it fired."""
+    CUDA_ERR = 3
+    ptrs = (ctypes.c_void_p * 2)(P * 8, P * 16)
+    calls = [
+        lambda: lib.attnres_full_fwd(P, 64, 2, 4, 16, 1, P, P, 1e-6, 8 * P, 1, None),
+        lambda: lib.attnres_full_pass(P, 64, 3, 4, 16, 1, P, P, 1e-6, 8 * P, 64, 1, None),
+        lambda: lib.attnres_block_merge(P, 2 * P, 3 * P, 4 * P, 0, P, P, 1e-6, 4, 16, 1, 5 * P, None),
+        lambda: lib.attnres_block_summary_accumulate(P, 2 * P, 0, 3 * P, 4, 16, 1, None),
+        lambda: lib.attnres_rmsnorm(P, 4, 16, 1, P, 1e-6, 2 * P, None),
+        lambda: lib.attnres_block_pass(P, 64, 2, 2, 4, 16, 1, 9 * P, 9 * P, 1e-6, 2 * P, 64, 0, 3 * P, 4 * P,
+                                       5 * P, 6 * P, 64, None),
+    ]
+    assert binding.attnres_test_fail_launch(-1) == -1      # off by default
+    for call in calls:
+        assert binding.attnres_test_fail_launch(0) == -1
+        assert call() == CUDA_ERR
+        assert binding.attnres_test_fail_launch(-1) == -1  # it fired and disarmed
+    # Argument errors are found before any launch: they leave it armed.
+    binding.attnres_test_fail_launch(0)
+    assert lib.attnres_full_fwd(P, 64, 0, 4, 16, 1, P, P, 1e-6, 8 * P, 1, None) == INVALID
+    assert lib.attnres_block_stage1(P, 64, 2, 4, 16, 1, P, P, 0, 1e-6, ptrs, None, None) == INVALID
+    assert binding.attnres_test_fail_launch(-1) == 0
+    # Counting down: two more launches allowed, then the failure.
+    binding.attnres_test_fail_launch(2)
+    assert binding.attnres_test_fail_launch(-1) == 2
+
+
+def test_withhold_hook_validation(lib):
+    assert lib.attnres_test_withhold_stage(9, 0) == INVALID
+    assert lib.attnres_test_withhold_stage(1, -1) == INVALID
+    assert lib.attnres_test_withhold_stage(-1, 0) == INVALID
+    assert lib.attnres_test_withhold_stage(2, 3) == 0
+    assert lib.attnres_test_withhold_stage(0, -1) == 0      # off again
+
+
+def test_noalloc_validation_order(lib):
+    """attnres_block_pass_noalloc checks its arguments before its workspace
+    limit, so a call that is both malformed and too large reports the
+    malformed argument; a well-formed oversized call is refused as
+    unsupported. Neither reaches the GPU."""
+    N, S, T, d = 2, 8, 8192, 1024          # needs about 144 MiB of workspace: too large
+    E = T * d
+    f = ctypes.c_float(1e-6)
+    assert lib.attnres_block_pass_noalloc(P, E, N, S, T, d, 1, P, P, f, 2 * P, E, 0, 3 * P, E, None) == UNSUPPORTED
+    assert lib.attnres_block_pass_noalloc(None, E, N, S, T, d, 1, P, P, f, 2 * P, E, 0, 3 * P, E, None) == INVALID
+    assert lib.attnres_block_pass_noalloc(P, E - 1, N, S, T, d, 1, P, P, f, 2 * P, E, 0, 3 * P, E, None) == INVALID
+    assert lib.attnres_block_pass_noalloc(P, E, N, S, T, d, 1, P, P, ctypes.c_float(-1.0), 2 * P, E, 0, 3 * P, E,
+                                          None) == INVALID
+    assert lib.attnres_block_pass_noalloc(P, E, N, 0, T, d, 1, P, P, f, 2 * P, E, 0, 3 * P, E, None) == INVALID
+    assert lib.attnres_block_pass_noalloc(P, E, N, S, 0, d, 1, P, P, f, 2 * P, E, 0, 3 * P, E, None) == 0
+
+
+def _plan_bytes(S, es, kept):
+    """Bytes per element the running sums of one block move under a plan
+    (kept: the positions j < S whose sum is stored): position j (1..S, S the
+    freeze) reads the outputs since the last kept position m (es each) and,
+    if m > 0, the kept fp32 sum (4); a kept sum is written once (4)."""
+    total, m = 0, 0
+    for j in range(1, S + 1):
+        total += es * (j - m) + (4 if m > 0 else 0)
+        if j < S and j in kept:
+            total += 4
+            m = j
+    return total
+
+
+@pytest.mark.parametrize("dtype,es", [(1, 2), (0, 4)])
+def test_running_sum_plan_is_the_cheapest(lib, dtype, es):
+    import itertools
+    for S in range(1, 17):
+        plan = binding.attnres_block_running_sum_plan(S, dtype)
+        assert len(plan) == S + 1 and plan[0] == 0 and plan[S] == 0
+        kept = {j for j in range(1, S) if plan[j]}
+        got = _plan_bytes(S, es, kept)
+        best = min(_plan_bytes(S, es, set(c)) for r in range(S) for c in itertools.combinations(range(1, S), r))
+        assert got == best, (S, kept, got, best)
+        fewest = min(len(c) for r in range(S) for c in itertools.combinations(range(1, S), r)
+                     if _plan_bytes(S, es, set(c)) == best)
+        assert len(kept) == fewest
+    # The long-context workload's blocks (bf16, S = 6) keep P_4 alone:
+    # 38 bytes per element instead of 52 for a sum stored at every step.
+    assert binding.attnres_block_running_sum_plan(6, 1) == [0, 0, 0, 0, 1, 0, 0]
+    assert _plan_bytes(6, 2, {4}) == 38 and _plan_bytes(6, 2, {1, 2, 3, 4, 5}) == 52
+    assert lib.attnres_block_running_sum_plan(0, 1, None) == INVALID
+
+
+def test_merge_parts_validation(lib):
+    # (O, lse, P_base, F_parts, part_stride, n_parts, P_out, w, gamma, eps, T, d, dtype, out)
+    f = ctypes.c_float(1e-6)
+    E = 64
+    assert lib.attnres_block_merge_parts(P, 2 * P, None, None, E, 0, None, P, P, f, 4, 16, 1, 5 * P, None) == INVALID
+    assert lib.attnres_block_merge_parts(P, 2 * P, None, 3 * P, E - 1, 2, None, P, P, f, 4, 16, 1, 5 * P,
+                                         None) == INVALID                         # parts overlap each other
+    assert lib.attnres_block_merge_parts(P, 2 * P, None, 3 * P, E, 17, None, P, P, f, 4, 16, 1, 5 * P,
+                                         None) == INVALID                         # too many parts
+    assert lib.attnres_block_merge_parts(P, 2 * P, 4 * P, 3 * P, E, 2, 4 * P + 64, P, P, f, 4, 16, 1, 5 * P,
+                                         None) == INVALID                         # P_out partly over P_base
+    assert lib.attnres_block_merge_parts(P, 2 * P, None, 3 * P, E, 2, 3 * P, P, P, f, 4, 16, 1, 5 * P,
+                                         None) == INVALID                         # P_out over the parts
+    binding.attnres_test_fail_launch(0)                                         # valid: reaches the launch
+    assert lib.attnres_block_merge_parts(P, 2 * P, 4 * P, 3 * P, E, 2, 4 * P, P, P, f, 4, 16, 1, 5 * P,
+                                         None) == 3
+    binding.attnres_test_fail_launch(0)
+    assert lib.attnres_block_summary_parts(None, 3 * P, E, 3, None, 5 * P, 4, 16, 1, None) == 3
+    binding.attnres_test_fail_launch(-1)
+    assert lib.attnres_block_summary_parts(None, 3 * P, E, 0, None, 5 * P, 4, 16, 1, None) == INVALID
+    assert lib.attnres_block_summary_parts(None, 3 * P, E, 2, None, None, 4, 16, 1, None) == INVALID
