@@ -7,31 +7,35 @@
 // 2.3 / 2.5).
 //
 // A tile is the n source rows of TM consecutive tokens (P = TM * n <= 16
-// (source, token) pairs). Three roles work on different tiles at once and hand
-// over through shared memory guarded by mbarriers, with no CTA-wide barrier in
-// the steady state:
+// (source, token) pairs); TM is the largest that leaves four tile buffers in
+// shared memory (up to eight are kept). Three roles work on different tiles at
+// once and hand over through shared memory guarded by mbarriers, with no
+// CTA-wide barrier in the steady state:
 //   producer warp: one TMA tensor copy per tile (box {64 features, n sources,
-//     TM rows, d / 64 chunks} of the [n, T, d] sources), up to six tiles in
-//     flight. The tile lands as 128-byte lines ordered (chunk, row, source)
-//     with the 128-byte swizzle, so the 8 pairs an ldmatrix reads at one
-//     feature offset sit in 8 different bank groups;
-//   4 score warps, tile t+1: the scores are a small dense contraction with the
-//     pairs as the rows of A (16 x d) and w * gamma as B (d x 8 queries, split
-//     into bf16 hi + lo so the product keeps about 16 mantissa bits), run as
+//     TM rows, d / 64 chunks} of the [n, T, d] sources). The tile lands as
+//     128-byte lines ordered (chunk, row, source) with the 128-byte swizzle,
+//     so the 8 pairs an ldmatrix reads at one feature offset sit in 8
+//     different bank groups;
+//   4 score warps: the scores are a small dense contraction with the pairs as
+//     the rows of A (16 x d) and w * gamma as B (d x 8 queries, split into
+//     bf16 hi + lo so the product keeps about 16 mantissa bits), run as
 //     m16n8k16 MMAs with fp32 accumulation; the sums of squares come from the
-//     same A fragments as the diagonal of A A^T (with at most 8 pairs the
-//     roles swap: w * gamma hi and lo rows are A, the pairs the 8 columns of B,
-//     halving the MMAs). The warps split d by 64-feature
+//     same A fragments as the diagonal of A A^T. A round fills the 16 MMA rows:
+//     one tile when P > 8, two consecutive tiles when P <= 8 (w * gamma is then
+//     loaded once per k-step for both). The warps split d by 64-feature
 //     chunks; their partials meet in shared memory, then a group of lanes per
 //     (row, query) takes the softmax over depth with shuffles and writes the
 //     weights (double-buffered) and lse;
-//   8 output warps, tile t: the S weighted sums of every row. With many
+//   8 output warps, tile by tile: the S weighted sums of every row. With many
 //     sources and queries (S * n > 32) they run on the tensor cores: per row,
 //     D[16 features x 8 queries] = V^T W, A = V^T taken from the tile with
 //     ldmatrix.trans and K holding the 8 sources twice against the weights'
-//     bf16 hi and lo parts, D transposed into a small staging area with
-//     stmatrix.trans and written with 16-byte stores. With few of them the
-//     CUDA cores are cheaper: 8 features per thread, packed fp32x2 FMAs.
+//     bf16 hi and lo parts, D transposed two chunks at a time into a small
+//     staging area (one row per query) with stmatrix.trans and written with
+//     16-byte stores. With few of them the CUDA cores are cheaper: 8 features
+//     per thread, packed fp32x2 FMAs.
+// Only the S queries' rows of w * gamma and of the staging are kept, so that
+// wide rows (d = 2048) still leave room for four or more tile buffers.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -83,8 +87,8 @@ inline TcGeom tc_geom_for(int n, int d, int S, int TM) {
   g.pitch = d * 2 + 16;
   g.srows = S < kQ ? S + 1 : kQ;
   g.w_off = kBarBytes;                                  // bf16 hi rows [S], then lo rows [S]
-  g.red_off = g.w_off + 2 * S * g.pitch;                // fp32 [npair][S + 1][kSW] partials
-  g.al_off = g.red_off + kSW * g.npair * (S + 1) * 4;   // float2 [2][npair][S2] weights as (a, a)
+  g.red_off = g.w_off + 2 * S * g.pitch;                // fp32 [16][S + 1][kSW] partials
+  g.al_off = g.red_off + kSW * kMaxPairs * (S + 1) * 4;  // float2 [2][npair][S2] weights as (a, a)
   g.bt_off = g.al_off + 2 * g.npair * round_up(S, 2) * 8;  // bf16 MMA weight fragments [2][kBtBytes]
   g.stg_off = g.bt_off + 2 * kBtBytes;                  // bf16 [kOW][srows][kStgPitch] output staging
   g.buf_off = round_up(g.stg_off + kOW * g.srows * kStgPitch, 1024);
@@ -126,7 +130,10 @@ __device__ __forceinline__ uint32_t line_base(uint32_t tile, int L) {
   return tile + static_cast<uint32_t>(L) * 128u + static_cast<uint32_t>((L & 7) << 4);
 }
 
-template <int S, bool kTC>
+// kKT: tiles per score round (2 when a tile has at most 8 pairs, else 1), a
+// template parameter so the one-tile instances carry none of the two-tile
+// bookkeeping.
+template <int S, bool kTC, int kKT>
 __global__ void __launch_bounds__(kThreads, 1)
     stage1_tc_kernel(MultiArgs a, TcGeom g, const __grid_constant__ CUtensorMap tmap) {
   constexpr int S2 = (S + 1) / 2 * 2;  // CUDA-core path: weights as (a, a) pairs, S2 per (token, source)
@@ -138,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* aempty = afull + 2;                             // [2] weights consumed
   volatile int* abort_flag = reinterpret_cast<volatile int*>(aempty + 2);
   unsigned char* wsm = smem + g.w_off;
-  float* red = reinterpret_cast<float*>(smem + g.red_off);  // [npair][SC][kSW] partials
+  float* red = reinterpret_cast<float*>(smem + g.red_off);  // [16][SC][kSW] partials
   float2* alpha = reinterpret_cast<float2*>(smem + g.al_off);
   unsigned char* btab = smem + g.bt_off;  // [2][TM][ceil(n/8)][8 queries][4] uint2 {hi pair, lo pair}
   unsigned char* bufs = smem + g.buf_off;
@@ -162,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&empty_bar[b]), kSW + kOW);
     }
     for (int k = 0; k < 2; ++k) {
-      mbar_init(smem_u32(&afull[k]), kScoreThreads);
+      mbar_init(smem_u32(&afull[k]), kSW);
       mbar_init(smem_u32(&aempty[k]), kOW);
     }
     *reinterpret_cast<int*>(aempty + 2) = 0;
@@ -253,135 +260,147 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kSW) {
     // ------------------------------------------------------------- scores
+    // The scores of a round are one m16 MMA tile: with P > 8 pairs a tile
+    // fills it alone; with P <= 8 two consecutive tiles share it (rows 0-7
+    // the first tile's pairs, rows 8-15 the second's), so w * gamma is loaded
+    // once per k-step for both and the MMA chains are twice as productive.
     const float inv_d = 1.0f / static_cast<float>(d);
     const int cb = warp * nchunk / kSW, ce = (warp + 1) * nchunk / kSW;  // this warp's chunks
+    constexpr int KT = kKT;          // tiles per round
+    const int RP = KT == 2 ? 8 : P;  // MMA rows per tile
     const int a_row = (lane & 7) + ((lane >> 3) & 1) * 8;
     const int a_koff = (lane >> 4) * 8;
+    const int a_tile = a_row / RP;                             // which tile of the round this row reads
+    const int a_pair = a_row - a_tile * RP;
     // Hi rows, then lo rows. Lanes of queries >= S read query 0's rows: what
-    // they feed lands only in the MMA rows or columns of queries >= S, which
-    // are never read.
+    // they feed lands only in the MMA columns of queries >= S, never read.
     const int b_row = ((lane & 7) < S ? (lane & 7) : 0) + ((lane >> 4) & 1) * S;
     const int b_koff = ((lane >> 3) & 1) * 8;
     const uint32_t b_base = smem_u32(wsm + b_row * g.pitch) + (cb * 64 + b_koff) * 2;
     const uint32_t a_x = static_cast<uint32_t>(a_koff) * 2u;  // this lane's 16-byte unit within a k-step
-    const int m = a_row < P ? a_row : 0;                      // rows past P only pad the m16 tile
     const int gid = lane >> 2, tig = lane & 3;
     // Softmax: a group of G lanes (n rounded up to a power of two) per (token, query).
     int lgG = 0;
     while ((1 << lgG) < n) ++lgG;
     const int G = 1 << lgG;
-    const int sm_items = TM * S * G;
     const int nk = (n + 7) >> 3;
-    int b = 0;
+    const int TMS = TM * S;
+    const int64_t ntile = t1 - t0;
+    int b = 0;            // buffer of tile it, and the parity of its current use
     uint32_t phase = 0;
-    int it = 0;
-    for (int64_t tile = t0; tile < t1; ++tile, ++it) {
-      const int ab = it & 1;
-      const uint32_t aph = static_cast<uint32_t>((it >> 1) & 1);
-      // The tile must have landed and weights buffer ab must be free. The
-      // score warps meet at a named barrier, so giving up is decided jointly.
-      if (!mbar_wait(smem_u32(&full_bar[b]), phase) || !mbar_wait(smem_u32(&aempty[ab]), aph ^ 1u))
-        *abort_flag = 1;
+    for (int64_t it = 0; it < ntile; it += KT) {
+      // Tiles this round (the last round of a CTA may hold one).
+      const int kt = KT == 1 ? 1 : static_cast<int>(min(static_cast<int64_t>(KT), ntile - it));
+      // Buffers of the round's tiles: b, and the one after it.
+      const int bk0 = b;
+      const uint32_t ph0 = phase;
+      int bk1 = b + 1;
+      uint32_t ph1 = phase;
+      if (bk1 == nbuf) {
+        bk1 = 0;
+        ph1 ^= 1u;
+      }
+      bool got = mbar_wait(smem_u32(&full_bar[bk0]), ph0);
+      if (kt == 2) got = got && mbar_wait(smem_u32(&full_bar[bk1]), ph1);
+      // A one-tile round also waits here for its weight buffer (measured
+      // faster than waiting after the MMAs); a two-tile round waits after
+      // them, so its MMAs overlap the output warps' last tile.
+      if (KT == 1) got = got && mbar_wait(smem_u32(&aempty[it & 1]), static_cast<uint32_t>(((it >> 1) & 1) ^ 1));
+      b = kt == 2 ? bk1 : bk0;
+      phase = kt == 2 ? ph1 : ph0;
+      if (++b == nbuf) {
+        b = 0;
+        phase ^= 1u;
+      }
+      // The score warps meet at a named barrier, so giving up is decided jointly.
+      if (!got) *abort_flag = 1;
       named_sync(1, kScoreThreads);
       if (*abort_flag) {
         ok = false;
         break;
       }
-      const uint32_t bb = smem_u32(bufs + b * g.buf_bytes);
-      const int64_t row0 = tile * TM;
-      const int rows = static_cast<int>(min(static_cast<int64_t>(TM), ntok - row0));
+      // The line this lane reads for MMA row a_row; rows past the round's
+      // pairs only pad the m16 tile and read the first pair.
+      const bool a_live = a_pair < P && a_tile < kt;
+      const uint32_t a_buf = smem_u32(bufs + (a_live && a_tile == 1 ? bk1 : bk0) * g.buf_bytes);
+      const int a_p = a_live ? a_pair : 0;
       {
+        float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-        // Per chunk: the line of pair m, then its four k-steps (one XOR each).
-        // All fragments of a chunk are loaded before its MMAs, since the asm
-        // statements issue in program order.
-        if (P <= 8) {
-          // Up to 8 pairs: w * gamma is A (rows: the hi parts of the 8 queries,
-          // then their lo parts) and the pairs are the 8 columns of B = V^T,
-          // so one MMA gives hi and lo dots; one more gives the A A^T block
-          // with the sums of squares.
-          float sw[4] = {0.f, 0.f, 0.f, 0.f};
-          for (int c = cb; c < ce; ++c) {
-            const uint32_t off = line_base(bb, c * P + m) ^ a_x;
-            const uint32_t bo = b_base + static_cast<uint32_t>(c - cb) * 128u;
-            uint32_t av[4][4], bv[4][4];
+        // Per chunk: the line of this lane's pair, then its four k-steps (one
+        // XOR each). All fragments of a chunk are loaded before its MMAs,
+        // since the asm statements issue in program order.
+        for (int c = cb; c < ce; ++c) {
+          const uint32_t off = line_base(a_buf, c * P + a_p) ^ a_x;
+          const uint32_t bo = b_base + static_cast<uint32_t>(c - cb) * 128u;
+          uint32_t av[4][4], bv[4][4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              ldsm_x4(off ^ (32u * u), av[u]);
-              ldsm_x4(bo + 32u * u, bv[u]);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint32_t wa[4] = {bv[u][0], bv[u][2], bv[u][1], bv[u][3]};
-              mma16816(sw, wa, av[u][0], av[u][2]);     // [hi; lo] dots x 8 pairs
-              mma16816(s0, av[u], av[u][0], av[u][2]);  // A A^T, columns 0..7
-            }
+          for (int u = 0; u < 4; ++u) {
+            ldsm_x4(off ^ (32u * u), av[u]);
+            ldsm_x4(bo + 32u * u, bv[u]);
           }
-          // This warp is done with the tile's rows.
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&empty_bar[b]));
-          // Lane (gid, tig) holds the dots of query gid with pairs 2 tig, 2 tig + 1.
-          if (gid < S) {
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int pp = 2 * tig + e;
-              if (pp < P) red[(pp * SC + 1 + gid) * kSW + warp] = sw[e] + sw[2 + e];
-            }
+          for (int u = 0; u < 4; ++u) {
+            mma16816(sh, av[u], bv[u][0], bv[u][1]);  // hi part of w * gamma
+            mma16816(sl, av[u], bv[u][2], bv[u][3]);  // lo part
+            mma16816(s0, av[u], av[u][0], av[u][2]);  // A A^T, columns 0..7
+            mma16816(s1, av[u], av[u][1], av[u][3]);  // A A^T, columns 8..15
           }
-        } else {
-          float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
-          for (int c = cb; c < ce; ++c) {
-            const uint32_t off = line_base(bb, c * P + m) ^ a_x;
-            const uint32_t bo = b_base + static_cast<uint32_t>(c - cb) * 128u;
-            uint32_t av[4][4], bv[4][4];
+        }
+        // This warp is done with the round's tiles.
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&empty_bar[bk0]));
+          if (kt == 2) mbar_arrive(smem_u32(&empty_bar[bk1]));
+        }
+        // Lane (gid, tig) holds the dots of MMA rows gid, gid + 8 with
+        // queries 2 tig, 2 tig + 1; row x of the MMA is row x of red[].
+        const bool lo_live = gid < P;
+        const bool hi_live = KT == 2 ? (gid < P && kt == 2) : gid + 8 < P;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              ldsm_x4(off ^ (32u * u), av[u]);
-              ldsm_x4(bo + 32u * u, bv[u]);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              mma16816(sh, av[u], bv[u][0], bv[u][1]);  // hi part of w * gamma
-              mma16816(sl, av[u], bv[u][2], bv[u][3]);  // lo part
-              mma16816(s0, av[u], av[u][0], av[u][2]);  // A A^T, columns 0..7
-              mma16816(s1, av[u], av[u][1], av[u][3]);  // A A^T, columns 8..15
-            }
-          }
-          // This warp is done with the tile's rows.
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&empty_bar[b]));
-          // Lane (gid, tig) holds the dots of pairs gid, gid + 8 with queries 2 tig, 2 tig + 1.
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int q = 2 * tig + e;
-            if (q < S) {
-              if (gid < P) red[(gid * SC + 1 + q) * kSW + warp] = sh[e] + sl[e];
-              if (gid + 8 < P) red[((gid + 8) * SC + 1 + q) * kSW + warp] = sh[2 + e] + sl[2 + e];
-            }
+        for (int e = 0; e < 2; ++e) {
+          const int q = 2 * tig + e;
+          if (q < S) {
+            if (lo_live) red[(gid * SC + 1 + q) * kSW + warp] = sh[e] + sl[e];
+            if (hi_live) red[((gid + 8) * SC + 1 + q) * kSW + warp] = sh[2 + e] + sl[2 + e];
           }
         }
         // Diagonal of A A^T: row gid in s0[gid & 1], row gid + 8 in s1[2 + (gid & 1)],
         // held by the lane whose 2 tig + e equals gid (selects keep registers).
         if (tig == (gid >> 1)) {
           const bool odd = gid & 1;
-          if (gid < P) red[(gid * SC) * kSW + warp] = odd ? s0[1] : s0[0];
-          if (gid + 8 < P) red[((gid + 8) * SC) * kSW + warp] = odd ? s1[3] : s1[2];
+          if (lo_live) red[(gid * SC) * kSW + warp] = odd ? s0[1] : s0[0];
+          if (hi_live) red[((gid + 8) * SC) * kSW + warp] = odd ? s1[3] : s1[2];
         }
       }
+      // The weight buffers of the round's tiles (tile it + k uses buffer
+      // (it + k) & 1) must be free before the softmax writes them.
+      if (KT == 2) {
+        bool free_ok = true;
+        for (int k = 0; k < kt; ++k)
+          free_ok = free_ok && mbar_wait(smem_u32(&aempty[(it + k) & 1]), static_cast<uint32_t>((((it + k) >> 1) & 1) ^ 1));
+        if (!free_ok) *abort_flag = 1;
+      }
       named_sync(1, kScoreThreads);
+      if (*abort_flag) {
+        ok = false;
+        break;
+      }
       // Softmax over depth, one lane per source: max and mass by shuffles
       // within the group.
-      float2* al = alpha + ab * g.npair * S2;
-      unsigned char* bt = btab + ab * kBtBytes;
+      const int sm_items = kt * TMS * G;
       for (int base = 0; base < sm_items; base += kScoreThreads) {
         const int item = base + tid;
         const int i = item & (G - 1);
-        const int rj = item >> lgG;
+        const int krj = item >> lgG;          // (tile of the round, token, query)
+        const int k = KT == 2 && krj >= TMS ? 1 : 0;  // a round has at most two tiles
+        const int rj = krj - k * TMS;
         const int r = rj / S, j = rj - (rj / S) * S;
+        const int64_t row0 = (t0 + it + k) * TM;
         const bool valid = item < sm_items && i < n;
         float e = -INFINITY;
         if (valid) {
-          const int p = r * n + i;
+          const int p = k * RP + r * n + i;   // row of red[]
           // The four warps' partials of pair p sit side by side.
           const float4 sq = *reinterpret_cast<const float4*>(red + (p * SC) * kSW);
           const float4 dt = *reinterpret_cast<const float4*>(red + (p * SC + 1 + j) * kSW);
@@ -395,29 +414,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         float z = x;
         for (int off = 1; off < G; off <<= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
         if (valid) {
+          const int ab = static_cast<int>((it + k) & 1);
           const float wgt = x * (1.0f / z);
           if constexpr (kTC) {
             // B fragment of the output MMA for token r, source block i / 8 and
             // query j: {hi(a[2t]), hi(a[2t+1])}, {lo(a[2t]), lo(a[2t+1])}, t = (i % 8) / 2.
+            unsigned char* bt = btab + ab * kBtBytes;
             const bf16 hi = __float2bfloat16_rn(wgt);
             const bf16 lo = __float2bfloat16_rn(wgt - __bfloat162float(hi));
             bf16* ep = reinterpret_cast<bf16*>(bt + (((r * nk + (i >> 3)) * 8 + j) * 4 + ((i & 7) >> 1)) * 8);
             ep[i & 1] = hi;
             ep[2 + (i & 1)] = lo;
           } else {
+            float2* al = alpha + ab * g.npair * S2;
             al[(r * n + i) * S2 + j] = make_float2(wgt, wgt);
           }
-          if (i == 0 && a.lse && r < rows) a.lse[j * ntok + row0 + r] = mx + __logf(z);
+          if (i == 0 && a.lse && row0 + r < ntok) a.lse[j * ntok + row0 + r] = mx + __logf(z);
         }
       }
-      // Weights of this tile are ready (each score thread arrives). red[] is
-      // rewritten by the next tile only after every score thread has passed
-      // the named barrier at its top.
-      mbar_arrive(smem_u32(&afull[ab]));
-      if (++b == nbuf) {
-        b = 0;
-        phase ^= 1u;
-      }
+      // Weights of the round's tiles are ready: each score warp arrives once
+      // its lanes have written theirs (the warp barrier orders the lanes'
+      // stores before lane 0's release). red[] is rewritten by the next round
+      // only after every score thread has passed the named barrier at its top.
+      __syncwarp();
+      if (lane == 0)
+        for (int k = 0; k < kt; ++k) mbar_arrive(smem_u32(&afull[(it + k) & 1]));
     }
   } else {
     // ------------------------------------------------------------- outputs
@@ -607,9 +628,9 @@ bool encode_tile_map(const MultiArgs& a, const TcGeom& g, CUtensorMap* map) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int S, bool kTC>
+template <int S, bool kTC, int kKT>
 cudaError_t launch_s(const MultiArgs& a, const TcGeom& g, cudaStream_t s) {
-  auto k = stage1_tc_kernel<S, kTC>;
+  auto k = stage1_tc_kernel<S, kTC, kKT>;
   cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(k), g.total);
   if (e != cudaSuccess) return e;
   alignas(64) CUtensorMap map;
@@ -620,9 +641,14 @@ cudaError_t launch_s(const MultiArgs& a, const TcGeom& g, cudaStream_t s) {
   return launch_pdl(k, static_cast<unsigned>(grid), kThreads, g.total, s, a, g, map);
 }
 
+template <int S, bool kTC>
+cudaError_t launch_kt(const MultiArgs& a, const TcGeom& g, cudaStream_t s) {
+  return g.P <= 8 ? launch_s<S, kTC, 2>(a, g, s) : launch_s<S, kTC, 1>(a, g, s);
+}
+
 template <int S>
 cudaError_t launch_q(const MultiArgs& a, const TcGeom& g, cudaStream_t s) {
-  return outputs_on_tensor_cores(a.n_src, S) ? launch_s<S, true>(a, g, s) : launch_s<S, false>(a, g, s);
+  return outputs_on_tensor_cores(a.n_src, S) ? launch_kt<S, true>(a, g, s) : launch_kt<S, false>(a, g, s);
 }
 
 }  // namespace
