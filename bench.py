@@ -226,8 +226,6 @@ def measured_peaks() -> dict:
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) over algorithmic
 # bytes, from one ncu capture of the kernel, keyed by the sha256 prefix of the
 # kernel source it was taken with: reported as null once the source changes.
-# full_fwd_bulk_kernel: the 21-source read (sublayer 20) of the 8192 x 896 pass,
-# 308.31 MB read + 11.15 MB written for 322.96 MB algorithmic.
 # full_bwd_bulk_kernel: the 44-source read (read 43) of the 8192 x 896 pass
 # backward, 2445.16 MB read + 1231.98 MB written for 3244.29 MB algorithmic
 # (the second pass over a tile's sources re-reads part of them from DRAM).
@@ -236,10 +234,30 @@ def measured_peaks() -> dict:
 # algorithmic (reads equal the algorithmic reads; the rest of the writes were
 # still in L2 when ncu flushed it between launches). The per-launch traffic
 # grows with the tokens.
-NCU_TRAFFIC = {("full_fwd_bulk_kernel", "7cc92f36c701ba29"): (308.313344 + 11.152128) / 322.961408,
+# full_fwd_bulk_kernel (source 664fdb90f174cfdb): all 64 launches of the 8192 x
+# 896 pass without ncu's cache flush between launches, 30289.2 MB read +
+# 1033.1 MB written for 31474.1 MB algorithmic.
+NCU_TRAFFIC = {("full_fwd_bulk_kernel", "664fdb90f174cfdb"): (30289.201664 + 1033.079552) / 31474.057216,
                ("full_bwd_bulk_kernel", "1d4588bb0e4b35ec"): (2445.157632 + 1231.980032) / 3244.294144,
                ("block_bwd_batched_kernel", "cb4b0fb7ff058c27"): (1554.098176 + 420.645888) / 2483.027968}
 
+
+# Block-pass kernels: DRAM bytes / algorithmic bytes over all launches of one
+# kind in one pass, captured without ncu's cache flush between launches
+# (steady-state write-backs counted), keyed by (kernel, source digest) and then
+# by workload. The 128K prefill's ratios come from the same blocks at 8192
+# tokens (profiles/block_pass_kernels_8x6x131072x2048_bf16.md).
+NCU_TRAFFIC_BLOCK = {
+    ("stage1_tc_kernel", "fd8dacdfa1f3443d"): {
+        "block_pass_8x6x131072x2048_bf16": (1145.2 + 1356.4) / 2820.1,
+        "block_pass_8x8x16384x1024_bf16": (1144.1 + 1864.6) / 3359.6},
+    ("merge_tile_kernel", "11ad511f1735a33e"): {
+        "block_pass_8x6x131072x2048_bf16": (4563.6 + 2108.6) / 6712.2,
+        "block_pass_8x8x16384x1024_bf16": (6762.6 + 3170.9) / 10204.2},
+    ("accum_fast_kernel", "11ad511f1735a33e"): {
+        "block_pass_8x6x131072x2048_bf16": (838.7 + 272.1) / 1174.4,
+        "block_pass_8x8x16384x1024_bf16": (840.0 + 288.6) / 1174.4},
+}
 
 KERNEL_FILES = {"full_fwd_bulk_kernel": "full_fwd.cu", "full_bwd_bulk_kernel": "full_bwd.cu",
                 "block_bwd_batched_kernel": "block_bwd.cu", "stage1_tc_kernel": "stage1_tc.cu",
@@ -606,7 +624,7 @@ def block_roofline(step, ms_step, stream, peaks, reps=3):
     top = max(kernels, key=lambda k: kernels[k]["ms"])
     g = kernels[top]["gbs"]
     name = {"stage1": "stage1_tc_kernel", "merge": "merge_tile_kernel", "freeze": "accum_fast_kernel"}[top]
-    ratio = NCU_TRAFFIC.get((name, kernel_digest(KERNEL_FILES[name])))
+    ratio = NCU_TRAFFIC_BLOCK.get((name, kernel_digest(KERNEL_FILES[name])), {}).get(step.wl.name)
     per_launch = parts[top] / kernels[top]["launches"]
     return {"kernel": name, "bound": "hbm", "achieved": g, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": g / peaks["hbm_gbs"], "frac_of_nominal_8000": g / NOMINAL_HBM_GBS,
