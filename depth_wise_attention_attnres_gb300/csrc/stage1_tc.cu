@@ -463,6 +463,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // contents are never copied out.
       const uint32_t st_base = smem_u32(stg) + (l8 < S ? l8 : g.srows - 1) * kStgPitch + lhalf * 16;
       const uint32_t lx = static_cast<uint32_t>(lhalf) << 4;
+      // Copy-out of two chunks (S rows of 16 16-byte pieces): lane l takes
+      // pieces l, l + 32, ..., i.e. piece l % 16 of rows l / 16, l / 16 + 2, ...
+      // Their output rows and staging offsets are fixed per lane, so they are
+      // formed once here rather than per piece.
+      constexpr int kPieces = (S * 16 + kWarp - 1) / kWarp;
+      bf16* obase[kPieces];
+      uint32_t soff[kPieces];
+#pragma unroll
+      for (int k = 0; k < kPieces; ++k) {
+        const int q = (lane >> 4) + 2 * k;
+        const int ch = lane & 15;
+        obase[k] = q < S ? static_cast<bf16*>(a.out[q]) + f_beg + ch * 8 : nullptr;
+        soff[k] = static_cast<uint32_t>(q * kStgPitch + ch * 16);
+      }
       for (int64_t tile = t0; tile < t1; ++tile, ++it) {
         const int ab = it & 1;
         const uint32_t aph = static_cast<uint32_t>((it >> 1) & 1);
@@ -521,12 +535,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 stsm_x2_trans(st_base + static_cast<uint32_t>(u * 32), pack_bf16x2(acc[u][0], acc[u][1]),
                               pack_bf16x2(acc[u][2], acc[u][3]));
             __syncwarp();
-            const int pq = two ? 16 : 8;  // 16-byte pieces per query row
-            for (int idx = lane; idx < S * pq; idx += kWarp) {
-              const int q = two ? idx >> 4 : idx >> 3;
-              const int ch = idx - q * pq;
-              const uint4 v = *reinterpret_cast<const uint4*>(stg + q * kStgPitch + ch * 16);
-              *reinterpret_cast<uint4*>(static_cast<bf16*>(a.out[q]) + row * d + f_beg + c * 64 + ch * 8) = v;
+            if (two) {
+              const int64_t ro = row * d + c * 64;
+#pragma unroll
+              for (int k = 0; k < kPieces; ++k) {
+                if ((lane >> 4) + 2 * k < S) {
+                  const uint4 v = *reinterpret_cast<const uint4*>(stg + soff[k]);
+                  *reinterpret_cast<uint4*>(obase[k] + ro) = v;
+                }
+              }
+            } else {
+              // The warp's last chunk alone: 8 pieces per row.
+              for (int idx = lane; idx < S * 8; idx += kWarp) {
+                const int q = idx >> 3;
+                const int ch = idx - q * 8;
+                const uint4 v = *reinterpret_cast<const uint4*>(stg + q * kStgPitch + ch * 16);
+                *reinterpret_cast<uint4*>(static_cast<bf16*>(a.out[q]) + row * d + f_beg + c * 64 + ch * 8) = v;
+              }
             }
           }
         }
