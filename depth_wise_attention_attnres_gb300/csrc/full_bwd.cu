@@ -38,9 +38,13 @@ constexpr int kBBar = 128;
 constexpr int kBMaxStages = 8;
 constexpr int kBSmemPerSM = 224 * 1024;
 
+// One CTA per SM: with two, the tiles of all CTAs together (8 rows of every
+// source each) outgrew the L2 sooner, and more of pass B's reads went to DRAM
+// (measured: 64-read 8192 x 896 pass backward 26.97 ms with two CTAs per SM,
+// 26.72 ms with one; 4-row tiles were slower at two or four CTAs per SM).
 template <int CH>
 struct BwdTraits {
-  static constexpr int kMinBlocks = CH <= 8 ? 2 : 1;
+  static constexpr int kMinBlocks = 1;
 };
 
 struct BwdGeom {
@@ -66,9 +70,35 @@ BwdGeom bwd_geom(int n) {
   return g;
 }
 
-__device__ __forceinline__ void red_add4(float* p, const float (&x)[4]) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(x[0]), "f"(x[1]), "f"(x[2]),
-               "f"(x[3])
+// L2 eviction priorities for the two passes over a tile's sources: pass A
+// marks the rows it brings in to be kept (pass B reads them again soon), pass
+// B and the dV reductions mark theirs to go first. Without them the dV
+// read-modify-write stream pushed part of the sources out of the L2 between
+// the passes, and pass B re-read them from DRAM.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 1-D bulk copy global -> shared with an L2 eviction priority.
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void red_add4(float* p, const float (&x)[4], uint64_t policy) {
+  asm volatile("red.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(x[0]), "f"(x[1]),
+               "f"(x[2]), "f"(x[3]), "l"(policy)
                : "memory");
 }
 
@@ -123,6 +153,7 @@ __global__ void __launch_bounds__(kBThreads, BwdTraits<CH>::kMinBlocks)
     // ------------------------------------------------------------ producer
     if (lane != 0) return;
     const char* V = static_cast<const char*>(a.V);
+    const uint64_t keep = policy_evict_last(), drop = policy_evict_first();
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
@@ -142,8 +173,9 @@ __global__ void __launch_bounds__(kBThreads, BwdTraits<CH>::kMinBlocks)
       const uint32_t bytes = static_cast<uint32_t>(rows) * D * sizeof(Tin);
       const uint32_t fb = smem_u32(&full_bar[stage]);
       mbar_arrive_expect_tx(fb, bytes);
-      bulk_g2s(smem_u32(stages + static_cast<size_t>(stage) * kStageElems),
-               V + (static_cast<int64_t>(src) * a.src_stride + row0 * D) * sizeof(Tin), bytes, fb);
+      bulk_g2s_hint(smem_u32(stages + static_cast<size_t>(stage) * kStageElems),
+                    V + (static_cast<int64_t>(src) * a.src_stride + row0 * D) * sizeof(Tin), bytes, fb,
+                    j < n ? keep : drop);
       ++issued;
       if (++stage == nstage) {
         stage = 0;
@@ -166,6 +198,7 @@ __global__ void __launch_bounds__(kBThreads, BwdTraits<CH>::kMinBlocks)
   }
   named_sync(1, kBNW * kWarp);
   const float inv_d = 1.0f / static_cast<float>(D);
+  const uint64_t dv_policy = policy_evict_first();
   float* grow = gsm + warp * D;
   float* sc = scs + warp * n * 3;
   float2 du[NE / 2];
@@ -289,7 +322,7 @@ __global__ void __launch_bounds__(kBThreads, BwdTraits<CH>::kMinBlocks)
           va = ffma2(C2, xa, va);
           vb = ffma2(C2, xb, vb);
           const float dv[4] = {va.x, va.y, vb.x, vb.y};
-          red_add4(dvrow + k, dv);
+          red_add4(dvrow + k, dv, dv_policy);
           du[c * 2] = ffma2(B2, xa, du[c * 2]);
           du[c * 2 + 1] = ffma2(B2, xb, du[c * 2 + 1]);
         }
