@@ -60,9 +60,15 @@ constexpr int kMaxBuf = 8;                          // tile buffers
 constexpr int kBarBytes = 256;
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kBtBytes = 16 * 256;                  // MMA weight fragments of a tile: TM * ceil(n / 8) <= 16 blocks
+// Weight buffers between the score and output warps: tile it uses buffer
+// it % slots. Two suffice for one-tile score rounds; two-tile rounds (P <= 8)
+// get four, so the score warps can fill the next round's while the output
+// warps still read the last round's.
+constexpr int kWSlots = 4;  // the most
+inline int weight_slots(int P) { return P <= 8 ? 4 : 2; }
 constexpr int kStgPitch = 2 * 128 + 16;             // output staging row: two 64-feature chunks, padded
-// full + empty per buffer, two weight handovers each way, then the abort flag
-static_assert((2 * kMaxBuf + 4) * 8 + 4 <= kBarBytes, "barrier area too small");
+// full + empty per buffer, the weight handovers each way, then the abort flag
+static_assert((2 * kMaxBuf + 2 * kWSlots) * 8 + 4 <= kBarBytes, "barrier area too small");
 
 struct TcGeom {
   int npair;       // pairs a tile holds (TM * n <= 16)
@@ -88,9 +94,10 @@ inline TcGeom tc_geom_for(int n, int d, int S, int TM) {
   g.srows = S < kQ ? S + 1 : kQ;
   g.w_off = kBarBytes;                                  // bf16 hi rows [S], then lo rows [S]
   g.red_off = g.w_off + 2 * S * g.pitch;                // fp32 [16][S + 1][kSW] partials
-  g.al_off = g.red_off + kSW * kMaxPairs * (S + 1) * 4;  // float2 [2][npair][S2] weights as (a, a)
-  g.bt_off = g.al_off + 2 * g.npair * round_up(S, 2) * 8;  // bf16 MMA weight fragments [2][kBtBytes]
-  g.stg_off = g.bt_off + 2 * kBtBytes;                  // bf16 [kOW][srows][kStgPitch] output staging
+  const int ws = weight_slots(g.P);
+  g.al_off = g.red_off + kSW * kMaxPairs * (S + 1) * 4;  // float2 [ws][npair][S2] weights as (a, a)
+  g.bt_off = g.al_off + ws * g.npair * round_up(S, 2) * 8;  // bf16 MMA weight fragments [ws][kBtBytes]
+  g.stg_off = g.bt_off + ws * kBtBytes;                 // bf16 [kOW][srows][kStgPitch] output staging
   g.buf_off = round_up(g.stg_off + kOW * g.srows * kStgPitch, 1024);
   g.buf_bytes = g.npair * d * 2;
   g.nbuf = (kSmemLimit - 1024 - g.buf_off) / g.buf_bytes;  // 1 KB slack to align the base
@@ -137,17 +144,18 @@ template <int S, bool kTC, int kKT>
 __global__ void __launch_bounds__(kThreads, 1)
     stage1_tc_kernel(MultiArgs a, TcGeom g, const __grid_constant__ CUtensorMap tmap) {
   constexpr int S2 = (S + 1) / 2 * 2;  // CUDA-core path: weights as (a, a) pairs, S2 per (token, source)
+  constexpr int WS = kKT == 2 ? 4 : 2;  // weight buffers (weight_slots of the launch's P)
   constexpr int SC = S + 1;            // partial columns per pair: sum of squares, then the S dots
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem);  // [kMaxBuf] tile landed
   uint64_t* empty_bar = full_bar + kMaxBuf;                 // [kMaxBuf] tile consumed
-  uint64_t* afull = empty_bar + kMaxBuf;                    // [2] weights ready
-  uint64_t* aempty = afull + 2;                             // [2] weights consumed
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(aempty + 2);
+  uint64_t* afull = empty_bar + kMaxBuf;                    // [WS] weights ready
+  uint64_t* aempty = afull + kWSlots;                       // [WS] weights consumed
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(aempty + kWSlots);
   unsigned char* wsm = smem + g.w_off;
   float* red = reinterpret_cast<float*>(smem + g.red_off);  // [16][SC][kSW] partials
   float2* alpha = reinterpret_cast<float2*>(smem + g.al_off);
-  unsigned char* btab = smem + g.bt_off;  // [2][TM][ceil(n/8)][8 queries][4] uint2 {hi pair, lo pair}
+  unsigned char* btab = smem + g.bt_off;  // [kWSlots][TM][ceil(n/8)][8 queries][4] uint2 {hi pair, lo pair}
   unsigned char* bufs = smem + g.buf_off;
   bufs += (1024u - (smem_u32(bufs) & 1023u)) & 1023u;  // the swizzle wants 1 KB alignment
 
@@ -168,11 +176,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&full_bar[b]), 1);
       mbar_init(smem_u32(&empty_bar[b]), kSW + kOW);
     }
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < WS; ++k) {
       mbar_init(smem_u32(&afull[k]), kSW);
       mbar_init(smem_u32(&aempty[k]), kOW);
     }
-    *reinterpret_cast<int*>(aempty + 2) = 0;
+    *reinterpret_cast<int*>(aempty + kWSlots) = 0;
     mbar_fence_init();
   }
   __syncthreads();
@@ -254,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // MMA weight fragments of sources >= n and of queries >= S stay zero.
-    for (int v = tid; v < 2 * kBtBytes / 16; v += kCT) reinterpret_cast<uint4*>(btab)[v] = make_uint4(0u, 0u, 0u, 0u);
+    for (int v = tid; v < WS * kBtBytes / 16; v += kCT) reinterpret_cast<uint4*>(btab)[v] = make_uint4(0u, 0u, 0u, 0u);
     named_sync(2, kCT);
   }
 
@@ -305,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // A one-tile round also waits here for its weight buffer (measured
       // faster than waiting after the MMAs); a two-tile round waits after
       // them, so its MMAs overlap the output warps' last tile.
-      if (KT == 1) got = got && mbar_wait(smem_u32(&aempty[it & 1]), static_cast<uint32_t>(((it >> 1) & 1) ^ 1));
+      if (KT == 1) got = got && mbar_wait(smem_u32(&aempty[it % WS]), static_cast<uint32_t>(((it / WS) & 1) ^ 1));
       b = kt == 2 ? bk1 : bk0;
       phase = kt == 2 ? ph1 : ph0;
       if (++b == nbuf) {
@@ -374,11 +382,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // The weight buffers of the round's tiles (tile it + k uses buffer
-      // (it + k) & 1) must be free before the softmax writes them.
+      // (it + k) % WS) must be free before the softmax writes them.
       if (KT == 2) {
         bool free_ok = true;
         for (int k = 0; k < kt; ++k)
-          free_ok = free_ok && mbar_wait(smem_u32(&aempty[(it + k) & 1]), static_cast<uint32_t>((((it + k) >> 1) & 1) ^ 1));
+          free_ok = free_ok && mbar_wait(smem_u32(&aempty[(it + k) % WS]),
+                                         static_cast<uint32_t>((((it + k) / WS) & 1) ^ 1));
         if (!free_ok) *abort_flag = 1;
       }
       named_sync(1, kScoreThreads);
@@ -414,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float z = x;
         for (int off = 1; off < G; off <<= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
         if (valid) {
-          const int ab = static_cast<int>((it + k) & 1);
+          const int ab = static_cast<int>((it + k) % WS);
           const float wgt = x * (1.0f / z);
           if constexpr (kTC) {
             // B fragment of the output MMA for token r, source block i / 8 and
@@ -438,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // only after every score thread has passed the named barrier at its top.
       __syncwarp();
       if (lane == 0)
-        for (int k = 0; k < kt; ++k) mbar_arrive(smem_u32(&afull[(it + k) & 1]));
+        for (int k = 0; k < kt; ++k) mbar_arrive(smem_u32(&afull[(it + k) % WS]));
     }
   } else {
     // ------------------------------------------------------------- outputs
@@ -478,8 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         soff[k] = static_cast<uint32_t>(q * kStgPitch + ch * 16);
       }
       for (int64_t tile = t0; tile < t1; ++tile, ++it) {
-        const int ab = it & 1;
-        const uint32_t aph = static_cast<uint32_t>((it >> 1) & 1);
+        const int ab = it % WS;
+        const uint32_t aph = static_cast<uint32_t>((it / WS) & 1);
         // Weights ready; waiting on the tile's own barrier as well makes the
         // copied rows visible to this warp.
         const bool got = mbar_wait(smem_u32(&afull[ab]), aph) && mbar_wait(smem_u32(&full_bar[b]), phase);
@@ -577,8 +586,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t kx = static_cast<uint32_t>((k >> 3) & 7) << 4;
       const int kc = k >> 6;
       for (int64_t tile = t0; tile < t1; ++tile, ++it) {
-        const int ab = it & 1;
-        const uint32_t aph = static_cast<uint32_t>((it >> 1) & 1);
+        const int ab = it % WS;
+        const uint32_t aph = static_cast<uint32_t>((it / WS) & 1);
         const bool got = mbar_wait(smem_u32(&afull[ab]), aph) && mbar_wait(smem_u32(&full_bar[b]), phase);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
