@@ -226,9 +226,10 @@ def measured_peaks() -> dict:
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) over algorithmic
 # bytes, from one ncu capture of the kernel, keyed by the sha256 prefix of the
 # kernel source it was taken with: reported as null once the source changes.
-# full_bwd_bulk_kernel: the 44-source read (read 43) of the 8192 x 896 pass
-# backward, 2445.16 MB read + 1231.98 MB written for 3244.29 MB algorithmic
-# (the second pass over a tile's sources re-reads part of them from DRAM).
+# full_bwd_bulk_kernel: all 64 launches of the 8192 x 896 pass backward
+# without ncu's cache flush between launches, 103100.1 MB read + 60938.3 MB
+# written for 153612.2 MB algorithmic (the second pass over a tile's sources
+# re-reads part of them from DRAM).
 # block_bwd_batched_kernel: all 8 launches of one 8x8 Block backward at 2048
 # tokens, 1554.1 MB read + 420.6 MB written for the step's 2483.0 MB
 # algorithmic (reads equal the algorithmic reads; the rest of the writes were
@@ -238,7 +239,7 @@ def measured_peaks() -> dict:
 # 896 pass without ncu's cache flush between launches, 30289.2 MB read +
 # 1033.1 MB written for 31474.1 MB algorithmic.
 NCU_TRAFFIC = {("full_fwd_bulk_kernel", "664fdb90f174cfdb"): (30289.201664 + 1033.079552) / 31474.057216,
-               ("full_bwd_bulk_kernel", "1d4588bb0e4b35ec"): (2445.157632 + 1231.980032) / 3244.294144,
+               ("full_bwd_bulk_kernel", "bd0791324025b552"): (103100.1 + 60938.3) / 153612.2,
                ("block_bwd_batched_kernel", "cb4b0fb7ff058c27"): (1554.098176 + 420.645888) / 2483.027968}
 
 
@@ -248,15 +249,15 @@ NCU_TRAFFIC = {("full_fwd_bulk_kernel", "664fdb90f174cfdb"): (30289.201664 + 103
 # by workload. The 128K prefill's ratios come from the same blocks at 8192
 # tokens (profiles/block_pass_kernels_8x6x131072x2048_bf16.md).
 NCU_TRAFFIC_BLOCK = {
-    ("stage1_tc_kernel", "fd8dacdfa1f3443d"): {
-        "block_pass_8x6x131072x2048_bf16": (1145.2 + 1356.4) / 2820.1,
-        "block_pass_8x8x16384x1024_bf16": (1144.1 + 1864.6) / 3359.6},
+    ("stage1_tc_kernel", "8b43063b78ead1d8"): {
+        "block_pass_8x6x131072x2048_bf16": (1144.8 + 1354.0) / 2820.1,
+        "block_pass_8x8x16384x1024_bf16": (1144.2 + 1864.0) / 3359.6},
     ("merge_tile_kernel", "11ad511f1735a33e"): {
-        "block_pass_8x6x131072x2048_bf16": (4563.6 + 2108.6) / 6712.2,
-        "block_pass_8x8x16384x1024_bf16": (6762.6 + 3170.9) / 10204.2},
+        "block_pass_8x6x131072x2048_bf16": (4563.3 + 2107.3) / 6712.2,
+        "block_pass_8x8x16384x1024_bf16": (6761.9 + 3173.7) / 10204.2},
     ("accum_fast_kernel", "11ad511f1735a33e"): {
-        "block_pass_8x6x131072x2048_bf16": (838.7 + 272.1) / 1174.4,
-        "block_pass_8x8x16384x1024_bf16": (840.0 + 288.6) / 1174.4},
+        "block_pass_8x6x131072x2048_bf16": (838.6 + 270.9) / 1174.4,
+        "block_pass_8x8x16384x1024_bf16": (839.5 + 285.8) / 1174.4},
 }
 
 KERNEL_FILES = {"full_fwd_bulk_kernel": "full_fwd.cu", "full_bwd_bulk_kernel": "full_bwd.cu",

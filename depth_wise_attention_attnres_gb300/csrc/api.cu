@@ -960,6 +960,9 @@ int attnres_kernel_path(int32_t op, const void* src, const void* out, int32_t n_
       AccumArgs a{wp, src, 0, 1, nullptr, const_cast<void*>(out), T, d, dtype == ATTNRES_BF16};
       return accum_fast_ok(a) ? 1 : 0;
     }
+    case 4:
+      if (dtype != ATTNRES_BF16) return -1;
+      return proj_path(src, src, reinterpret_cast<const float*>(out), T, d);
     default: return -1;
   }
 }

@@ -175,6 +175,8 @@ cudaError_t launch_proj(const void* H, const void* Wq, float* Q, int64_t T, int 
 cudaError_t launch_proj_generic(const void* H, const void* Wq, float* Q, int64_t T, int d, cudaStream_t s);
 bool proj_tc_ok(const void* H, const void* Wq, const float* Q, int64_t T, int d);
 cudaError_t launch_proj_tensor(const void* H, const void* Wq, float* Q, int64_t T, int d, cudaStream_t s);
+// 2: tcgen05 CTA pairs, 1: tcgen05 single CTAs, 0: neither (mma.sync or plain).
+int proj_path(const void* H, const void* Wq, const float* Q, int64_t T, int d);
 cudaError_t take_timeout_proj(unsigned int* flag);
 bool dsplit_ok(const DsplitArgs& a);
 cudaError_t launch_dsplit_partials(const DsplitArgs& a, cudaStream_t s);

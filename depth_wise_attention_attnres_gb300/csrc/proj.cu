@@ -4,16 +4,21 @@
 // per-layer d x d matrix instead of the fixed learned pseudo-query; LLMRes
 // blog, on the paper's ablation).
 //
-// A dense contraction, so it runs on the tensor cores. Three kernels, chosen
+// A dense contraction, so it runs on the tensor cores. Four kernels, chosen
 // by attnres_query_projection in this order:
-//   proj_tc_kernel, the path that runs whenever d is a multiple of 128, 160,
-//     192, 224 or 256, the operands are 16-byte aligned and the driver can
-//     encode tensor maps: 5th-generation tensor cores. Persistent, one CTA
-//     per SM over 128 x BN output tiles; a TMA warp streams 128-byte-swizzled
-//     operand stages, one thread issues tcgen05.mma (M = 128, N = BN,
-//     K = 16) into one of two fp32 accumulators in tensor memory, and four
-//     epilogue warps drain the other with tcgen05.ld through a small shared
-//     staging block (section "tcgen05 path" below).
+//   proj_tc2_kernel, when d is a multiple of 256 and the product has at least
+//     one 256 x 256 output tile for every pair of SMs the device can hold:
+//     clusters of two CTAs share each tile through tcgen05.mma.cta_group::2
+//     (M = 256), each CTA holding half of the tile's A rows and half of its B
+//     rows (section "tcgen05 path, CTA pairs" below).
+//   proj_tc_kernel, the path that runs otherwise whenever d is a multiple of
+//     128, 160, 192, 224 or 256, the operands are 16-byte aligned and the
+//     driver can encode tensor maps: 5th-generation tensor cores. Persistent,
+//     one CTA per SM over 128 x BN output tiles; a TMA warp streams
+//     128-byte-swizzled operand stages, one thread issues tcgen05.mma
+//     (M = 128, N = BN, K = 16) into one of two fp32 accumulators in tensor
+//     memory, and four epilogue warps drain the other with tcgen05.ld through
+//     a small shared staging block (section "tcgen05 path" below).
 //   proj_kernel (fallback when no tensor map is available, d a multiple of
 //     128): warp-level m16n8k16 bf16 MMAs, 128 x 128 tiles per CTA, 8 warps of
 //     64 x 32, K in steps of 32 staged by a 3-deep cp.async pipeline into
@@ -23,6 +28,10 @@
 // the sums on every path.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <mutex>
+#include <utility>
+#include <vector>
 
 #include "common.cuh"
 #include "internal.h"
@@ -147,11 +156,11 @@ cudaError_t launch_proj_generic(const void* H, const void* Wq, float* Q, int64_t
 
 
 // ------------------------------------------------------------ tcgen05 path --
-// The same GEMM on the 5th-generation tensor cores: one 128 x 128 output tile
-// per CTA, the fp32 accumulator in tensor memory (128 lanes x 128 columns).
-// Operand tiles of 128 rows x 64 K (one 128-byte swizzle atom per row) arrive
-// by 2-d TMA copies with the 128-byte swizzle into 4 stages; one thread issues
-// tcgen05.mma (M = 128, N = 128, K = 16, bf16 x bf16 -> fp32), and
+// The same GEMM on the 5th-generation tensor cores: 128 x BN output tiles,
+// the fp32 accumulator in tensor memory (128 lanes x BN columns). Operand
+// tiles of 128 (A) and BN (B) rows x 64 K (one 128-byte swizzle atom per row)
+// arrive by 2-d TMA copies with the 128-byte swizzle into 4 stages; one thread
+// issues tcgen05.mma (M = 128, N = BN, K = 16, bf16 x bf16 -> fp32), and
 // tcgen05.commit frees a stage once the MMAs that read it are done. The four
 // epilogue warps then read their 32-lane quarter of the accumulator with
 // tcgen05.ld and store it through a small shared-memory staging block, as
@@ -407,7 +416,309 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-// A [rows, d] bf16 operand as a 2-d tensor, box {64, 128}, 128-byte swizzle.
+// ------------------------------------------------ tcgen05 path, CTA pairs --
+// Clusters of two CTAs on two SMs share each 256 x BN output tile through
+// tcgen05.mma.cta_group::2 (M = 256). CTA r of a pair holds rows
+// 128 r .. 128 r + 127 of the tile's A block and rows r BN/2 .. r BN/2 +
+// BN/2 - 1 of its B block (output columns); the MMAs, issued by one thread of
+// the even CTA, read both CTAs' shared memory and leave each CTA's 128 rows of
+// the accumulator in that CTA's own tensor memory. Per K step an SM so takes
+// in 128 + BN/2 operand rows for its 128 x BN share of the product, where a
+// CTA alone takes in 128 + BN.
+//
+// Barriers (every wait bounded):
+//  * full[s], in the even CTA: its producer arms the phase with the bytes of
+//    both CTAs' copies, and the copies of both producers (the cta_group::2
+//    form of the TMA load, which may signal the peer's barrier) complete on it;
+//  * empty[s] and tfull[a], in both CTAs: the MMA thread's commits arrive on
+//    the barrier at the same offset in both CTAs (multicast);
+//  * tempty[a], in the even CTA: each epilogue warp of both CTAs arrives after
+//    reading its share of accumulator a;
+//  * done, in both CTAs: a last multicast commit once every MMA has finished.
+// Teardown: each CTA waits for done, the pair meets at a cluster barrier (so
+// no CTA leaves while its peer may still touch its shared memory), and both
+// free the tensor memory together.
+constexpr int kT2Epi = 8;  // epilogue warps per CTA: two per tensor-memory lane quarter
+constexpr int kT2Warps = 2 + kT2Epi;
+constexpr int kT2Threads = kT2Warps * 32;
+constexpr int kT2SmemMax = 227 * 1024;
+constexpr int kT2Fixed = 1024 + 256 + kT2Epi * kEpiWarpFloats * 4;  // alignment slack, barriers, staging
+template <int BN> struct Tc2Tile {
+  static constexpr int kBRows = BN / 2;  // B rows a CTA holds
+  static constexpr int kStageBytes = kTTileBytes + kBRows * kTBK * 2;
+  static constexpr int kStages = (kT2SmemMax - kT2Fixed) / kStageBytes < 8 ? (kT2SmemMax - kT2Fixed) / kStageBytes : 8;
+  static constexpr int kSmem = kT2Fixed + kStages * kStageBytes;
+  static constexpr uint32_t kTmemCols = BN <= 128 ? 128u : 256u;
+  // As TcTile's descriptor, with M = 256.
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                                     (static_cast<uint32_t>(256 >> 4) << 24);
+  static_assert(kBRows % 8 == 0, "B rows come in 8-row swizzle atoms");
+  static_assert(kStages >= 4, "at least four operand stages");
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The shared::cluster address of the same shared-memory offset in CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+
+// All threads of both CTAs; orders each thread's earlier memory operations
+// (remote arrivals included) before the other CTA's later ones.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+
+// mbar_wait for barriers that other CTAs of the cluster signal.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// TMA tile load whose completion may be signalled on the peer CTA's barrier
+// (`bar` a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_bf16_pair(uint32_t tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives once on the barrier at offset `bar` in both CTAs of the pair when
+// the MMAs issued so far have finished.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+
+// Persistent over pair tiles: pair p = blockIdx.x / 2 takes tiles
+// p + i * (gridDim.x / 2). Roles in each CTA: warp 0 lane 0 streams this
+// CTA's operand rows by TMA; warp 1 holds the tensor memory (both CTAs take
+// part in its allocation) and, in the even CTA, its lane 0 issues the MMAs;
+// warps 2-9 drain the accumulators, two warps per lane quarter, splitting
+// the 32-column blocks between them.
+template <int BN>
+__global__ void __launch_bounds__(kT2Threads, 1)
+    proj_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, float* Q,
+                    int64_t T, int d) {
+  using G = Tc2Tile<BN>;
+  constexpr int kS = G::kStages;
+  constexpr uint32_t kAccCols = G::kTmemCols;
+  constexpr uint32_t kCols = 2 * kAccCols;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kS * G::kStageBytes);
+  uint64_t* empty_bar = full_bar + kS;
+  uint64_t* tfull = empty_bar + kS;   // [2]
+  uint64_t* tempty = tfull + 2;       // [2]
+  uint64_t* done_bar = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done_bar + 1);
+  float* epi_stage = reinterpret_cast<float*>(smem + kS * G::kStageBytes + 256);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int ntn = d / BN;
+  const int64_t ntiles = ((T + 255) / 256) * ntn;
+  const int nk = d / kTBK;
+  const int64_t mine = pair < ntiles ? (ntiles - 1 - pair) / npairs + 1 : 0;
+
+  pdl_trigger();
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < kS; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(smem_u32(&tfull[k]), 1);
+      mbar_init(smem_u32(&tempty[k]), 2 * kT2Epi);
+    }
+    mbar_init(smem_u32(done_bar), 1);
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                 "r"(kCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  cluster_sync();  // both CTAs' barriers are initialised before any remote use
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_holder;
+  pdl_wait();
+
+  bool ok = true;
+  if (warp == 0) {
+    if (lane == 0) {
+      int s = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      for (int64_t i = 0; i < mine && ok; ++i) {
+        const int64_t tile = pair + i * npairs;
+        const int m0 = static_cast<int>(tile / ntn) * 256 + static_cast<int>(rank) * kTBM;
+        const int n0 = static_cast<int>(tile % ntn) * BN + static_cast<int>(rank) * G::kBRows;
+        for (int kt = 0; kt < nk; ++kt) {
+          if (!mbar_wait(smem_u32(&empty_bar[s]), phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full_bar[s]);
+          if (rank == 0) mbar_arrive_expect_tx(fb, 2 * G::kStageBytes);
+          const uint32_t fbc = cluster_addr(fb, 0);
+          const uint32_t st = smem_u32(smem + s * G::kStageBytes);
+          tma_load_2d_pair(st, &tmA, kt * kTBK, m0, fbc);
+          tma_load_2d_pair(st + kTTileBytes, &tmB, kt * kTBK, n0, fbc);
+          ++issued;
+          if (++s == kS) {
+            s = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        atomicOr(&g_proj_timeout, 1u);
+        // The even CTA's full barriers count both CTAs' copies; once the
+        // phases it armed complete, no copy of either CTA is in flight.
+        if (rank == 0)
+          for (int64_t it = issued > kS ? issued - kS : 0; it < issued; ++it)
+            (void)mbar_wait_cluster(smem_u32(&full_bar[it % kS]), static_cast<uint32_t>((it / kS) & 1));
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (rank == 0 && lane == 0) {
+      int s = 0;
+      uint32_t phase = 0;
+      for (int64_t i = 0; i < mine && ok; ++i) {
+        const int acc = static_cast<int>(i & 1);
+        if (!mbar_wait_cluster(smem_u32(&tempty[acc]), static_cast<uint32_t>(((i >> 1) & 1) ^ 1))) {
+          ok = false;
+          break;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t tacc = tmem + static_cast<uint32_t>(acc) * kAccCols;
+        for (int kt = 0; kt < nk; ++kt) {
+          if (!mbar_wait_cluster(smem_u32(&full_bar[s]), phase)) {
+            ok = false;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t st = smem_u32(smem + s * G::kStageBytes);
+          const uint64_t da = sw128_desc(st), db = sw128_desc(st + kTTileBytes);
+#pragma unroll
+          for (int k = 0; k < kTBK / 16; ++k)
+            umma_bf16_pair(tacc, da + static_cast<uint64_t>(k * 2), db + static_cast<uint64_t>(k * 2), G::kIdesc,
+                           (kt | k) != 0);
+          umma_commit_pair(smem_u32(&empty_bar[s]));
+          if (++s == kS) {
+            s = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair(smem_u32(&tfull[acc]));
+      }
+      if (!ok) atomicOr(&g_proj_timeout, 1u);
+      umma_commit_pair(smem_u32(done_bar));
+    }
+    __syncwarp();
+  } else {
+    const int q4 = warp & 3;
+    const int half = (warp - 2) >> 2;
+    float* stg = epi_stage + (warp - 2) * kEpiWarpFloats;
+    const uint32_t tempty_c0 = cluster_addr(smem_u32(&tempty[0]), 0);
+    const uint32_t tempty_c1 = cluster_addr(smem_u32(&tempty[1]), 0);
+    for (int64_t i = 0; i < mine; ++i) {
+      const int acc = static_cast<int>(i & 1);
+      const bool got =
+          __all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(&tfull[acc]), static_cast<uint32_t>((i >> 1) & 1)));
+      if (!got) {
+        ok = false;
+        break;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const int64_t tile = pair + i * npairs;
+      const int64_t rbase = (tile / ntn) * 256 + static_cast<int64_t>(rank) * kTBM + q4 * 32;
+      const int n0 = static_cast<int>(tile % ntn) * BN;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(acc) * kAccCols;
+#pragma unroll 1
+      for (int c = half; c < BN / 32; c += 2) {
+        float v[32];
+        tmem_ld32(taddr + static_cast<uint32_t>(c * 32), v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          *reinterpret_cast<float4*>(stg + lane * kEpiLd + 4 * e) =
+              make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          const int r = h * 4 + (lane >> 3);
+          const float4 x = *reinterpret_cast<const float4*>(stg + r * kEpiLd + 4 * (lane & 7));
+          if (rbase + r < T)
+            *reinterpret_cast<float4*>(Q + (rbase + r) * d + n0 + c * 32 + 4 * (lane & 7)) = x;
+        }
+        __syncwarp();
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(acc ? tempty_c1 : tempty_c0);
+    }
+    if (!ok && lane == 0) atomicOr(&g_proj_timeout, 1u);
+  }
+  // Teardown: every MMA has finished (done), then neither CTA leaves or frees
+  // the tensor memory before the other is through.
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 1 && !__all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(done_bar), 0)) && lane == 0)
+    atomicOr(&g_proj_timeout, 1u);
+  cluster_sync();
+  if (warp == 1) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
+  }
+}
+
+// A [rows, d] bf16 operand as a 2-d tensor, box {64, box_rows}, 128-byte swizzle.
 bool encode_operand(const void* base, int64_t rows, int d, int box_rows, CUtensorMap* map) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encode_fn();
   if (!fn) return false;
@@ -466,6 +777,77 @@ cudaError_t launch_proj_tc(const void* H, const void* Wq, float* Q, int64_t T, i
   }
 }
 
+// Launch configuration of the pair kernel with its cluster attribute.
+template <int BN>
+void pair_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], int64_t pairs, cudaStream_t s) {
+  cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  cfg.blockDim = dim3(kT2Threads);
+  cfg.dynamicSmemBytes = Tc2Tile<BN>::kSmem;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+}
+
+// How many CTA pairs of the pair kernel fit on the device at once (0 when
+// clusters cannot be launched), asked once per device and tile width.
+template <int BN>
+int pair_slots() {
+  static std::mutex mu;
+  static std::vector<std::pair<int, int>> known;  // (device, pairs)
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  for (const auto& k : known)
+    if (k.first == dev) return k.second;
+  int n = 0;
+  if (allow_dynamic_smem(reinterpret_cast<const void*>(&proj_tc2_kernel<BN>), Tc2Tile<BN>::kSmem) == cudaSuccess) {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    pair_config<BN>(cfg, attr, sm_count() / 2, nullptr);
+    cfg.numAttrs = 1;  // the occupancy query takes the cluster shape only
+    if (cudaOccupancyMaxActiveClusters(&n, proj_tc2_kernel<BN>, &cfg) != cudaSuccess) n = 0;
+  }
+  (void)cudaGetLastError();
+  known.emplace_back(dev, n);
+  return n;
+}
+
+// Pair tile width for the pair kernel, 0 when it does not serve the shape.
+// Pairs pay with 256-wide tiles: measured at 16384 x 1024 and 8192 x 2048,
+// 30.3 and 47.4 us against 33.4 and 52.3 us for single CTAs. With 224-wide
+// tiles (d = 896) they tie with single CTAs (14.6 against 14.1 us at 8192
+// rows) and with 128-wide ones they lose (17.1 us): there an SM's K steps
+// are set by the MMAs and the operand copies together, not by the operand
+// bytes. The 256-row tiles must also give every pair slot a tile.
+inline int proj2_tile_n(int d, int64_t T) {
+  if (d % 256 != 0) return 0;
+  const int slots = pair_slots<256>();
+  return slots >= 1 && ((T + 255) / 256) * (d / 256) >= slots ? 256 : 0;
+}
+
+template <int BN>
+cudaError_t launch_proj_tc2_n(const void* H, const void* Wq, float* Q, int64_t T, int d, cudaStream_t s) {
+  alignas(64) CUtensorMap ma, mb;
+  if (!encode_operand(H, T, d, kTBM, &ma) || !encode_operand(Wq, d, d, BN / 2, &mb)) return cudaErrorInvalidValue;
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(&proj_tc2_kernel<BN>), Tc2Tile<BN>::kSmem);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = ((T + 255) / 256) * (d / BN);
+  int64_t pairs = pair_slots<BN>();
+  if (pairs > tiles) pairs = tiles;
+  if (pairs < 1) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  pair_config<BN>(cfg, attr, pairs, s);
+  return cudaLaunchKernelEx(&cfg, proj_tc2_kernel<BN>, ma, mb, Q, T, d);
+}
+
 }  // namespace
 
 bool proj_tc_ok(const void* H, const void* Wq, const float* Q, int64_t T, int d) {
@@ -481,7 +863,12 @@ cudaError_t take_timeout_proj(unsigned int* flag) {
 }
 
 cudaError_t launch_proj_tensor(const void* H, const void* Wq, float* Q, int64_t T, int d, cudaStream_t s) {
-  return launch_proj_tc(H, Wq, Q, T, d, s);
+  return proj2_tile_n(d, T) ? launch_proj_tc2_n<256>(H, Wq, Q, T, d, s) : launch_proj_tc(H, Wq, Q, T, d, s);
+}
+
+int proj_path(const void* H, const void* Wq, const float* Q, int64_t T, int d) {
+  if (proj_tc_ok(H, Wq, Q, T, d)) return proj2_tile_n(d, T) ? 2 : 1;
+  return 0;
 }
 
 bool proj_ok(const void* H, const void* Wq, const float* Q, int d) {

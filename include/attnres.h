@@ -533,9 +533,12 @@ const char* attnres_status_string(int32_t status);
 /*
  * attnres_kernel_path - which kernel a call with these arguments would use:
  * 1 = the fast kernel, 0 = the general kernel, negative = invalid arguments.
- * op: 0 full read, 1 stage 1, 2 merge, 3 accumulate. Pointers are only
- * inspected for alignment; n_or_s is n_src for op 0 and 1, ignored otherwise;
- * s is S for op 1.
+ * op: 0 full read, 1 stage 1, 2 merge, 3 accumulate, 4 query projection
+ * (attnres_query_projection with H = Wq = src and Q = out; dtype must be
+ * ATTNRES_BF16): 2 = tensor-core tiles shared by pairs of CTAs, 1 = tensor-core
+ * tiles of one CTA, 0 = another kernel. Pointers are only inspected for
+ * alignment; n_or_s is n_src for op 0 and 1, ignored otherwise; s is S for
+ * op 1. Op 4 asks the device how many CTA pairs fit, so it wants one.
  */
 int attnres_kernel_path(int32_t op, const void* src, const void* out, int32_t n_or_s,
                         int32_t s, int64_t T, int32_t d, int32_t dtype);

@@ -26,19 +26,33 @@ def _wq(d, g):
     return (inputs.randn((d, d), "f32", g, dev()) / d ** 0.5).to(torch.bfloat16).contiguous()
 
 
-# Small products take 128-wide output tiles; the large ones here take the
-# 256-, 224-, 192- and 160-wide tiles (the widest dividing d).
+# Single CTAs take 128-wide tiles, or the widest of 256, 224, 192, 160
+# dividing d; products with d a multiple of 256 that give every CTA pair a
+# 256 x 256 tile run on CTA pairs. The ragged pair cases end in a 256-row tile
+# whose second CTA has some rows (8392) or none (8292, 4103) inside the product.
 @pytest.mark.parametrize("T,d", [(300, 128), (1000, 896), (129, 256), (50, 100), (7, 1024), (200, 640), (77, 384),
-                                 (130, 2048), (4096, 2048), (16384, 896), (32768, 384), (16383, 640)])
+                                 (130, 2048), (4096, 2048), (16384, 896), (32768, 384), (16383, 640), (8192, 896),
+                                 (16384, 1024), (8192, 2048), (8292, 1024), (8392, 1024), (4103, 2048), (8200, 1280)])
 def test_query_projection(T, d):
     g = inputs.generator(40, dev())
     H = inputs.randn((T, d), "bf16", g, dev())
     Wq = _wq(d, g)
-    Q = torch.empty(T, d, device=dev())
+    Q = torch.full((T, d), float("nan"), device=dev())
     ar.attnres_query_projection(H, Wq, Q)
     torch.cuda.synchronize()
     ref = oracle.query_projection(H.cpu(), Wq.cpu())
     assert rel_err(Q, ref) <= TOL["f32"]
+
+
+@pytest.mark.parametrize("T,d,path", [(16384, 1024, 2), (8192, 2048, 2), (8292, 1024, 2), (8392, 1024, 2),
+                                      (4103, 2048, 2), (8192, 896, 1), (1000, 896, 1), (300, 128, 1), (130, 2048, 1),
+                                      (50, 100, 0)])
+def test_query_projection_kernel_choice(T, d, path):
+    """Which of the projection's kernels the shapes above reach (so that both
+    tensor-core kernels are covered)."""
+    H = torch.empty(T, d, device=dev(), dtype=torch.bfloat16)
+    Q = torch.empty(T, d, device=dev())
+    assert ar.attnres_kernel_path(4, H.data_ptr(), Q.data_ptr(), 0, 0, T, d, ar.BF16) == path
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
