@@ -252,12 +252,12 @@ NCU_TRAFFIC_BLOCK = {
     ("stage1_tc_kernel", "8b43063b78ead1d8"): {
         "block_pass_8x6x131072x2048_bf16": (1144.8 + 1354.0) / 2820.1,
         "block_pass_8x8x16384x1024_bf16": (1144.2 + 1864.0) / 3359.6},
-    ("merge_tile_kernel", "11ad511f1735a33e"): {
-        "block_pass_8x6x131072x2048_bf16": (4563.3 + 2107.3) / 6712.2,
-        "block_pass_8x8x16384x1024_bf16": (6761.9 + 3173.7) / 10204.2},
-    ("accum_fast_kernel", "11ad511f1735a33e"): {
-        "block_pass_8x6x131072x2048_bf16": (838.6 + 270.9) / 1174.4,
-        "block_pass_8x8x16384x1024_bf16": (839.5 + 285.8) / 1174.4},
+    ("merge_tile_kernel", "8e6ad3544a6eee10"): {
+        "block_pass_8x6x131072x2048_bf16": (4544.0 + 2067.4) / 6712.2,
+        "block_pass_8x8x16384x1024_bf16": (6719.3 + 3111.0) / 10204.2},
+    ("accum_fast_kernel", "8e6ad3544a6eee10"): {
+        "block_pass_8x6x131072x2048_bf16": (839.5 + 297.6) / 1174.4,
+        "block_pass_8x8x16384x1024_bf16": (839.7 + 319.8) / 1174.4},
 }
 
 KERNEL_FILES = {"full_fwd_bulk_kernel": "full_fwd.cu", "full_bwd_bulk_kernel": "full_bwd.cu",
