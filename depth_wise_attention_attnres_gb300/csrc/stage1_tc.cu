@@ -417,14 +417,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float dot = ((dt.x + dt.y) + dt.z) + dt.w;
           e = dot * rsqrtf(ss * inv_d + a.eps);
         }
+        // Butterflies over the group (G <= 16; the bound is the same in every
+        // lane, so the unrolled steps past it are skipped by the whole warp).
         float mx = e;
-        for (int off = 1; off < G; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+#pragma unroll
+        for (int off = 1; off < 16; off <<= 1)
+          if (off < G) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
         const float x = valid ? __expf(e - mx) : 0.f;
         float z = x;
-        for (int off = 1; off < G; off <<= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+#pragma unroll
+        for (int off = 1; off < 16; off <<= 1)
+          if (off < G) z += __shfl_xor_sync(0xffffffffu, z, off);
         if (valid) {
           const int ab = static_cast<int>((it + k) % WS);
-          const float wgt = x * (1.0f / z);
+          const float wgt = __fdividef(x, z);
           if constexpr (kTC) {
             // B fragment of the output MMA for token r, source block i / 8 and
             // query j: {hi(a[2t]), hi(a[2t+1])}, {lo(a[2t]), lo(a[2t+1])}, t = (i % 8) / 2.
