@@ -249,15 +249,15 @@ NCU_TRAFFIC = {("full_fwd_bulk_kernel", "664fdb90f174cfdb"): (30289.201664 + 103
 # by workload. The 128K prefill's ratios come from the same blocks at 8192
 # tokens (profiles/block_pass_kernels_8x6x131072x2048_bf16.md).
 NCU_TRAFFIC_BLOCK = {
-    ("stage1_tc_kernel", "8b43063b78ead1d8"): {
-        "block_pass_8x6x131072x2048_bf16": (1144.8 + 1354.0) / 2820.1,
-        "block_pass_8x8x16384x1024_bf16": (1144.2 + 1864.0) / 3359.6},
-    ("merge_tile_kernel", "8e6ad3544a6eee10"): {
-        "block_pass_8x6x131072x2048_bf16": (4544.0 + 2067.4) / 6712.2,
-        "block_pass_8x8x16384x1024_bf16": (6719.3 + 3111.0) / 10204.2},
-    ("accum_fast_kernel", "8e6ad3544a6eee10"): {
-        "block_pass_8x6x131072x2048_bf16": (839.5 + 297.6) / 1174.4,
-        "block_pass_8x8x16384x1024_bf16": (839.7 + 319.8) / 1174.4},
+    ("stage1_tc_kernel", "424235d9916c799e"): {
+        "block_pass_8x6x131072x2048_bf16": (1144.4 + 1357.0) / 2820.1,
+        "block_pass_8x8x16384x1024_bf16": (1143.3 + 1870.3) / 3359.6},
+    ("merge_tile_kernel", "855a3f0eb8eb07a0"): {
+        "block_pass_8x6x131072x2048_bf16": (4667.5 + 2071.2) / 6712.2,
+        "block_pass_8x8x16384x1024_bf16": (6996.1 + 3134.6) / 10204.2},
+    ("accum_fast_kernel", "855a3f0eb8eb07a0"): {
+        "block_pass_8x6x131072x2048_bf16": (839.7 + 287.9) / 1174.4,
+        "block_pass_8x8x16384x1024_bf16": (838.5 + 302.1) / 1174.4},
 }
 
 KERNEL_FILES = {"full_fwd_bulk_kernel": "full_fwd.cu", "full_bwd_bulk_kernel": "full_bwd.cu",
