@@ -58,16 +58,20 @@ def full_pass_bytes(R: int, T: int, d: int, es: int) -> int:
     return sum(r + 2 for r in range(R)) * T * d * es
 
 
-def block_pass_bytes(N: int, S: int, T: int, d: int, es: int, plan=None, freeze_last: bool = False) -> dict:
+def block_pass_bytes(N: int, S: int, T: int, d: int, es: int, plan=None, freeze_last: bool = False,
+                     fused_freeze: bool = True) -> dict:
     """Algorithmic bytes per kernel of the two-stage Block pass.
 
     stage 1 of block n (n+1 sources): reads (n+1) rows, writes S output rows
     and S lse values per token. Merge j (1 <= j < S): reads O_j, lse_j and its
     running sum P_j as the last kept sum P_m (fp32, if m > 0) plus the j - m
     outputs since, writes out_j and, if the plan keeps P_j, P_j (fp32). The
-    freeze reads P_S the same way and writes the summary. plan[j] = 1 where
-    the pass keeps P_j (attnres_block_running_sum_plan); None keeps every sum
-    (the one-step merges).
+    block's last merge also freezes the summary (fused_freeze, as
+    attnres_block_pass does when S > 1): it reads f_{S-1} more and writes the
+    summary. A separate freeze (S = 1, or not fused) reads P_S the same way
+    as a merge and writes the summary. plan[j] = 1 where the pass keeps P_j
+    (attnres_block_running_sum_plan); None keeps every sum (the one-step
+    merges).
     """
     if plan is None:
         plan = [0] + [1] * (S - 1) + [0]
@@ -81,7 +85,10 @@ def block_pass_bytes(N: int, S: int, T: int, d: int, es: int, plan=None, freeze_
             if plan[j]:
                 m = j
         if n + 1 < N or freeze_last:
-            freeze += (S - m) * E * es + (4 * E if m > 0 else 0) + E * es
+            if S > 1 and fused_freeze:
+                merge += 2 * E * es
+            else:
+                freeze += (S - m) * E * es + (4 * E if m > 0 else 0) + E * es
     return {"stage1": st1, "merge": merge, "freeze": freeze, "total": st1 + merge + freeze}
 
 
@@ -387,7 +394,9 @@ class BlockPassStep:
         self.lse = torch.empty(wl.S, wl.T, device=dev)
         self.P = torch.empty(wl.T, wl.d, device=dev)
         self.out = torch.empty(wl.N * wl.S, wl.T, wl.d, device=dev, dtype=dt)
-        self.launches = wl.N + wl.N * (wl.S - 1) + (wl.N - 1)
+        # Stage 1 and S - 1 merges per block; a separate freeze only with one
+        # sublayer per block (otherwise the block's last merge freezes).
+        self.launches = wl.N + wl.N * (wl.S - 1) + (wl.N - 1 if wl.S == 1 else 0)
         es = 2 if wl.dtype == "bf16" else 4
         self.plan = binding.attnres_block_running_sum_plan(wl.S, binding.BF16 if es == 2 else binding.F32)
         self.byte_parts = block_pass_bytes(wl.N, wl.S, wl.T, wl.d, es, self.plan)
@@ -409,12 +418,15 @@ class BlockPassStep:
                 self.Src, n + 1, self.W[k0:k0 + wl.S], self.G[k0:k0 + wl.S], wl.eps, O, self.lse))
             m = 0
             for j in range(1, wl.S):
-                groups["merge"].append(lambda k0=k0, j=j, m=m: ar.attnres_block_merge_parts(
+                # The block's last merge also freezes its summary.
+                summ = self.Src[n + 1] if j == wl.S - 1 and n + 1 < wl.N else None
+                groups["merge"].append(lambda k0=k0, j=j, m=m, summ=summ: ar.attnres_block_merge_parts(
                     self.O[j - 1], self.lse[j], self.P if m > 0 else None, self.F[k0 + m:], j - m,
-                    self.P if plan[j] else None, self.W[k0 + j], self.G[k0 + j], wl.eps, self.out[k0 + j]))
+                    self.P if plan[j] else None, self.W[k0 + j], self.G[k0 + j], wl.eps, self.out[k0 + j],
+                    summary_out=summ))
                 if plan[j]:
                     m = j
-            if n + 1 < wl.N:
+            if n + 1 < wl.N and wl.S == 1:
                 groups["freeze"].append(lambda n=n, k0=k0, m=m: ar.attnres_block_summary_parts(
                     self.P if m > 0 else None, self.F[k0 + m:], wl.S - m, summary_out=self.Src[n + 1]))
         return groups

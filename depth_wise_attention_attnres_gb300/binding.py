@@ -50,7 +50,7 @@ _SIGNATURES = {
                                     _VP, _VP, _VP],
     "attnres_block_summary_accumulate": [_VP, _VP, _I32, _VP, _I64, _I32, _I32, _VP],
     "attnres_block_merge_parts": [_VP, _VP, _VP, _VP, _I64, _I32, _VP, _VP, _VP, _F, _I64, _I32, _I32, _VP,
-                                  _VP],
+                                  _VP, _VP],
     "attnres_block_summary_parts": [_VP, _VP, _I64, _I32, _VP, _VP, _I64, _I32, _I32, _VP],
     "attnres_block_running_sum_plan": [_I32, _I32, ctypes.POINTER(_I32)],
     "attnres_block_pass": [_VP, _I64, _I32, _I32, _I64, _I32, _I32, _VP, _VP, _F, _VP, _I64,
@@ -395,13 +395,14 @@ def _parts(F_parts: torch.Tensor, n_parts: int) -> tuple[int, int, int, int]:
 
 def attnres_block_merge_parts(O_j: torch.Tensor, lse_j: torch.Tensor, P_base, F_parts: torch.Tensor,
                               n_parts: int, P_out, w: torch.Tensor, gamma: torch.Tensor, eps: float,
-                              out: torch.Tensor, stream=None) -> torch.Tensor:
+                              out: torch.Tensor, summary_out=None, stream=None) -> torch.Tensor:
     """Merge with the running sum P_base + F_parts[0] + ... + F_parts[n_parts-1]
-    (P_base may be None), storing it to P_out when given."""
-    T, d, pstride, code = _parts(F_parts, n_parts)
+    (P_base may be None), storing it to P_out when given; with summary_out,
+    also the block summary: that sum plus F_parts[n_parts], rounded."""
+    T, d, pstride, code = _parts(F_parts, n_parts + (1 if summary_out is not None else 0))
     _check("attnres_block_merge_parts", lib().attnres_block_merge_parts(
         _ptr(O_j), _ptr(lse_j), _ptr(P_base), _ptr(F_parts), pstride, n_parts, _ptr(P_out), _ptr(w),
-        _ptr(gamma), eps, T, d, code, _ptr(out), _stream(stream)))
+        _ptr(gamma), eps, T, d, code, _ptr(out), _ptr(summary_out), _stream(stream)))
     return out
 
 

@@ -247,29 +247,35 @@ int run_stage1(const MultiArgs& m, cudaStream_t s) {
 // sublayer outputs at F_parts (part_stride apart), stored to P_out if given.
 int make_merge_parts(const void* O_j, const float* lse_j, const float* P_base, const void* F_parts,
                      int64_t part_stride, int32_t n_parts, float* P_out, const float* w, const float* gamma,
-                     float eps, int64_t T, int32_t d, int32_t dtype, void* out, MergeArgs* a) {
-  if (d < 1 || T < 0 || !valid_dtype(dtype) || !valid_eps(eps) || n_parts < 0 || n_parts > kMaxMergeParts)
+                     float eps, int64_t T, int32_t d, int32_t dtype, void* out, void* summary_out, MergeArgs* a) {
+  // With a summary the parts hold one output more than the running sum.
+  const int32_t nf = n_parts + (summary_out ? 1 : 0);
+  if (d < 1 || T < 0 || !valid_dtype(dtype) || !valid_eps(eps) || n_parts < 0 || nf > kMaxMergeParts)
     return ATTNRES_ERR_INVALID_ARG;
   if (n_parts == 0 && !P_base) return ATTNRES_ERR_INVALID_ARG;
   if (T == 0) return ATTNRES_OK;
-  if (!O_j || !lse_j || !w || !gamma || !out || (n_parts > 0 && !F_parts)) return ATTNRES_ERR_INVALID_ARG;
+  if (!O_j || !lse_j || !w || !gamma || !out || (nf > 0 && !F_parts)) return ATTNRES_ERR_INVALID_ARG;
   const int64_t E = T * d;
-  if (n_parts > 1 && part_stride < E) return ATTNRES_ERR_INVALID_ARG;
+  if (nf > 1 && part_stride < E) return ATTNRES_ERR_INVALID_ARG;
   const int es = elem_size(dtype);
   const Range ro = range_of(O_j, E * es), rl = range_of(lse_j, T * 4), rout = range_of(out, E * es);
   const Range rb = P_base ? range_of(P_base, E * 4) : Range{};
-  const Range rf = n_parts > 0 ? range_of(F_parts, ((n_parts - 1) * (n_parts > 1 ? part_stride : 0) + E) * es)
-                               : Range{};
+  const Range rf = nf > 0 ? range_of(F_parts, ((nf - 1) * (nf > 1 ? part_stride : 0) + E) * es) : Range{};
   const Range rp = P_out ? range_of(P_out, E * 4) : Range{};
-  // out and P_out are written: they overlap nothing else, except that P_out
-  // may be P_base itself (the running sum advanced in place).
-  if (overlap(rout, ro) || overlap(rout, rl) || overlap(rout, rb) || overlap(rout, rf) || overlap(rout, rp))
+  const Range rs = summary_out ? range_of(summary_out, E * es) : Range{};
+  // out, P_out and summary_out are written: they overlap nothing else, except
+  // that P_out may be P_base itself (the running sum advanced in place).
+  if (overlap(rout, ro) || overlap(rout, rl) || overlap(rout, rb) || overlap(rout, rf) || overlap(rout, rp) ||
+      overlap(rout, rs))
     return ATTNRES_ERR_INVALID_ARG;
-  if (overlap(rp, ro) || overlap(rp, rl) || overlap(rp, rf) || (overlap(rp, rb) && P_out != P_base))
+  if (overlap(rp, ro) || overlap(rp, rl) || overlap(rp, rf) || (overlap(rp, rb) && P_out != P_base) ||
+      overlap(rp, rs))
     return ATTNRES_ERR_INVALID_ARG;
-  *a = MergeArgs{O_j, lse_j, P_base, F_parts, n_parts > 1 ? part_stride : 0, n_parts, P_out, w, gamma, eps, T, d,
+  if (overlap(rs, ro) || overlap(rs, rl) || overlap(rs, rb) || overlap(rs, rf)) return ATTNRES_ERR_INVALID_ARG;
+  *a = MergeArgs{O_j, lse_j, P_base, F_parts, nf > 1 ? part_stride : 0, n_parts, P_out, w, gamma, eps, T, d,
                  dtype == ATTNRES_BF16, out};
   a->withhold = withhold_for(kWithholdMerge);
+  a->summary = summary_out;
   return ATTNRES_OK;
 }
 
@@ -289,7 +295,7 @@ int make_merge(const void* O_j, const float* lse_j, float* P, const void* f_prev
       overlap(rp, ro) || overlap(rp, rf) || overlap(rp, rl))
     return ATTNRES_ERR_INVALID_ARG;
   return make_merge_parts(O_j, lse_j, p_is_empty ? nullptr : P, f_prev, 0, f_prev ? 1 : 0, f_prev ? P : nullptr, w,
-                          gamma, eps, T, d, dtype, out, a);
+                          gamma, eps, T, d, dtype, out, nullptr, a);
 }
 
 // Checks and fills a running-sum step: P_base + the n_parts outputs, into
@@ -786,10 +792,10 @@ int attnres_block_merge_prenorm(const void* O_j, const float* lse_j, float* P, c
 int attnres_block_merge_parts(const void* O_j, const float* lse_j, const float* P_base, const void* F_parts,
                               int64_t part_stride, int32_t n_parts, float* P_out, const float* w,
                               const float* gamma, float eps, int64_t T, int32_t d, int32_t dtype, void* out,
-                              void* stream) {
+                              void* summary_out, void* stream) {
   MergeArgs a{};
   const int st = make_merge_parts(O_j, lse_j, P_base, F_parts, part_stride, n_parts, P_out, w, gamma, eps, T, d,
-                                  dtype, out, &a);
+                                  dtype, out, summary_out, &a);
   if (st != ATTNRES_OK || T == 0) return st;
   return launched([&] { return launch_merge(a, as_stream(stream), merge_fast_ok(a)); });
 }
@@ -865,11 +871,16 @@ int attnres_block_pass(const void* F, int64_t f_stride, int32_t N, int32_t S, in
     // Stage 2: merge each later sublayer's read with its running sum P_j =
     // P_m + f_{k0+m} + ... + f_{k0+j-1}, m the last kept position (0: none).
     int m = 0;
+    const bool freeze = n + 1 < N || freeze_last;
     for (int j = 1; j < S; ++j) {
+      // The block's last merge also freezes its summary b_{n+1} = P_{S-1} +
+      // f_{S-1} into Src[n + 1]: it forms P_{S-1} anyway, so the freeze
+      // reads only f_{S-1} more.
+      void* summary = j == S - 1 && freeze ? Srcb + (n + 1) * src_stride * es : nullptr;
       MergeArgs a{};
       st = make_merge_parts(O[j], lse_scratch + j * T, m > 0 ? P_scratch : nullptr, Fb + (k0 + m) * f_stride * es,
                             f_stride, j - m, plan[j] ? P_scratch : nullptr, W + (k0 + j) * d, Gamma + (k0 + j) * d,
-                            eps, T, d, dtype, outb + (k0 + j) * out_stride * es, &a);
+                            eps, T, d, dtype, outb + (k0 + j) * out_stride * es, summary, &a);
       if (st != ATTNRES_OK) return st;
       // The merge before this one writes neither O[j] nor any output f;
       // stage 1 (before merge 1) writes O[j].
@@ -878,8 +889,9 @@ int attnres_block_pass(const void* F, int64_t f_stride, int32_t N, int32_t S, in
       if (st != ATTNRES_OK) return st;
       if (plan[j]) m = j;
     }
-    // Freeze the block summary b_{n+1} = P_S into Src[n + 1].
-    if (n + 1 < N || freeze_last) {
+    // With one sublayer a block has no merge: freeze its summary b_{n+1} = f
+    // into Src[n + 1] here.
+    if (freeze && S == 1) {
       st = attnres_block_summary_parts(m > 0 ? P_scratch : nullptr, Fb + (k0 + m) * f_stride * es, f_stride, S - m,
                                        nullptr, Srcb + (n + 1) * src_stride * es, T, d, dtype, stream);
       if (st != ATTNRES_OK) return st;

@@ -92,6 +92,9 @@ struct MergeArgs {
   // merge before, never stage 1, which writes O_j).
   int early;
   int64_t withhold = -1;  // test hook of the tiled merge (as FullArgs)
+  // Also store round(running sum + parts[nparts]) here:
+  // a block's summary, the freeze fused into its last merge. nullptr: none.
+  void* summary = nullptr;
 };
 constexpr int kMaxMergeParts = 16;
 

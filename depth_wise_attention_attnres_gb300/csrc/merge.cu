@@ -97,10 +97,12 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
   const uint32_t row_t = static_cast<uint32_t>(d) * sizeof(T);
   const uint32_t row_p = static_cast<uint32_t>(d) * 4u;
   const int np = a.nparts;
+  const int nx = a.summary ? 1 : 0;  // the part after the running sum's, for the summary
   const bool with_p = a.P != nullptr;
-  // Stage layout: O rows, then each part's rows, then P rows.
-  const uint32_t p_off = static_cast<uint32_t>(TM) * row_t * static_cast<uint32_t>(1 + np);
-  const uint32_t tx_row = row_t * static_cast<uint32_t>(1 + np) + (with_p ? row_p : 0u);
+  // Stage layout: O rows, then each part's rows (the summary's extra part
+  // last), then P rows.
+  const uint32_t p_off = static_cast<uint32_t>(TM) * row_t * static_cast<uint32_t>(1 + np + nx);
+  const uint32_t tx_row = row_t * static_cast<uint32_t>(1 + np + nx) + (with_p ? row_p : 0u);
   const int64_t ntok = a.T;
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * ntok / gridDim.x;
   const int64_t r1 = static_cast<int64_t>(blockIdx.x + 1) * ntok / gridDim.x;
@@ -126,7 +128,7 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
     // O_j rows and the parts' rows of tile t into stage st.
     auto load_inputs = [&](unsigned char* st, int64_t row0, uint32_t rows, uint32_t fb) {
       bulk_g2s(smem_u32(st), static_cast<const T*>(a.O) + row0 * d, rows * row_t, fb);
-      for (int u = 0; u < np; ++u)
+      for (int u = 0; u < np + nx; ++u)
         bulk_g2s(smem_u32(st + static_cast<uint32_t>(1 + u) * TM * row_t),
                  static_cast<const T*>(a.parts) + u * a.part_stride + row0 * d, rows * row_t, fb);
     };
@@ -217,6 +219,14 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
     const unsigned char* st = stages + static_cast<size_t>(s) * g.stage_bytes;
     const T* so = reinterpret_cast<const T*>(st) + rslot * d;
     const float* sp = reinterpret_cast<const float*>(st + p_off) + rslot * d;
+    // The block summary: the running sum plus the extra part, in fp32, then
+    // rounded once (the freeze's sum, in its order).
+    auto store_summary = [&](int k, const float (&pk)[4]) {
+      float f[4];
+      lds4(reinterpret_cast<const T*>(st + static_cast<uint32_t>(1 + np) * TM * row_t) + rslot * d + k, f);
+      const float b4[4] = {pk[0] + f[0], pk[1] + f[1], pk[2] + f[2], pk[3] + f[3]};
+      st4(static_cast<T*>(a.summary) + row * d + k, b4);
+    };
     float p[Q][4];
     float ss = 0.f, dot = 0.f;
     if (Q >= 8 && wok && live) {
@@ -242,6 +252,7 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
             p[q][0] += f[0]; p[q][1] += f[1]; p[q][2] += f[2]; p[q][3] += f[3];
           }
           if (a.P_out) st4(a.P_out + row * d + k, p[q]);
+          if (nx) store_summary(k, p[q]);
           const float4 w4 = *reinterpret_cast<const float4*>(wq + k);
           ss = fmaf(p[q][0], p[q][0], ss); ss = fmaf(p[q][1], p[q][1], ss);
           ss = fmaf(p[q][2], p[q][2], ss); ss = fmaf(p[q][3], p[q][3], ss);
@@ -283,6 +294,7 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
         const int k = kbeg + (q * 32 + lane) * 4;
         if (k < kend) {
           if (a.P_out) st4(a.P_out + row * d + k, p[q]);
+          if (nx) store_summary(k, p[q]);
           const float4 w4 = *reinterpret_cast<const float4*>(wq + k);
           ss = fmaf(p[q][0], p[q][0], ss); ss1 = fmaf(p[q][1], p[q][1], ss1);
           ss = fmaf(p[q][2], p[q][2], ss); ss1 = fmaf(p[q][3], p[q][3], ss1);
@@ -419,6 +431,9 @@ __global__ void __launch_bounds__(kBlock) merge_generic_kernel(MergeArgs a) {
       const int64_t off = row * d + k;
       const float p = running_sum_at<T>(a.P, a.parts, a.part_stride, a.nparts, off);
       if (a.P_out) a.P_out[off] = p;
+      if (a.summary)  // the block summary: one part more, then rounded
+        static_cast<T*>(a.summary)[off] =
+            from_f32<T>(p + to_f32(static_cast<const T*>(a.parts)[a.nparts * a.part_stride + off]));
       ss = fmaf(p, p, ss);
       dot = fmaf(a.w[k] * a.gamma[k], p, dot);
     }
@@ -536,12 +551,14 @@ bool merge_fast_ok(const MergeArgs& a) {
   const int es = a.bf16 ? 2 : 4;
   if (a.d % 4 != 0 || (a.d * es) % 16 != 0) return false;
   if ((a.part_stride * es) % 16 != 0) return false;
-  const MergeGeom g = merge_geom(a.d, es, a.pre.gamma != nullptr, a.nparts, a.P != nullptr);
+  const int nx = a.summary ? 1 : 0;
+  const MergeGeom g = merge_geom(a.d, es, a.pre.gamma != nullptr, a.nparts + nx, a.P != nullptr);
   const int per_warp = (a.d + g.wpr - 1) / g.wpr;
   // Every part of a row starts on a 4-feature chunk (aligned vector loads).
   if (per_warp % 4 != 0 || per_warp > 8 * 128 || g.total > 227 * 1024) return false;
-  return aligned16(a.O) && aligned16(a.P) && aligned16(a.P_out) && aligned16(a.out) &&
-         (a.nparts == 0 || aligned16(a.parts)) && (!a.pre.gamma || (aligned16(a.pre.gamma) && aligned16(a.pre.out)));
+  return aligned16(a.O) && aligned16(a.P) && aligned16(a.P_out) && aligned16(a.out) && aligned16(a.summary) &&
+         (a.nparts + nx == 0 || aligned16(a.parts)) &&
+         (!a.pre.gamma || (aligned16(a.pre.gamma) && aligned16(a.pre.out)));
 }
 
 bool accum_fast_ok(const AccumArgs& a) {
@@ -564,7 +581,8 @@ cudaError_t launch_merge_tiles(const MergeArgs& a, const MergeGeom& g, cudaStrea
 
 template <typename T>
 cudaError_t launch_merge_dtype(const MergeArgs& a, cudaStream_t s) {
-  const MergeGeom g = merge_geom(a.d, sizeof(T), a.pre.gamma != nullptr, a.nparts, a.P != nullptr);
+  const MergeGeom g = merge_geom(a.d, sizeof(T), a.pre.gamma != nullptr, a.nparts + (a.summary ? 1 : 0),
+                                 a.P != nullptr);
   const int per_warp = (a.d + g.wpr - 1) / g.wpr;
   int q = 1;
   while (q * 128 < per_warp) q <<= 1;

@@ -370,12 +370,19 @@ int attnres_block_summary_accumulate(float* P, const void* f, int32_t p_is_empty
  *               P_base itself (in place) but must not overlap anything else.
  *   w, gamma    device, fp32 [d] of this sublayer.
  *   out         device, [T, d] dtype; overlaps no other argument.
+ *   summary_out device, [T, d] dtype, or NULL. When given, F_parts holds one
+ *               output more (n_parts + 1 of them, at most 16) and summary_out
+ *               receives P_j + f_{n_parts}, added in fp32 after the others
+ *               and rounded: the block's summary, frozen by its last merge
+ *               (the same bits as attnres_block_summary_parts over all
+ *               n_parts + 1 parts). Overlaps no other argument.
  * Errors as attnres_block_merge.
  */
 int attnres_block_merge_parts(const void* O_j, const float* lse_j, const float* P_base,
                               const void* F_parts, int64_t part_stride, int32_t n_parts,
                               float* P_out, const float* w, const float* gamma, float eps,
-                              int64_t T, int32_t d, int32_t dtype, void* out, void* stream);
+                              int64_t T, int32_t d, int32_t dtype, void* out, void* summary_out,
+                              void* stream);
 
 /*
  * attnres_block_summary_parts - a running sum from parts (as in

@@ -271,21 +271,34 @@ def test_running_sum_plan_is_the_cheapest(lib, dtype, es):
 
 
 def test_merge_parts_validation(lib):
-    # (O, lse, P_base, F_parts, part_stride, n_parts, P_out, w, gamma, eps, T, d, dtype, out)
+    # (O, lse, P_base, F_parts, part_stride, n_parts, P_out, w, gamma, eps, T, d, dtype, out, summary_out)
     f = ctypes.c_float(1e-6)
     E = 64
-    assert lib.attnres_block_merge_parts(P, 2 * P, None, None, E, 0, None, P, P, f, 4, 16, 1, 5 * P, None) == INVALID
+    assert lib.attnres_block_merge_parts(P, 2 * P, None, None, E, 0, None, P, P, f, 4, 16, 1, 5 * P, None,
+                                         None) == INVALID
     assert lib.attnres_block_merge_parts(P, 2 * P, None, 3 * P, E - 1, 2, None, P, P, f, 4, 16, 1, 5 * P,
-                                         None) == INVALID                         # parts overlap each other
+                                         None, None) == INVALID                   # parts overlap each other
     assert lib.attnres_block_merge_parts(P, 2 * P, None, 3 * P, E, 17, None, P, P, f, 4, 16, 1, 5 * P,
-                                         None) == INVALID                         # too many parts
+                                         None, None) == INVALID                   # too many parts
     assert lib.attnres_block_merge_parts(P, 2 * P, 4 * P, 3 * P, E, 2, 4 * P + 64, P, P, f, 4, 16, 1, 5 * P,
-                                         None) == INVALID                         # P_out partly over P_base
+                                         None, None) == INVALID                   # P_out partly over P_base
     assert lib.attnres_block_merge_parts(P, 2 * P, None, 3 * P, E, 2, 3 * P, P, P, f, 4, 16, 1, 5 * P,
-                                         None) == INVALID                         # P_out over the parts
+                                         None, None) == INVALID                   # P_out over the parts
+    # The summary: one part more (16 at most), written over nothing else.
+    assert lib.attnres_block_merge_parts(P, 2 * P, None, 3 * P, E, 16, None, P, P, f, 4, 16, 1, 5 * P,
+                                         6 * P, None) == INVALID                  # 17 parts
+    assert lib.attnres_block_merge_parts(P, 2 * P, None, 3 * P, E, 2, None, P, P, f, 4, 16, 1, 5 * P,
+                                         5 * P, None) == INVALID                  # summary over out
+    assert lib.attnres_block_merge_parts(P, 2 * P, None, 3 * P, E, 2, None, P, P, f, 4, 16, 1, 5 * P,
+                                         3 * P + 2 * E * 2, None) == INVALID      # summary over the extra part
+    assert lib.attnres_block_merge_parts(P, 2 * P, None, None, E, 0, None, P, P, f, 4, 16, 1, 5 * P,
+                                         6 * P, None) == INVALID                  # no parts, no base
     binding.attnres_test_fail_launch(0)                                         # valid: reaches the launch
     assert lib.attnres_block_merge_parts(P, 2 * P, 4 * P, 3 * P, E, 2, 4 * P, P, P, f, 4, 16, 1, 5 * P,
-                                         None) == 3
+                                         None, None) == 3
+    binding.attnres_test_fail_launch(0)
+    assert lib.attnres_block_merge_parts(P, 2 * P, 4 * P, 3 * P, E, 2, 4 * P, P, P, f, 4, 16, 1, 5 * P,
+                                         6 * P, None) == 3
     binding.attnres_test_fail_launch(0)
     assert lib.attnres_block_summary_parts(None, 3 * P, E, 3, None, 5 * P, 4, 16, 1, None) == 3
     binding.attnres_test_fail_launch(-1)

@@ -101,6 +101,40 @@ def test_summary_parts_equals_one_step_freeze(dt, T, d):
         assert torch.equal(P_out, sums[S - 1]), m
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+@pytest.mark.parametrize("T,d", [(300, 1024), (77, 2048), (45, 640), (13, 100), (9, 3)])
+def test_merge_parts_with_summary(dt, T, d):
+    """The block's last merge freezing its summary: summary_out must hold the
+    freeze's bits (attnres_block_summary_parts over one part more), P_out the
+    running sum's, and out the merge (to the reduction-order tolerance: the
+    extra part changes the tile shape)."""
+    g = inputs.generator(84, dev())
+    J = 6
+    F = inputs.randn((J, T, d), dt, g, dev())
+    O = inputs.randn((T, d), dt, g, dev())
+    lse = torch.randn(T, device=dev())
+    w = inputs.queries(1, d, 0.05, g, dev())[0]
+    gam = 1 + 0.3 * inputs.queries(1, d, 1.0, g, dev())[0]
+    sums = _one_step_sums(F, J)
+    for j in range(1, J):
+        for m in range(0, j + 1):
+            base = sums[m - 1] if m > 0 else None
+            if base is None and m == j:
+                continue
+            ref_out = torch.empty(T, d, device=dev(), dtype=dtype_of(dt))
+            ar.attnres_block_merge_parts(O, lse, base, F[m:], j - m, None, w, gam, 1e-6, ref_out)
+            ref_sum = torch.empty(T, d, device=dev(), dtype=dtype_of(dt))
+            ar.attnres_block_summary_parts(base, F[m:], j + 1 - m, summary_out=ref_sum)
+            out = torch.full((T, d), float("nan"), device=dev(), dtype=dtype_of(dt))
+            summ = torch.full((T, d), float("nan"), device=dev(), dtype=dtype_of(dt))
+            P_out = torch.full((T, d), float("nan"), device=dev())
+            ar.attnres_block_merge_parts(O, lse, base, F[m:], j - m, P_out, w, gam, 1e-6, out, summary_out=summ)
+            torch.cuda.synchronize()
+            assert torch.equal(summ, ref_sum), (j, m)
+            assert torch.equal(P_out, sums[j - 1]), (j, m)
+            assert rel_err(out, ref_out.double().cpu().numpy()) <= ORDER_TOL[dt], (j, m)
+
+
 def _pass_by_one_step_calls(F, emb, N, S, W, G):
     """The Block pass written out with the one-step merge and freeze calls
     (the running sum kept in P at every step)."""
