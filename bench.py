@@ -5,7 +5,8 @@ inputs already resident in HBM. The default (headline) workload is the
 long-context prefill Block AttnRes pass: T = 131072 tokens (128K), d = 2048,
 48 sublayers in 8 blocks of 6, bf16 storage with fp32 arithmetic; every
 sublayer's read runs by the two-stage computation (stage 1 per block, one
-online-softmax merge per later sublayer, a freeze per block summary). This is
+online-softmax merge per later sublayer, the block's last merge also freezing
+the block summary). This is
 the largest single-GPU footprint of the standard workloads (about 60 GB
 resident). The other bench workloads are measured in the same run and
 reported under "extras": the deep-narrow Full pass (141 reads, 32768 x 640),
@@ -582,7 +583,7 @@ def time_graph(step, steps, warmup, world, stream):
 def time_block_kernels(step, reps, stream):
     """Device time per kernel kind of the Block pass, measured the way the
     step is: each kind's launches of one pass (its stage-1 reads, its merges,
-    its freezes) are captured in a CUDA graph of their own and replayed `reps`
+    its separate freezes, if any) are captured in a CUDA graph of their own and replayed `reps`
     times between CUDA events on the launching stream. Returns ms per pass
     and launches per pass for each kind. The kinds' sum differs from the
     step's own graph time by the overlap of neighbouring launches."""
