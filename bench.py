@@ -5,8 +5,8 @@ inputs already resident in HBM. The default (headline) workload is the
 long-context prefill Block AttnRes pass: T = 131072 tokens (128K), d = 2048,
 48 sublayers in 8 blocks of 6, bf16 storage with fp32 arithmetic; every
 sublayer's read runs by the two-stage computation (stage 1 per block, one
-online-softmax merge per later sublayer, the block's last merge also freezing
-the block summary). This is
+online-softmax merge per later sublayer, a freeze per block summary, in the
+order a layer-by-layer forward runs them). This is
 the largest single-GPU footprint of the standard workloads (about 60 GB
 resident). The other bench workloads are measured in the same run and
 reported under "extras": the deep-narrow Full pass (141 reads, 32768 x 640),
@@ -60,17 +60,18 @@ def full_pass_bytes(R: int, T: int, d: int, es: int) -> int:
 
 
 def block_pass_bytes(N: int, S: int, T: int, d: int, es: int, plan=None, freeze_last: bool = False,
-                     fused_freeze: bool = True) -> dict:
+                     fused_freeze: bool = False) -> dict:
     """Algorithmic bytes per kernel of the two-stage Block pass.
 
     stage 1 of block n (n+1 sources): reads (n+1) rows, writes S output rows
     and S lse values per token. Merge j (1 <= j < S): reads O_j, lse_j and its
     running sum P_j as the last kept sum P_m (fp32, if m > 0) plus the j - m
     outputs since, writes out_j and, if the plan keeps P_j, P_j (fp32). The
-    block's last merge also freezes the summary (fused_freeze, as
-    attnres_block_pass does when S > 1): it reads f_{S-1} more and writes the
-    summary. A separate freeze (S = 1, or not fused) reads P_S the same way
-    as a merge and writes the summary. plan[j] = 1 where the pass keeps P_j
+    freeze reads P_S the same way and writes the summary (attnres_block_pass,
+    in the order of a layer-by-layer forward). With fused_freeze the block's
+    last merge freezes instead (attnres_block_merge_parts' summary_out, for
+    callers holding every output): it reads f_{S-1} more and writes the
+    summary. plan[j] = 1 where the pass keeps P_j
     (attnres_block_running_sum_plan); None keeps every sum (the one-step
     merges).
     """
@@ -395,9 +396,7 @@ class BlockPassStep:
         self.lse = torch.empty(wl.S, wl.T, device=dev)
         self.P = torch.empty(wl.T, wl.d, device=dev)
         self.out = torch.empty(wl.N * wl.S, wl.T, wl.d, device=dev, dtype=dt)
-        # Stage 1 and S - 1 merges per block; a separate freeze only with one
-        # sublayer per block (otherwise the block's last merge freezes).
-        self.launches = wl.N + wl.N * (wl.S - 1) + (wl.N - 1 if wl.S == 1 else 0)
+        self.launches = wl.N + wl.N * (wl.S - 1) + (wl.N - 1)
         es = 2 if wl.dtype == "bf16" else 4
         self.plan = binding.attnres_block_running_sum_plan(wl.S, binding.BF16 if es == 2 else binding.F32)
         self.byte_parts = block_pass_bytes(wl.N, wl.S, wl.T, wl.d, es, self.plan)
@@ -419,15 +418,12 @@ class BlockPassStep:
                 self.Src, n + 1, self.W[k0:k0 + wl.S], self.G[k0:k0 + wl.S], wl.eps, O, self.lse))
             m = 0
             for j in range(1, wl.S):
-                # The block's last merge also freezes its summary.
-                summ = self.Src[n + 1] if j == wl.S - 1 and n + 1 < wl.N else None
-                groups["merge"].append(lambda k0=k0, j=j, m=m, summ=summ: ar.attnres_block_merge_parts(
+                groups["merge"].append(lambda k0=k0, j=j, m=m: ar.attnres_block_merge_parts(
                     self.O[j - 1], self.lse[j], self.P if m > 0 else None, self.F[k0 + m:], j - m,
-                    self.P if plan[j] else None, self.W[k0 + j], self.G[k0 + j], wl.eps, self.out[k0 + j],
-                    summary_out=summ))
+                    self.P if plan[j] else None, self.W[k0 + j], self.G[k0 + j], wl.eps, self.out[k0 + j]))
                 if plan[j]:
                     m = j
-            if n + 1 < wl.N and wl.S == 1:
+            if n + 1 < wl.N:
                 groups["freeze"].append(lambda n=n, k0=k0, m=m: ar.attnres_block_summary_parts(
                     self.P if m > 0 else None, self.F[k0 + m:], wl.S - m, summary_out=self.Src[n + 1]))
         return groups
@@ -583,7 +579,7 @@ def time_graph(step, steps, warmup, world, stream):
 def time_block_kernels(step, reps, stream):
     """Device time per kernel kind of the Block pass, measured the way the
     step is: each kind's launches of one pass (its stage-1 reads, its merges,
-    its separate freezes, if any) are captured in a CUDA graph of their own and replayed `reps`
+    its freezes) are captured in a CUDA graph of their own and replayed `reps`
     times between CUDA events on the launching stream. Returns ms per pass
     and launches per pass for each kind. The kinds' sum differs from the
     step's own graph time by the overlap of neighbouring launches."""

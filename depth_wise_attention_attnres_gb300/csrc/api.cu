@@ -870,17 +870,17 @@ int attnres_block_pass(const void* F, int64_t f_stride, int32_t N, int32_t S, in
     if (st != ATTNRES_OK) return st;
     // Stage 2: merge each later sublayer's read with its running sum P_j =
     // P_m + f_{k0+m} + ... + f_{k0+j-1}, m the last kept position (0: none).
+    // Each read sees only what a layer-by-layer forward has at that point:
+    // merge j the outputs f_0 .. f_{j-1}, the freeze the block's last output
+    // too. (A merge can also freeze the summary when the caller holds the
+    // next output already, attnres_block_merge_parts' summary_out; a model
+    // makes f_{S-1} from the last merge's result, so the pass does not.)
     int m = 0;
-    const bool freeze = n + 1 < N || freeze_last;
     for (int j = 1; j < S; ++j) {
-      // The block's last merge also freezes its summary b_{n+1} = P_{S-1} +
-      // f_{S-1} into Src[n + 1]: it forms P_{S-1} anyway, so the freeze
-      // reads only f_{S-1} more.
-      void* summary = j == S - 1 && freeze ? Srcb + (n + 1) * src_stride * es : nullptr;
       MergeArgs a{};
       st = make_merge_parts(O[j], lse_scratch + j * T, m > 0 ? P_scratch : nullptr, Fb + (k0 + m) * f_stride * es,
                             f_stride, j - m, plan[j] ? P_scratch : nullptr, W + (k0 + j) * d, Gamma + (k0 + j) * d,
-                            eps, T, d, dtype, outb + (k0 + j) * out_stride * es, summary, &a);
+                            eps, T, d, dtype, outb + (k0 + j) * out_stride * es, nullptr, &a);
       if (st != ATTNRES_OK) return st;
       // The merge before this one writes neither O[j] nor any output f;
       // stage 1 (before merge 1) writes O[j].
@@ -889,9 +889,8 @@ int attnres_block_pass(const void* F, int64_t f_stride, int32_t N, int32_t S, in
       if (st != ATTNRES_OK) return st;
       if (plan[j]) m = j;
     }
-    // With one sublayer a block has no merge: freeze its summary b_{n+1} = f
-    // into Src[n + 1] here.
-    if (freeze && S == 1) {
+    // Freeze the block summary b_{n+1} = P_S into Src[n + 1].
+    if (n + 1 < N || freeze_last) {
       st = attnres_block_summary_parts(m > 0 ? P_scratch : nullptr, Fb + (k0 + m) * f_stride * es, f_stride, S - m,
                                        nullptr, Srcb + (n + 1) * src_stride * es, T, d, dtype, stream);
       if (st != ATTNRES_OK) return st;

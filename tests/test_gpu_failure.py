@@ -77,9 +77,8 @@ def test_injected_failure_stops_a_block_pass(oracle_mod):
     lse = torch.empty(S, T, device=dev())
     P = torch.empty(T, d, device=dev())
     out = torch.full((N * S, T, d), float("nan"), device=dev(), dtype=torch.bfloat16)
-    # Block 0 makes 3 launches (stage 1 and 2 merges, the last also freezing its
-    # summary); block 1's stage 1 fails.
-    ar.attnres_test_fail_launch(3)
+    # Block 0 makes 4 launches (stage 1, 2 merges, freeze); block 1's stage 1 fails.
+    ar.attnres_test_fail_launch(4)
     with pytest.raises(ar.AttnResError) as ei:
         ar.attnres_block_pass(F, N, S, W, G, 1e-6, Src, O, lse, P, out)
     assert ei.value.status == CUDA_ERR
