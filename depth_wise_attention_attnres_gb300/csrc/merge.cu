@@ -82,7 +82,10 @@ inline MergeGeom merge_geom(int d, int es, bool pre, int nparts, bool with_base)
 // Q = 4-feature chunks per lane (a warp covers at most 128 * Q features).
 // kPre: also write the sublayer pre-norm of the merged row (a separate
 // instance, so the plain merge keeps its own code).
-template <typename T, int Q, bool kPre>
+// kSum: also write the block summary (a.summary; a separate instance, so the
+// plain merge keeps its own code: a run-time test cost merge 1 at 131072 x
+// 2048 246 -> 262 us).
+template <typename T, int Q, bool kPre, bool kSum>
 __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, MergeGeom g) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem);
@@ -97,7 +100,7 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
   const uint32_t row_t = static_cast<uint32_t>(d) * sizeof(T);
   const uint32_t row_p = static_cast<uint32_t>(d) * 4u;
   const int np = a.nparts;
-  const int nx = a.summary ? 1 : 0;  // the part after the running sum's, for the summary
+  constexpr int nx = kSum ? 1 : 0;  // the part after the running sum's, for the summary
   const bool with_p = a.P != nullptr;
   // Stage layout: O rows, then each part's rows (the summary's extra part
   // last), then P rows.
@@ -252,7 +255,7 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
             p[q][0] += f[0]; p[q][1] += f[1]; p[q][2] += f[2]; p[q][3] += f[3];
           }
           if (a.P_out) st4(a.P_out + row * d + k, p[q]);
-          if (nx) store_summary(k, p[q]);
+          if constexpr (kSum) store_summary(k, p[q]);
           const float4 w4 = *reinterpret_cast<const float4*>(wq + k);
           ss = fmaf(p[q][0], p[q][0], ss); ss = fmaf(p[q][1], p[q][1], ss);
           ss = fmaf(p[q][2], p[q][2], ss); ss = fmaf(p[q][3], p[q][3], ss);
@@ -294,7 +297,7 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
         const int k = kbeg + (q * 32 + lane) * 4;
         if (k < kend) {
           if (a.P_out) st4(a.P_out + row * d + k, p[q]);
-          if (nx) store_summary(k, p[q]);
+          if constexpr (kSum) store_summary(k, p[q]);
           const float4 w4 = *reinterpret_cast<const float4*>(wq + k);
           ss = fmaf(p[q][0], p[q][0], ss); ss1 = fmaf(p[q][1], p[q][1], ss1);
           ss = fmaf(p[q][2], p[q][2], ss); ss1 = fmaf(p[q][3], p[q][3], ss1);
@@ -570,7 +573,8 @@ bool accum_fast_ok(const AccumArgs& a) {
 namespace {
 template <typename T, int Q>
 cudaError_t launch_merge_tiles(const MergeArgs& a, const MergeGeom& g, cudaStream_t s) {
-  auto k = a.pre.gamma ? merge_tile_kernel<T, Q, true> : merge_tile_kernel<T, Q, false>;
+  auto k = a.pre.gamma ? merge_tile_kernel<T, Q, true, false>
+                       : (a.summary ? merge_tile_kernel<T, Q, false, true> : merge_tile_kernel<T, Q, false, false>);
   cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(k), g.total);
   if (e != cudaSuccess) return e;
   int64_t grid = (a.T + g.TM - 1) / g.TM;
