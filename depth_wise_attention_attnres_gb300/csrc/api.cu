@@ -883,16 +883,24 @@ int attnres_block_pass(const void* F, int64_t f_stride, int32_t N, int32_t S, in
                             eps, T, d, dtype, outb + (k0 + j) * out_stride * es, nullptr, &a);
       if (st != ATTNRES_OK) return st;
       // The merge before this one writes neither O[j] nor any output f;
-      // stage 1 (before merge 1) writes O[j].
-      a.early = j >= 2;
+      // stage 1 (before merge 1) writes O[j] but no output f.
+      a.early = j >= 2 ? 1 : 2;
       st = launched([&] { return launch_merge(a, as_stream(stream), merge_fast_ok(a)); });
       if (st != ATTNRES_OK) return st;
       if (plan[j]) m = j;
     }
-    // Freeze the block summary b_{n+1} = P_S into Src[n + 1].
+    // Freeze the block summary b_{n+1} = P_S into Src[n + 1]. After a merge it
+    // reads the outputs and a kept sum from before that merge, and the merge
+    // neither writes those nor reads Src[n + 1]; it lets the freeze start only
+    // once it has waited for the kernel before it. So the freeze need not
+    // wait, unless the last merge kept the sum it reads.
     if (n + 1 < N || freeze_last) {
-      st = attnres_block_summary_parts(m > 0 ? P_scratch : nullptr, Fb + (k0 + m) * f_stride * es, f_stride, S - m,
-                                       nullptr, Srcb + (n + 1) * src_stride * es, T, d, dtype, stream);
+      AccumArgs a{};
+      st = make_accum_parts(m > 0 ? P_scratch : nullptr, Fb + (k0 + m) * f_stride * es, f_stride, S - m, nullptr,
+                            Srcb + (n + 1) * src_stride * es, T, d, dtype, &a);
+      if (st != ATTNRES_OK) return st;
+      a.no_wait = S > 1 && !plan[S - 1];
+      st = launched([&] { return launch_accum(a, as_stream(stream), accum_fast_ok(a)); });
       if (st != ATTNRES_OK) return st;
     }
   }

@@ -89,7 +89,7 @@ struct MergeArgs {
   PreNorm pre;
   // Fetch the first tiles of O_j and the parts before waiting for the previous
   // kernel: only when that kernel writes none of them (in a Block pass, the
-  // merge before, never stage 1, which writes O_j).
+  // merge before). 2: the parts only (after stage 1, which writes O_j).
   int early;
   int64_t withhold = -1;  // test hook of the tiled merge (as FullArgs)
   // Also store round(running sum + parts[nparts]) here:
@@ -151,6 +151,10 @@ struct AccumArgs {
   int64_t T;
   int d;
   int bf16;
+  // Skip the wait for the previous kernel: only when no kernel that may still
+  // be running writes what this one reads or reads what it writes (in a Block
+  // pass, the freeze after the block's last merge).
+  int no_wait = 0;
 };
 
 // Kernel selection (pure functions of the arguments).

@@ -129,15 +129,22 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
     int issued = 0;
     bool ok = true;
     // O_j rows and the parts' rows of tile t into stage st.
-    auto load_inputs = [&](unsigned char* st, int64_t row0, uint32_t rows, uint32_t fb) {
+    auto load_o = [&](unsigned char* st, int64_t row0, uint32_t rows, uint32_t fb) {
       bulk_g2s(smem_u32(st), static_cast<const T*>(a.O) + row0 * d, rows * row_t, fb);
+    };
+    auto load_parts = [&](unsigned char* st, int64_t row0, uint32_t rows, uint32_t fb) {
       for (int u = 0; u < np + nx; ++u)
         bulk_g2s(smem_u32(st + static_cast<uint32_t>(1 + u) * TM * row_t),
                  static_cast<const T*>(a.parts) + u * a.part_stride + row0 * d, rows * row_t, fb);
     };
-    // With a.early the first stages' O_j and part rows (which no kernel still
-    // running writes) are fetched before the previous kernel has finished;
-    // their P rows, which it may write, after.
+    auto load_inputs = [&](unsigned char* st, int64_t row0, uint32_t rows, uint32_t fb) {
+      load_o(st, row0, rows, fb);
+      load_parts(st, row0, rows, fb);
+    };
+    // With a.early the first stages' rows that no kernel still running writes
+    // are fetched before the previous kernel has finished: the parts, and
+    // O_j unless a.early == 2 (the kernel before is the stage 1 that writes
+    // it); O_j then and the P rows, which it may write, after.
     const int nst = g.nst;
     const int t_pre = a.early ? min(nst, ntiles) : 0;
     for (int t = 0; t < t_pre; ++t) {
@@ -146,7 +153,10 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
       unsigned char* st = stages + static_cast<size_t>(t) * g.stage_bytes;
       const uint32_t fb = smem_u32(&full_bar[t]);
       mbar_arrive_expect_tx(fb, rows * tx_row);
-      load_inputs(st, row0, rows, fb);
+      if (a.early == 2)
+        load_parts(st, row0, rows, fb);
+      else
+        load_inputs(st, row0, rows, fb);
     }
     pdl_wait();
     pdl_trigger();
@@ -154,6 +164,7 @@ __global__ void __launch_bounds__(kMThreads, 2) merge_tile_kernel(MergeArgs a, M
       const int64_t row0 = r0 + static_cast<int64_t>(t) * R / ntiles;
       const uint32_t rows = static_cast<uint32_t>(r0 + static_cast<int64_t>(t + 1) * R / ntiles - row0);
       unsigned char* st = stages + static_cast<size_t>(t) * g.stage_bytes;
+      if (a.early == 2) load_o(st, row0, rows, smem_u32(&full_bar[t]));
       if (with_p) bulk_g2s(smem_u32(st + p_off), a.P + row0 * d, rows * row_p, smem_u32(&full_bar[t]));
     }
     issued = t_pre;
@@ -502,7 +513,7 @@ __global__ void __launch_bounds__(kBlock) rmsnorm_kernel(const T* x, int64_t nto
 template <typename T>
 __global__ void __launch_bounds__(kBlock) accum_fast_kernel(AccumArgs a, int64_t nchunks) {
   pdl_trigger();
-  pdl_wait();
+  if (!a.no_wait) pdl_wait();
   const T* f = static_cast<const T*>(a.parts);
   for (int64_t c = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x; c < nchunks;
        c += static_cast<int64_t>(gridDim.x) * kBlock) {
