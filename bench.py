@@ -259,14 +259,14 @@ NCU_TRAFFIC = {("full_fwd_bulk_kernel", "664fdb90f174cfdb"): (30289.201664 + 103
 # tokens (profiles/block_pass_kernels_8x6x131072x2048_bf16.md).
 NCU_TRAFFIC_BLOCK = {
     ("stage1_tc_kernel", "424235d9916c799e"): {
-        "block_pass_8x6x131072x2048_bf16": (1144.3 + 1357.1) / 2820.1,
-        "block_pass_8x8x16384x1024_bf16": (1143.3 + 1870.9) / 3359.6},
-    ("merge_tile_kernel", "2482544618419e37"): {
-        "block_pass_8x6x131072x2048_bf16": (4668.6 + 2072.2) / 6712.2,
-        "block_pass_8x8x16384x1024_bf16": (6995.8 + 3134.0) / 10204.2},
-    ("accum_fast_kernel", "2482544618419e37"): {
-        "block_pass_8x6x131072x2048_bf16": (839.2 + 286.9) / 1174.4,
-        "block_pass_8x8x16384x1024_bf16": (839.8 + 303.3) / 1174.4},
+        "block_pass_8x6x131072x2048_bf16": (1144.0 + 1357.6) / 2820.1,
+        "block_pass_8x8x16384x1024_bf16": (1143.2 + 1871.4) / 3359.6},
+    ("merge_tile_kernel", "0eb18c612a846d80"): {
+        "block_pass_8x6x131072x2048_bf16": (4676.6 + 2071.9) / 6712.2,
+        "block_pass_8x8x16384x1024_bf16": (7003.8 + 3135.3) / 10204.2},
+    ("accum_fast_kernel", "0eb18c612a846d80"): {
+        "block_pass_8x6x131072x2048_bf16": (838.3 + 289.7) / 1174.4,
+        "block_pass_8x8x16384x1024_bf16": (838.7 + 303.9) / 1174.4},
 }
 
 KERNEL_FILES = {"full_fwd_bulk_kernel": "full_fwd.cu", "full_bwd_bulk_kernel": "full_bwd.cu",
