@@ -1,6 +1,6 @@
 // C ABI of the AttnRes aggregation library: argument checks, kernel choice,
 // pass sequencing and device status. Every computation runs in the kernels of
-// full_fwd.cu, stage1.cu, merge.cu and generic.cu.
+// the other .cu files.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -17,7 +17,10 @@ namespace attnres {
 
 namespace {
 std::mutex g_mu;
-std::map<std::pair<const void*, int>, int> g_smem_set;            // (kernel, device) -> bytes
+// (kernel, context) -> dynamic shared memory bytes allowed. A kernel's
+// attributes belong to a context: a device reset makes a new one, which must
+// be set up again.
+std::map<std::pair<const void*, unsigned long long>, int> g_smem_set;
 std::map<std::tuple<const void*, int, int, int>, int> g_occ;      // (kernel, dev, thr, smem)
 std::map<int, int> g_sms;
 
@@ -25,6 +28,33 @@ int current_device() {
   int dev = 0;
   cudaGetDevice(&dev);
   return dev;
+}
+
+// Process-unique id of the current context (cuCtxGetId), or, when there is
+// none yet or the driver cannot say, the device number with the top bit set.
+// Two driver queries, no synchronisation (also fine inside stream capture).
+unsigned long long current_context_key() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    cudaGetLastError();
+  });
+  const unsigned long long fallback = (1ull << 63) | static_cast<unsigned long long>(current_device());
+  if (!get_current || !get_id) return fallback;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return fallback;
+  return id;
 }
 }  // namespace
 
@@ -41,11 +71,11 @@ int sm_count() {
 
 // Lets `kernel` use `bytes` of dynamic shared memory and asks for the largest
 // shared-memory carveout, so that the CTAs the occupancy allows fit. Done
-// once per (kernel, device); later calls only look the answer up.
+// once per (kernel, context); later calls only look the answer up.
 cudaError_t allow_dynamic_smem(const void* kernel, int bytes) {
-  const int dev = current_device();
+  const unsigned long long ctx = current_context_key();
   std::lock_guard<std::mutex> lk(g_mu);
-  auto key = std::make_pair(kernel, dev);
+  auto key = std::make_pair(kernel, ctx);
   auto it = g_smem_set.find(key);
   if (it != g_smem_set.end() && it->second >= bytes) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
